@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""Throughput of the MoE layer forward pass on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config dsv3] [--impl ours|reference]
+
+One step = one pass of the whole layer (route -> permute -> grouped gate/up GEMM
++ SwiGLU -> grouped down GEMM x gate weight -> combine) over one batch of
+synthetic tokens, through the library's C ABI (moe_forward).  Inputs and
+weights are resident in HBM before the timed region; they are larger than L2
+(x 235 MB and 22.6 GB of expert weights at the DeepSeek-V3 shape), so no L2
+flush is needed between steps.  Prints ONE JSON line on rank 0.
+
+--impl reference times the CPU oracle (the fp64 definition of the layer) on a
+bounded sample of the same workload per step, on the host cores.
+
+Under torchrun (--gpus N > 1) every rank runs an independent replica of the
+whole workload on its own GPU (the layer has no exchange step here): weak
+scaling, value = tokens of all ranks / slowest rank's time.
+"""
+from __future__ import annotations
+
+import os
+
+# The oracle baseline runs single-threaded; set before numpy loads its BLAS.
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import tempfile  # noqa: E402
+import time  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workload as wl  # noqa: E402
+
+METRIC = "MoE-layer prefill tokens/s and TFLOP/s (% of GB300 tensor peak), 1 GPU"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def dist_init(backend: str):
+    rank, world, _ = dist_info()
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+    return rank, world
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v: float, device=None) -> float:
+    """Largest value of v over all ranks (v itself without a process group)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(v)
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.proc = None
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        try:
+            for ln in open(self.path):
+                p = [x.strip() for x in ln.split(",")]
+                if len(p) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(p[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + p[0].split(".")[1]) if "." in p[0] else 0.0
+                    rows.append((ts, float(p[2]), float(p[3]), p[6:10]))
+                except Exception:
+                    continue
+        except Exception:
+            return None
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 - 0.06 <= r[0] <= t1 + 0.06] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside)}
+
+
+# ------------------------------------------------------------------ helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "moe_expert_layer_router_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None when
+    the summary is missing or was taken on other kernel sources."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_ncu.md")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    for ln in open(p):
+        if ln.startswith("- ") and ":" in ln:
+            k, _, v = ln[2:].partition(":")
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def describe(lc) -> str:
+    s = (f"{lc.name}: T={lc.T} H={lc.H} E={lc.E} top-{lc.k} I={lc.I} {lc.score}"
+         f"{' x' + str(lc.route_scale) if lc.route_scale != 1.0 else ''}")
+    if lc.I_shared:
+        s += f" + shared I={lc.I_shared}"
+    if lc.zipf_bias:
+        s += " + Zipf(1.2) router bias"
+    return s + f", {lc.wtype}"
+
+
+class Layer:
+    """Seeded layer on one device; every expert matrix in its own allocation."""
+
+    def __init__(self, lc, dev):
+        import moe_expert_layer_router_gb300 as m
+        self.lc = lc
+        self.x = wl.gen_x(lc, dev)
+        self.wr = wl.gen_router(lc, dev)
+        b = wl.gen_bias(lc)
+        self.bias = b.to(dev) if b is not None else None
+        self.W = [tuple(wl.gen_expert(lc, e, w, dev) for w in ("gate", "up", "down"))
+                  for e in range(lc.E)]
+        self.S = (tuple(wl.gen_shared(lc, w, dev) for w in ("gate", "up", "down"))
+                  if lc.I_shared else None)
+        self.cfg = m.config_from(lc)
+        self.weights = m.ExpertWeights(self.cfg, [w[0] for w in self.W], [w[1] for w in self.W],
+                                       [w[2] for w in self.W], shared=self.S)
+
+
+# ------------------------------------------------------------------ oracle baseline
+def oracle_sample(lc, layer, tokens):
+    """Time the CPU oracle on `tokens` of the workload; returns (seconds, n)."""
+    from oracle import moe as om
+    idx = torch.tensor(tokens, device=layer.x.device)
+    x = layer.x[idx].cpu()
+    wr = layer.wr.cpu()
+    b = None if layer.bias is None else layer.bias.cpu()
+    # the weights the sample needs, moved to host memory outside the timing
+    lg = om.router_logits(x, wr, b)
+    need = sorted(set(om.select_topk(lg, lc.k).reshape(-1).tolist()))
+    host = {e: tuple(t.cpu() for t in layer.W[e]) for e in need}
+    sh = tuple(t.cpu() for t in layer.S) if layer.S is not None else None
+    t0 = time.perf_counter()
+    om.moe_layer(x, wr, b, lambda e: host[e], sh, lc.k, lc.score, lc.renormalize, lc.route_scale)
+    return time.perf_counter() - t0, len(tokens)
+
+
+def cpu_baseline(lc, layer, n_tokens=8):
+    g = np.random.default_rng(1)
+    tokens = sorted(g.choice(lc.T, size=n_tokens, replace=False).tolist())
+    secs, n = oracle_sample(lc, layer, tokens)
+    return {"value": n / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} tokens of the {lc.name} workload through the fp64 oracle "
+                      f"(routing, permutation, grouped experts, combine), {secs:.1f} s, "
+                      f"1 thread"}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, lc, rank, world, dev):
+    import moe_expert_layer_router_gb300 as m
+    from moe_expert_layer_router_gb300 import _native as N
+
+    layer = Layer(lc, dev)
+    cfg = layer.cfg
+    ws = m.Workspace(cfg, "forward", dev)
+    out = torch.empty(lc.T, lc.H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        m.moe_forward(cfg, layer.weights, layer.x, layer.wr, layer.bias, out=out, ws=ws,
+                      stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    m.moe_get_device_error(ws)
+
+    # kernel trace: one event before every kernel and one after the last, per step
+    per_step = 16
+    cap = per_step * args.steps
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(cap)]
+    for e in evs:
+        e.record(stream)      # creates the CUDA event on this device
+    torch.cuda.synchronize(dev)
+    ev_arr = (N.C.c_void_p * cap)(*[e.cuda_event for e in evs])
+    kid = (N.C.c_int32 * cap)()
+    trace = N.MoeTrace(N.C.cast(ev_arr, N.C.POINTER(N.C.c_void_p)),
+                       N.C.cast(kid, N.C.POINTER(N.C.c_int32)), cap, 0)
+
+    clocks = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    time.sleep(0.3 if clocks else 0)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    N.check(N.lib().moe_set_trace(N.C.byref(trace)), "moe_set_trace")
+    w0 = time.time()
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    w1 = time.time()
+    N.lib().moe_set_trace(None)
+    barrier()
+    ms_local = start.elapsed_time(end) / args.steps
+    m.moe_get_device_error(ws)
+
+    # per-kernel durations from the trace
+    per_kernel = {}
+    launches = 0
+    for i in range(trace.count - 1):
+        k = kid[i]
+        if k < 0:
+            continue
+        launches += 1
+        per_kernel.setdefault(N.KERNEL_NAMES[k], []).append(evs[i].elapsed_time(evs[i + 1]))
+    kernels_ms = {k: sum(v) / len(v) for k, v in per_kernel.items()}
+
+    # end to end through the public call with host buffers (pinned), copies included
+    x_host = layer.x.cpu().pin_memory()
+    out_host = torch.empty(lc.T, lc.H, dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(layer.x)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        m.moe_forward(cfg, layer.weights, x_dev, layer.wr, layer.bias, out=out, ws=ws,
+                      stream=stream)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e2.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms_local = s2.elapsed_time(e2) / args.steps
+    barrier()
+    if clocks:
+        clocks.stop()
+
+    ms = max_over_ranks(ms_local, dev)
+    e2e_ms = max_over_ranks(e2e_ms_local, dev)
+    if rank != 0:
+        return None
+
+    peaks, peak_src = load_peaks()
+    tokens = lc.T * world
+    flops = lc.flops()
+    tflops = flops * world / (ms * 1e-3) / 1e12
+    g1_ms = kernels_ms.get("gemm1_gate_up_swiglu")
+    g1_flops = 4.0 * lc.R * lc.H * lc.I + 4.0 * lc.T * lc.H * lc.I_shared
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    g1_tf = g1_flops / (g1_ms * 1e-3) / 1e12 if g1_ms else None
+    res = {
+        "metric": METRIC,
+        "value": tokens / (ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator; x ~N(0,1), weights ~N(0,0.02))",
+        "config": {"workload": describe(lc), "tokens_per_gpu": lc.T,
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (x, 22.6 GB of expert weights); no flush"},
+        "tflops": tflops,
+        "pct_of_peak": {"bf16_burst": 100 * tflops / world / float(peaks.get("bf16_tflops", 1900.0)),
+                        "bf16_sustained": 100 * tflops / world / peak, "source": peak_src},
+        "kernels_ms": {k: round(v, 4) for k, v in sorted(kernels_ms.items(),
+                                                           key=lambda kv: -kv[1])},
+        "roofline": {"kernel": "gemm1_gate_up_swiglu", "bound": "tensor",
+                     "achieved": g1_tf, "peak": peak, "unit": "TFLOP/s",
+                     "frac": (g1_tf / peak) if g1_tf else None,
+                     "peak_kind": f"bf16 sustained, of {peak_src}",
+                     "algorithmic_flop_per_launch": g1_flops,
+                     "traffic": recorded_traffic("gemm1_gate_up_swiglu", lc.name)},
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": layer.x.numel() * 2, "d2h_bytes_per_step": out.numel() * 2},
+        "gpu_launches": launches,
+        "clocks": clocks.summary(w0, w1) if clocks else None,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(lc, layer, args.cpu_tokens)
+    return res
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, lc, rank, world, dev):
+    if rank != 0:
+        return None
+    layer_dev = dev if torch.cuda.is_available() else torch.device("cpu")
+
+    class HostLayer:  # inputs only; the oracle needs no descriptor table
+        pass
+
+    L = HostLayer()
+    L.x = wl.gen_x(lc, layer_dev)
+    L.wr = wl.gen_router(lc, layer_dev)
+    b = wl.gen_bias(lc)
+    L.bias = b.to(layer_dev) if b is not None else None
+    L.W = [tuple(wl.gen_expert(lc, e, w, layer_dev) for w in ("gate", "up", "down"))
+           for e in range(lc.E)]
+    L.S = (tuple(wl.gen_shared(lc, w, layer_dev) for w in ("gate", "up", "down"))
+           if lc.I_shared else None)
+    g = np.random.default_rng(2)
+    per = args.ref_tokens
+    times, n_tok = [], 0
+    for i in range(args.warmup + args.steps):
+        toks = sorted(g.choice(lc.T, size=per, replace=False).tolist())
+        s, n = oracle_sample(lc, L, toks)
+        if i >= args.warmup:
+            times.append(s)
+            n_tok += n
+    total = sum(times)
+    v = n_tok / total
+    return {"metric": METRIC, "impl": "reference", "value": v, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / len(times), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": describe(lc), "tokens_per_step": per},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{per} random tokens of the workload per step through "
+                                       f"the fp64 oracle, 1 thread"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="dsv3", choices=sorted(wl.CONFIGS))
+    ap.add_argument("--cpu-tokens", type=int, default=8)
+    ap.add_argument("--ref-tokens", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    lc = wl.CONFIGS[args.config]
+    rank, world, local = dist_info()
+    if world > 1:
+        torch.cuda.set_device(local)
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    rank, world = dist_init("nccl" if torch.cuda.is_available() else "gloo")
+    if args.impl == "reference":
+        res = run_reference(args, lc, rank, world, dev)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+        import moe_expert_layer_router_gb300.build as b
+        b.build()
+        torch.cuda.set_device(dev)
+        res = run_ours(args, lc, rank, world, dev)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,285 @@
+/*
+ * moe_layer.h -- C ABI of a single-GPU Mixture-of-Experts FFN layer forward
+ * pass over a prefill token batch, for NVIDIA GB300 (sm_103a).
+ *
+ * The layer (gated routing + expert computation, "Memory-Compute
+ * Disaggregation for Large-Model Inference: AFD Architecture Analysis and
+ * Performance Validation", section 3, Data-Flow Closed Loop step 3):
+ *   1. router logits l = x W_r^T (+ bias), top-k experts per token, gate weights
+ *   2. per-expert token histogram and a permutation grouping rows by expert
+ *   3. grouped GEMM over each expert's W_gate / W_up with fused SwiGLU
+ *   4. grouped down projection W_down, each row scaled by its gate weight
+ *   5. combine back to token order (plus the always-on shared expert)
+ * The grouped GEMMs take hidden states as the left operand and the layer's
+ * expert weights as the right operand ("ASAP: A DiSaggregated and
+ * Asynchronous Inference System for MoE Prefill", section 3.4.2), and read
+ * every expert's weights from its own allocation through a per-expert
+ * pointer list, with no merge copy ("DWDP: Distributed Weight Data
+ * Parallelism for High-Performance LLM Inference on NVL72", section 4.2).
+ *
+ * Conventions for every call
+ *   - Pointers named x, w_*, out, ... are DEVICE pointers into memory the
+ *     caller owns (the library never frees them).  Arrays "of device
+ *     pointers" are HOST arrays.  All matrices are row-major and dense.
+ *   - bf16 matrices and every buffer read by TMA must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream): they enqueue kernels and return.  None synchronises
+ *     or copies device->host, except moe_get_device_error and
+ *     moe_weights_create / moe_weights_destroy.
+ *   - Arguments are validated on the host BEFORE anything is enqueued; a
+ *     failed check returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED /
+ *     MOE_ERR_WORKSPACE with nothing launched, and moe_last_error_message()
+ *     describes it.  No C++ exception crosses this boundary.
+ *   - Device-side checks (an expert id outside [0,E), a row index outside
+ *     [0,T*k), a bounded wait that expired) never trap: they set bits of a
+ *     sticky status word at the start of the caller's workspace, skip the
+ *     offending access and let the kernel finish.  moe_get_device_error()
+ *     reads and clears that word.
+ *   - Workspace: caller-allocated device memory of at least
+ *     moe_workspace_size() bytes, 256-byte aligned, initialised once with
+ *     moe_workspace_init().  Calls on one workspace must not overlap in time
+ *     (use one stream per workspace).
+ *   - The current CUDA device must be the one holding every pointer.
+ */
+#ifndef MOE_LAYER_H_
+#define MOE_LAYER_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,    /* null / misaligned pointer, bad size or enum */
+  MOE_ERR_UNSUPPORTED = 2,    /* valid but outside what the kernels handle */
+  MOE_ERR_WORKSPACE = 3,      /* workspace too small or misaligned */
+  MOE_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed */
+  MOE_ERR_DEVICE_TIMEOUT = 5, /* a kernel's bounded wait expired */
+  MOE_ERR_BOUNDS = 6          /* a kernel met an out-of-range index */
+} moe_status_t;
+
+typedef enum moe_score {
+  MOE_SCORE_SOFTMAX = 0,      /* w = softmax over the selected logits (renormalize=1) */
+  MOE_SCORE_SIGMOID = 1       /* w = sigmoid(l) / sum over the selection (renormalize=1) */
+} moe_score_t;
+
+typedef enum moe_dtype {
+  MOE_DTYPE_BF16 = 0,         /* bf16 weights, bf16 x_perm / h, fp32 accumulation */
+  MOE_DTYPE_FP8_E4M3 = 1      /* e4m3 weights with 128x128 fp32 block scales;
+                                 e4m3 activations with 1x128 fp32 group scales */
+} moe_dtype_t;
+
+typedef enum moe_op {
+  MOE_OP_ROUTE = 0,
+  MOE_OP_PERMUTE = 1,
+  MOE_OP_GROUPED_FFN = 2,
+  MOE_OP_COMBINE = 3,
+  MOE_OP_FORWARD = 4
+} moe_op_t;
+
+/* Layer shape and routing rule.
+ *   T          tokens (>= 0; 0 makes every call a no-op); T*k < 2^31
+ *   H          hidden size, multiple of 128, >= 128
+ *   E          routed experts, 1..256
+ *   k          experts per token, 1..min(E, 16)
+ *   I          routed expert intermediate size, multiple of 128
+ *   I_shared   shared expert intermediate size, 0 (none) or multiple of 128
+ *   score      moe_score_t
+ *   renormalize 1: normalise the k selected weights to sum 1; 0: softmax over
+ *              all E (softmax) or the raw sigmoid (sigmoid)
+ *   route_scale multiplies every gate weight (e.g. 2.5), finite and > 0
+ *   wtype      moe_dtype_t of the expert weights */
+typedef struct moe_config {
+  int64_t T;
+  int32_t H;
+  int32_t E;
+  int32_t k;
+  int32_t I;
+  int32_t I_shared;
+  int32_t score;
+  int32_t renormalize;
+  float route_scale;
+  int32_t wtype;
+} moe_config_t;
+
+/* Per-expert weight pointer list (DWDP section 4.2: a list of separately
+ * allocated weight buffers instead of one contiguous tensor).  Every pointer
+ * is a device pointer, 16-byte aligned; the arrays themselves are host arrays
+ * of length E.
+ *   gate[e], up[e]  [I, H]      down[e] [H, I]        (bf16, or e4m3 bytes)
+ *   *_scales[e]     fp8 only: fp32 block scales, gate/up [I/128, H/128],
+ *                   down [H/128, I/128]; NULL arrays for bf16
+ *   shared_*        the shared expert ([I_shared, H] / [H, I_shared]) and its
+ *                   scales; NULL when I_shared == 0 */
+typedef struct moe_weight_list {
+  const void* const* gate;
+  const void* const* up;
+  const void* const* down;
+  const float* const* gate_scales;
+  const float* const* up_scales;
+  const float* const* down_scales;
+  const void* shared_gate;
+  const void* shared_up;
+  const void* shared_down;
+  const float* shared_gate_scales;
+  const float* shared_up_scales;
+  const float* shared_down_scales;
+} moe_weight_list_t;
+
+typedef struct moe_weights* moe_weights_t;
+
+/* Builds the device-side expert table: one TMA tensor descriptor per expert
+ * matrix plus pointer arrays, in one small device allocation owned by the
+ * returned handle.  The weights themselves are neither copied nor owned and
+ * must stay valid while the handle is used.  Synchronous (one host->device
+ * copy).  Errors: MOE_ERR_INVALID_ARG (null/misaligned pointer, bad config),
+ * MOE_ERR_CUDA. */
+MOE_API moe_status_t moe_weights_create(const moe_config_t* cfg, const moe_weight_list_t* weights,
+                                moe_weights_t* out);
+/* Frees the handle's device table (synchronises the device first).  NULL is a no-op. */
+MOE_API void moe_weights_destroy(moe_weights_t weights);
+
+/* Bytes of workspace that `op` needs for `cfg` (always a multiple of 256). */
+MOE_API moe_status_t moe_workspace_size(const moe_config_t* cfg, int32_t op, size_t* bytes);
+
+/* Zeroes the workspace's status header (asynchronous).  Call once after allocating. */
+MOE_API moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Step 1 -- routing (AFD write-up section 3, "gated routing"; ASAP section
+ * 5.1, 8 of 256 experts per token).
+ *   x          bf16 [T, H]
+ *   w_router   bf16 [E, H]
+ *   logit_bias fp32 [E] added to every token's logits, or NULL
+ *   topk_ids   int32 [T, k] out: selected experts in descending logit order,
+ *              exact ties to the lower index
+ *   topk_w     fp32 [T, k] out: gate weights (see moe_config_t)
+ *   logits_out fp32 [T, E] out, or NULL: the fp32 logits used for selection
+ * Logits accumulate in fp32 on the tensor cores. */
+MOE_API moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_router,
+                       const float* logit_bias, int32_t* topk_ids, float* topk_w,
+                       float* logits_out, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Step 2 -- histogram and permutation (ASAP table 2: per-expert token counts
+ * of the dispatch metadata).  Deterministic: rows of expert e are
+ * [expert_offsets[e], expert_offsets[e+1]) in ascending token order.
+ *   topk_ids        int32 [T, k] in (each row k distinct ids in [0, E))
+ *   topk_w          fp32 [T, k] in, or NULL
+ *   x               bf16 [T, H] in, or NULL when x_perm is NULL
+ *   expert_counts   int32 [E] out
+ *   expert_offsets  int32 [E+1] out, exclusive prefix sum, [E] = T*k
+ *   perm_token      int32 [T*k] out: row -> token
+ *   inv_row         int32 [T, k] out: (token, slot) -> row
+ *   row_weight      fp32 [T*k] out, or NULL: topk_w in row order (needs topk_w)
+ *   x_perm          [T*k, H] out, or NULL: x[perm_token[r]]; bf16, or e4m3 codes
+ *                   for MOE_DTYPE_FP8_E4M3 (each token quantised once in 1x128
+ *                   groups: s = amax/448, q = rn_satfinite(x/s), in fp32)
+ *   x_perm_scales   fp32 [T*k, H/128] out for fp8, else NULL */
+MOE_API moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, const float* topk_w,
+                         const void* x, int32_t* expert_counts, int32_t* expert_offsets,
+                         int32_t* perm_token, int32_t* inv_row, float* row_weight,
+                         void* x_perm, float* x_perm_scales, void* ws, size_t ws_bytes,
+                         moe_stream_t stream);
+
+/* Steps 3+4 -- grouped expert FFN (ASAP section 3.4.2 grouped matrix
+ * multiplication; DWDP section 4.2 pointer-list weights):
+ *   y_perm[r] = row_weight[r] * W_down[e] (silu(W_gate[e] x_perm[r]) * (W_up[e] x_perm[r]))
+ * for r in expert e's segment, and, when x_shared != NULL and I_shared > 0,
+ *   shared_out[t] = W_sd (silu(W_sg x_shared[t]) * (W_su x_shared[t])).
+ *   x_perm          [T*k, H] bf16 (or e4m3 + x_perm_scales [T*k, H/128])
+ *   expert_offsets  int32 [E+1] (device), as written by moe_permute
+ *   row_weight      fp32 [T*k] or NULL (all ones)
+ *   x_shared        [T, H] bf16 (or e4m3 + x_shared_scales [T, H/128]) or NULL
+ *   y_perm          fp32 [T*k, H] out;  shared_out fp32 [T, H] out or NULL
+ * The intermediate h is rounded to bf16 (e4m3 + 1x128 scales for fp8); the
+ * expert outputs stay fp32 so that each token's rows are rounded only once,
+ * after the combine has summed them. */
+MOE_API moe_status_t moe_grouped_ffn(const moe_config_t* cfg, moe_weights_t weights, const void* x_perm,
+                             const float* x_perm_scales, const int32_t* expert_offsets,
+                             const float* row_weight, const void* x_shared,
+                             const float* x_shared_scales, void* y_perm, void* shared_out,
+                             void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Step 5 -- combine: out[t] = sum_j y_perm[inv_row[t, j]] (+ shared_out[t]),
+ * summed in fp32 in slot order j = 0..k-1, then the shared row, rounded to bf16.
+ *   y_perm fp32 [T*k, H], inv_row int32 [T, k], shared_out fp32 [T, H] or NULL,
+ *   out bf16 [T, H] (must not alias y_perm). */
+MOE_API moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm, const int32_t* inv_row,
+                         const void* shared_out, void* out, void* ws, size_t ws_bytes,
+                         moe_stream_t stream);
+
+/* Steps 1-5 in one call, all intermediates in the workspace.
+ *   x bf16 [T, H], w_router bf16 [E, H], logit_bias fp32 [E] or NULL,
+ *   out bf16 [T, H];  topk_ids_out int32 [T, k] / topk_w_out fp32 [T, k]
+ *   optional copies of the routing decision (NULL to skip). */
+MOE_API moe_status_t moe_forward(const moe_config_t* cfg, moe_weights_t weights, const void* x,
+                         const void* w_router, const float* logit_bias, void* out,
+                         int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
+                         moe_stream_t stream);
+
+/* fp8 weight preparation: 128x128 block quantisation of an fp32 [N, K] matrix
+ * (N, K multiples of 128): scales[N/128, K/128] = amax/448 (1 for an all-zero
+ * block), q = e4m3 rn_satfinite(w/s), computed in fp32.  Asynchronous. */
+MOE_API moe_status_t moe_quantize_weight_fp8(const float* w, int64_t N, int64_t K, uint8_t* q,
+                                     float* scales, moe_stream_t stream);
+
+/* fp8 activation quantisation of a bf16 [M, K] matrix (K multiple of 128) in
+ * 1x128 groups: scales[M, K/128], codes q[M, K], same rule as above. */
+MOE_API moe_status_t moe_quantize_act_fp8(const void* x, int64_t M, int64_t K, uint8_t* q, float* scales,
+                                  moe_stream_t stream);
+
+/* Waits for `stream`, reads the workspace's sticky device status word, clears
+ * it and maps it to MOE_OK / MOE_ERR_BOUNDS / MOE_ERR_DEVICE_TIMEOUT.
+ * *device_bits (optional) receives the raw word (bit 0 bounds, bit 1 timeout). */
+MOE_API moe_status_t moe_get_device_error(void* ws, moe_stream_t stream, int32_t* device_bits);
+
+/* Kernel tracing.  While a trace is set on the calling thread, every call
+ * records one of the caller's CUDA events on its stream before each kernel it
+ * launches (kernel_ids[i] = the moe_kernel_t that follows events[i]) and one
+ * after the last (kernel_ids[i] = -1), so consecutive events bracket each
+ * kernel.  Recording stops silently when `capacity` is reached; `count` is
+ * advanced by the library.  The events must be created by the caller
+ * (cudaEventCreate) on the current device.  NULL clears the trace. */
+typedef enum moe_kernel {
+  MOE_K_ROUTER = 0,
+  MOE_K_HIST = 1,
+  MOE_K_SCAN = 2,
+  MOE_K_SCATTER = 3,
+  MOE_K_PLAN = 4,
+  MOE_K_GEMM1 = 5,   /* grouped gate/up GEMM + SwiGLU */
+  MOE_K_GEMM2 = 6,   /* grouped down GEMM x gate weight */
+  MOE_K_COMBINE = 7,
+  MOE_K_QUANT = 8,
+  MOE_K_COUNT = 9
+} moe_kernel_t;
+
+typedef struct moe_trace {
+  void** events;       /* cudaEvent_t[capacity] */
+  int32_t* kernel_ids; /* int32[capacity], written by the library */
+  int32_t capacity;
+  int32_t count;
+} moe_trace_t;
+
+MOE_API moe_status_t moe_set_trace(moe_trace_t* trace);
+
+MOE_API const char* moe_status_string(moe_status_t status);
+/* Text of the last host-side failure on the calling thread ("" if none). */
+MOE_API const char* moe_last_error_message(void);
+MOE_API int32_t moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_LAYER_H_ */

@@ -1,0 +1,674 @@
+// Host side of the C ABI declared in include/moe_layer.h: argument validation,
+// workspace layout, TMA descriptor encoding and the launch sequence of each
+// step.  Everything here runs on the host; every step of the layer runs in
+// the kernels of router.cu, permute.cu, grouped_gemm.cu and combine.cu.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/moe_layer.h"
+#include "moe_internal.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ errors
+static thread_local std::string g_last_error;
+
+static moe_status_t fail(moe_status_t s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+static moe_status_t cuda_fail(cudaError_t e, const char* where) {
+  return fail(MOE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+#define MOE_CUDA(call)                                   \
+  do {                                                   \
+    cudaError_t e_ = (call);                             \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call);  \
+  } while (0)
+
+// ------------------------------------------------------------------ device info
+static int current_device() {
+  int d = 0;
+  cudaGetDevice(&d);
+  return d;
+}
+
+static int sm_count() {
+  static std::mutex mu;
+  static std::unordered_map<int, int> cache;
+  const int d = current_device();
+  std::lock_guard<std::mutex> g(mu);
+  auto it = cache.find(d);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || n <= 0) n = 1;
+  cache[d] = n;
+  return n;
+}
+
+cudaError_t ensure_smem_attr(const void* func, int bytes) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, uint64_t> done;  // device bitmask per kernel
+  const int d = current_device();
+  const uint64_t bit = d < 64 ? (uint64_t(1) << d) : 0;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (bit && (done[func] & bit)) return cudaSuccess;
+  }
+  cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> g(mu);
+  done[func] |= bit;
+  return cudaSuccess;
+}
+
+// ------------------------------------------------------------------ tracing
+static thread_local moe_trace_t* g_trace = nullptr;
+
+void trace_mark(cudaStream_t stream, int id) {
+  moe_trace_t* t = g_trace;
+  if (!t || t->count >= t->capacity) return;
+  if (cudaEventRecord(static_cast<cudaEvent_t>(t->events[t->count]), stream) != cudaSuccess) return;
+  t->kernel_ids[t->count] = id;
+  t->count += 1;
+}
+
+// ------------------------------------------------------------------ TMA descriptors
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Row-major [rows, inner] matrix, 128-byte swizzled boxes of box_rows x box_inner.
+static moe_status_t encode_2d(CUtensorMap* m, bool bf16, const void* base, uint64_t inner,
+                              uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const uint64_t esz = bf16 ? 2 : 1;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * esz};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a [%llu, %llu] matrix",
+                static_cast<int>(r), static_cast<unsigned long long>(rows),
+                static_cast<unsigned long long>(inner));
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------------ validation
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+static moe_status_t check_config(const moe_config_t* c) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "cfg is NULL");
+  if (c->T < 0) return fail(MOE_ERR_INVALID_ARG, "T = %lld is negative", (long long)c->T);
+  if (c->E < 1 || c->E > kMaxExperts)
+    return fail(MOE_ERR_UNSUPPORTED, "E = %d outside 1..%d", c->E, kMaxExperts);
+  if (c->k < 1 || c->k > c->E || c->k > 16)
+    return fail(MOE_ERR_INVALID_ARG, "k = %d outside 1..min(E, 16)", c->k);
+  if (c->H < 128 || c->H % 128)
+    return fail(MOE_ERR_UNSUPPORTED, "H = %d is not a positive multiple of 128", c->H);
+  if (c->I < 128 || c->I % 128)
+    return fail(MOE_ERR_UNSUPPORTED, "I = %d is not a positive multiple of 128", c->I);
+  if (c->I_shared < 0 || c->I_shared % 128)
+    return fail(MOE_ERR_UNSUPPORTED, "I_shared = %d is not 0 or a multiple of 128", c->I_shared);
+  if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID)
+    return fail(MOE_ERR_INVALID_ARG, "score = %d is not a moe_score_t", c->score);
+  if (c->renormalize != 0 && c->renormalize != 1)
+    return fail(MOE_ERR_INVALID_ARG, "renormalize = %d is not 0 or 1", c->renormalize);
+  if (!std::isfinite(c->route_scale) || c->route_scale <= 0.0f)
+    return fail(MOE_ERR_INVALID_ARG, "route_scale must be finite and > 0");
+  if (c->wtype != MOE_DTYPE_BF16 && c->wtype != MOE_DTYPE_FP8_E4M3)
+    return fail(MOE_ERR_INVALID_ARG, "wtype = %d is not a moe_dtype_t", c->wtype);
+  if (c->T * int64_t(c->k) >= (int64_t(1) << 31))
+    return fail(MOE_ERR_UNSUPPORTED, "T*k = %lld does not fit int32 row indices",
+                (long long)(c->T * c->k));
+  return MOE_OK;
+}
+
+static moe_status_t check_ptr(const void* p, const char* name, bool needs16 = true) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "%s is NULL", name);
+  if (needs16 && !aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  return MOE_OK;
+}
+
+static moe_status_t check_ptr4(const void* p, const char* name) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "%s is NULL", name);
+  if (reinterpret_cast<uintptr_t>(p) & 3) return fail(MOE_ERR_INVALID_ARG, "%s is not 4-byte aligned", name);
+  return MOE_OK;
+}
+
+#define MOE_TRY(expr)                     \
+  do {                                    \
+    moe_status_t s_ = (expr);             \
+    if (s_ != MOE_OK) return s_;          \
+  } while (0)
+
+// ------------------------------------------------------------------ workspace layout
+constexpr size_t kHeaderBytes = 256;
+
+static size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
+
+struct Layout {
+  size_t blk_counts = 0, blk_base = 0;        // permute
+  size_t sched1 = 0, sched2 = 0, h = 0, hs = 0;  // grouped ffn
+  size_t ids = 0, w = 0, counts = 0, offsets = 0, perm_token = 0, inv_row = 0, row_weight = 0,
+         x_perm = 0, y_perm = 0, shared_out = 0;  // forward
+  size_t total = 0;
+};
+
+static Layout layout(const moe_config_t& c, int op) {
+  Layout L;
+  size_t at = kHeaderBytes;
+  auto take = [&](size_t bytes) {
+    const size_t o = at;
+    at += up256(bytes);
+    return o;
+  };
+  const int64_t T = c.T, R = c.T * c.k;
+  const int nblk = static_cast<int>((T + kPermTok - 1) / kPermTok);
+  const int G = c.E + (c.I_shared > 0 ? 1 : 0);
+  const bool perm = op == MOE_OP_PERMUTE || op == MOE_OP_FORWARD;
+  const bool ffn = op == MOE_OP_GROUPED_FFN || op == MOE_OP_FORWARD;
+  if (perm) {
+    L.blk_counts = take(size_t(nblk) * c.E * 4);
+    L.blk_base = take(size_t(nblk) * c.E * 4);
+  }
+  if (ffn) {
+    L.sched1 = take(size_t(sched_ints(G)) * 4);
+    L.sched2 = take(size_t(sched_ints(G)) * 4);
+    L.h = take(size_t(R) * c.I * 2);
+    L.hs = take(size_t(T) * c.I_shared * 2);
+  }
+  if (op == MOE_OP_FORWARD) {
+    L.ids = take(size_t(R) * 4);
+    L.w = take(size_t(R) * 4);
+    L.counts = take(size_t(c.E) * 4);
+    L.offsets = take(size_t(c.E + 1) * 4);
+    L.perm_token = take(size_t(R) * 4);
+    L.inv_row = take(size_t(R) * 4);
+    L.row_weight = take(size_t(R) * 4);
+    L.x_perm = take(size_t(R) * c.H * 2);
+    L.y_perm = take(size_t(R) * c.H * 4);
+    L.shared_out = take(size_t(T) * c.H * 4);
+  }
+  L.total = at;
+  return L;
+}
+
+static moe_status_t check_ws(const moe_config_t& c, int op, const void* ws, size_t bytes) {
+  if (!ws) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) & 255)
+    return fail(MOE_ERR_WORKSPACE, "workspace is not 256-byte aligned");
+  const size_t need = layout(c, op).total;
+  if (bytes < need)
+    return fail(MOE_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", bytes, need);
+  return MOE_OK;
+}
+
+template <typename P>
+static P at(void* ws, size_t off) {
+  return reinterpret_cast<P>(static_cast<uint8_t*>(ws) + off);
+}
+
+static uint32_t* err_word(void* ws) { return static_cast<uint32_t*>(ws); }
+
+}  // namespace moe
+
+// ======================================================================== weights
+struct moe_weights {
+  moe_config_t cfg;
+  int device;
+  void* table;          // device: CUtensorMap maps1[2G], maps2[G]
+  CUtensorMap* maps1;
+  CUtensorMap* maps2;
+};
+
+using namespace moe;
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+moe_status_t moe_set_trace(moe_trace_t* trace) {
+  if (trace && (!trace->events || !trace->kernel_ids || trace->capacity < 0 || trace->count < 0))
+    return fail(MOE_ERR_INVALID_ARG, "trace needs events, kernel_ids and a capacity");
+  g_trace = trace;
+  return MOE_OK;
+}
+
+const char* moe_last_error_message(void) { return g_last_error.c_str(); }
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_BOUNDS: return "device index out of bounds";
+  }
+  return "unknown status";
+}
+
+moe_status_t moe_workspace_size(const moe_config_t* cfg, int32_t op, size_t* bytes) {
+  MOE_TRY(check_config(cfg));
+  if (!bytes) return fail(MOE_ERR_INVALID_ARG, "bytes is NULL");
+  if (op < MOE_OP_ROUTE || op > MOE_OP_FORWARD) return fail(MOE_ERR_INVALID_ARG, "op = %d", op);
+  *bytes = layout(*cfg, op).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!ws || ws_bytes < kHeaderBytes) return fail(MOE_ERR_WORKSPACE, "workspace NULL or too small");
+  if (reinterpret_cast<uintptr_t>(ws) & 255)
+    return fail(MOE_ERR_WORKSPACE, "workspace is not 256-byte aligned");
+  MOE_CUDA(cudaMemsetAsync(ws, 0, kHeaderBytes, reinterpret_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+moe_status_t moe_get_device_error(void* ws, moe_stream_t stream, int32_t* device_bits) {
+  if (!ws) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t w = 0;
+  MOE_CUDA(cudaMemcpyAsync(&w, ws, 4, cudaMemcpyDeviceToHost, st));
+  MOE_CUDA(cudaMemsetAsync(ws, 0, 4, st));
+  MOE_CUDA(cudaStreamSynchronize(st));
+  if (device_bits) *device_bits = static_cast<int32_t>(w);
+  if (w & kErrTimeout) return fail(MOE_ERR_DEVICE_TIMEOUT, "a kernel wait timed out (bits 0x%x)", w);
+  if (w & (kErrBounds | kErrNoSelect))
+    return fail(MOE_ERR_BOUNDS, "a kernel met an out-of-range index (bits 0x%x)", w);
+  return MOE_OK;
+}
+
+moe_status_t moe_weights_create(const moe_config_t* cfg, const moe_weight_list_t* wl,
+                                moe_weights_t* out) {
+  MOE_TRY(check_config(cfg));
+  if (!wl || !out) return fail(MOE_ERR_INVALID_ARG, "weights or out is NULL");
+  *out = nullptr;
+  if (cfg->wtype != MOE_DTYPE_BF16)
+    return fail(MOE_ERR_UNSUPPORTED, "fp8 expert weights are not supported by this build");
+  if (!wl->gate || !wl->up || !wl->down)
+    return fail(MOE_ERR_INVALID_ARG, "gate/up/down pointer arrays must not be NULL");
+  const int E = cfg->E;
+  for (int e = 0; e < E; ++e) {
+    char nm[64];
+    snprintf(nm, sizeof nm, "gate[%d]", e);
+    MOE_TRY(check_ptr(wl->gate[e], nm));
+    snprintf(nm, sizeof nm, "up[%d]", e);
+    MOE_TRY(check_ptr(wl->up[e], nm));
+    snprintf(nm, sizeof nm, "down[%d]", e);
+    MOE_TRY(check_ptr(wl->down[e], nm));
+  }
+  const bool shared = cfg->I_shared > 0;
+  if (shared) {
+    MOE_TRY(check_ptr(wl->shared_gate, "shared_gate"));
+    MOE_TRY(check_ptr(wl->shared_up, "shared_up"));
+    MOE_TRY(check_ptr(wl->shared_down, "shared_down"));
+  }
+  const int G = E + (shared ? 1 : 0);
+  std::vector<CUtensorMap> maps(3 * G);
+  CUtensorMap* m1 = maps.data();
+  CUtensorMap* m2 = maps.data() + 2 * G;
+  const uint64_t H = cfg->H, I = cfg->I, Is = cfg->I_shared;
+  for (int g = 0; g < G; ++g) {
+    const bool sh = g == E;
+    const uint64_t inter = sh ? Is : I;
+    MOE_TRY(encode_2d(&m1[2 * g], true, sh ? wl->shared_gate : wl->gate[g], H, inter, kTileK,
+                      kGemm1TileN));
+    MOE_TRY(encode_2d(&m1[2 * g + 1], true, sh ? wl->shared_up : wl->up[g], H, inter, kTileK,
+                      kGemm1TileN));
+    MOE_TRY(encode_2d(&m2[g], true, sh ? wl->shared_down : wl->down[g], inter, H, kTileK,
+                      kGemm2TileN));
+  }
+  void* table = nullptr;
+  const size_t bytes = maps.size() * sizeof(CUtensorMap);
+  MOE_CUDA(cudaMalloc(&table, bytes));
+  cudaError_t e = cudaMemcpy(table, maps.data(), bytes, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(table);
+    return cuda_fail(e, "cudaMemcpy(weight table)");
+  }
+  moe_weights* w = new moe_weights;
+  w->cfg = *cfg;
+  w->device = current_device();
+  w->table = table;
+  w->maps1 = static_cast<CUtensorMap*>(table);
+  w->maps2 = static_cast<CUtensorMap*>(table) + 2 * G;
+  *out = w;
+  return MOE_OK;
+}
+
+void moe_weights_destroy(moe_weights_t w) {
+  if (!w) return;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(w->device);
+  cudaDeviceSynchronize();
+  cudaFree(w->table);
+  cudaSetDevice(prev);
+  delete w;
+}
+
+}  // extern "C"
+
+// ======================================================================== steps
+namespace moe {
+
+static moe_status_t run_route(const moe_config_t& c, const void* x, const void* w_router,
+                              const float* bias, int32_t* ids, float* w, float* logits,
+                              uint32_t* err, cudaStream_t st) {
+  const int E_pad = (c.E + 15) / 16 * 16;
+  CUtensorMap mx, mw;
+  MOE_TRY(encode_2d(&mx, true, x, c.H, c.T, kTileK, kTileM));
+  MOE_TRY(encode_2d(&mw, true, w_router, c.H, c.E, kTileK, E_pad));
+  trace_mark(st, MOE_K_ROUTER);
+  MOE_CUDA(launch_router(mx, mw, c.T, c.H, c.E, E_pad, c.k, c.score, c.renormalize, c.route_scale,
+                         bias, ids, w, logits, err, st));
+  return MOE_OK;
+}
+
+static moe_status_t run_permute(const moe_config_t& c, const Layout& L, void* ws, const int32_t* ids,
+                                const float* topk_w, const void* x, int32_t* counts,
+                                int32_t* offsets, int32_t* perm_token, int32_t* inv_row,
+                                float* row_weight, void* x_perm, float* x_perm_scales,
+                                cudaStream_t st) {
+  uint32_t* err = err_word(ws);
+  const int nblk = static_cast<int>((c.T + kPermTok - 1) / kPermTok);
+  int32_t* blk_counts = at<int32_t*>(ws, L.blk_counts);
+  int32_t* blk_base = at<int32_t*>(ws, L.blk_base);
+  trace_mark(st, MOE_K_HIST);
+  MOE_CUDA(launch_hist(ids, c.T, c.k, c.E, blk_counts, err, st));
+  trace_mark(st, MOE_K_SCAN);
+  MOE_CUDA(launch_scan(blk_counts, nblk, c.E, blk_base, counts, offsets, st));
+  trace_mark(st, MOE_K_SCATTER);
+  MOE_CUDA(launch_scatter(ids, topk_w, x, c.T, c.k, c.E, c.H, c.wtype == MOE_DTYPE_FP8_E4M3,
+                          blk_base, offsets, perm_token, inv_row, row_weight, x_perm,
+                          x_perm_scales, err, st));
+  return MOE_OK;
+}
+
+static moe_status_t run_ffn(const moe_config_t& c, const moe_weights* W, const Layout& L, void* ws,
+                            const void* x_perm, const int32_t* offsets, const float* row_weight,
+                            const void* x_shared, void* y_perm, void* shared_out,
+                            cudaStream_t st) {
+  uint32_t* err = err_word(ws);
+  const bool shared = c.I_shared > 0 && x_shared != nullptr;
+  const int64_t R = c.T * c.k;
+  int32_t* s1 = at<int32_t*>(ws, L.sched1);
+  int32_t* s2 = at<int32_t*>(ws, L.sched2);
+  __nv_bfloat16* h = at<__nv_bfloat16*>(ws, L.h);
+  __nv_bfloat16* hs = at<__nv_bfloat16*>(ws, L.hs);
+  const int n1r = c.I / kGemm1TileN, n1s = c.I_shared / kGemm1TileN;
+  const int n2 = (c.H + kGemm2TileN - 1) / kGemm2TileN;
+  trace_mark(st, MOE_K_PLAN);
+  MOE_CUDA(launch_plan(offsets, c.E, shared ? 1 : 0, c.T, n1r, n1s, n2, n2, s1, s2, st));
+
+  CUtensorMap a0, a1;
+  MOE_TRY(encode_2d(&a0, true, x_perm, c.H, R, kTileK, kTileM));
+  if (shared) MOE_TRY(encode_2d(&a1, true, x_shared, c.H, c.T, kTileK, kTileM));
+  else a1 = a0;
+  GemmArgs g1{};
+  g1.b_maps = W->maps1;
+  g1.offsets = offsets;
+  g1.sched = s1;
+  g1.out0 = h;
+  g1.out1 = hs;
+  g1.row_weight = nullptr;
+  g1.err = err;
+  g1.E = c.E;
+  g1.has_shared = shared ? 1 : 0;
+  g1.T = static_cast<int32_t>(c.T);
+  g1.K_routed = c.H;
+  g1.K_shared = c.H;
+  g1.N_routed = c.I;
+  g1.N_shared = c.I_shared;
+  const int grid = sm_count();
+  trace_mark(st, MOE_K_GEMM1);
+  MOE_CUDA(launch_grouped_gemm(true, a0, a1, g1, grid, st));
+
+  CUtensorMap b0, b1;
+  MOE_TRY(encode_2d(&b0, true, h, c.I, R, kTileK, kTileM));
+  if (shared) MOE_TRY(encode_2d(&b1, true, hs, c.I_shared, c.T, kTileK, kTileM));
+  else b1 = b0;
+  GemmArgs g2 = g1;
+  g2.b_maps = W->maps2;
+  g2.sched = s2;
+  g2.out0 = y_perm;
+  g2.out1 = shared_out;
+  g2.row_weight = row_weight;
+  g2.K_routed = c.I;
+  g2.K_shared = c.I_shared;
+  g2.N_routed = c.H;
+  g2.N_shared = c.H;
+  trace_mark(st, MOE_K_GEMM2);
+  MOE_CUDA(launch_grouped_gemm(false, b0, b1, g2, grid, st));
+  return MOE_OK;
+}
+
+static bool same_shape(const moe_config_t& a, const moe_config_t& b) {
+  return a.H == b.H && a.E == b.E && a.I == b.I && a.I_shared == b.I_shared && a.wtype == b.wtype;
+}
+
+}  // namespace moe
+
+extern "C" {
+
+moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_router,
+                       const float* logit_bias, int32_t* topk_ids, float* topk_w,
+                       float* logits_out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_TRY(check_ws(*cfg, MOE_OP_ROUTE, ws, ws_bytes));
+  if (cfg->T == 0) return MOE_OK;
+  MOE_TRY(check_ptr(x, "x"));
+  MOE_TRY(check_ptr(w_router, "w_router"));
+  MOE_TRY(check_ptr4(topk_ids, "topk_ids"));
+  MOE_TRY(check_ptr4(topk_w, "topk_w"));
+  if (logit_bias) MOE_TRY(check_ptr4(logit_bias, "logit_bias"));
+  if (logits_out) MOE_TRY(check_ptr(logits_out, "logits_out"));
+  if (logits_out && cfg->E % 4)
+    return fail(MOE_ERR_UNSUPPORTED, "logits_out needs E to be a multiple of 4");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const moe_status_t s = run_route(*cfg, x, w_router, logit_bias, topk_ids, topk_w, logits_out,
+                                   err_word(ws), st);
+  trace_mark(st, -1);
+  return s;
+}
+
+moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, const float* topk_w,
+                         const void* x, int32_t* expert_counts, int32_t* expert_offsets,
+                         int32_t* perm_token, int32_t* inv_row, float* row_weight, void* x_perm,
+                         float* x_perm_scales, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_TRY(check_ws(*cfg, MOE_OP_PERMUTE, ws, ws_bytes));
+  MOE_TRY(check_ptr4(expert_counts, "expert_counts"));
+  MOE_TRY(check_ptr4(expert_offsets, "expert_offsets"));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cfg->T == 0) {
+    MOE_CUDA(cudaMemsetAsync(expert_counts, 0, size_t(cfg->E) * 4, st));
+    MOE_CUDA(cudaMemsetAsync(expert_offsets, 0, size_t(cfg->E + 1) * 4, st));
+    return MOE_OK;
+  }
+  MOE_TRY(check_ptr4(topk_ids, "topk_ids"));
+  MOE_TRY(check_ptr4(perm_token, "perm_token"));
+  MOE_TRY(check_ptr4(inv_row, "inv_row"));
+  if (row_weight) {
+    MOE_TRY(check_ptr4(row_weight, "row_weight"));
+    if (!topk_w) return fail(MOE_ERR_INVALID_ARG, "row_weight needs topk_w");
+    MOE_TRY(check_ptr4(topk_w, "topk_w"));
+  }
+  if (x_perm) {
+    MOE_TRY(check_ptr(x, "x"));
+    MOE_TRY(check_ptr(x_perm, "x_perm"));
+    if (cfg->wtype == MOE_DTYPE_FP8_E4M3) MOE_TRY(check_ptr4(x_perm_scales, "x_perm_scales"));
+  }
+  Layout L = layout(*cfg, MOE_OP_PERMUTE);
+  const moe_status_t s = run_permute(*cfg, L, ws, topk_ids, topk_w, x, expert_counts,
+                                     expert_offsets, perm_token, inv_row, row_weight, x_perm,
+                                     x_perm_scales, st);
+  trace_mark(st, -1);
+  return s;
+}
+
+moe_status_t moe_grouped_ffn(const moe_config_t* cfg, moe_weights_t weights, const void* x_perm,
+                             const float* x_perm_scales, const int32_t* expert_offsets,
+                             const float* row_weight, const void* x_shared,
+                             const float* x_shared_scales, void* y_perm, void* shared_out,
+                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_TRY(check_ws(*cfg, MOE_OP_GROUPED_FFN, ws, ws_bytes));
+  if (!weights) return fail(MOE_ERR_INVALID_ARG, "weights is NULL");
+  if (!same_shape(weights->cfg, *cfg))
+    return fail(MOE_ERR_INVALID_ARG, "weights were created for a different layer shape");
+  if (cfg->wtype != MOE_DTYPE_BF16)
+    return fail(MOE_ERR_UNSUPPORTED, "fp8 grouped FFN is not supported by this build");
+  (void)x_perm_scales;
+  (void)x_shared_scales;
+  if (cfg->T == 0) return MOE_OK;
+  MOE_TRY(check_ptr(x_perm, "x_perm"));
+  MOE_TRY(check_ptr4(expert_offsets, "expert_offsets"));
+  MOE_TRY(check_ptr(y_perm, "y_perm"));
+  if (row_weight) MOE_TRY(check_ptr4(row_weight, "row_weight"));
+  if (x_shared && cfg->I_shared > 0) {
+    MOE_TRY(check_ptr(x_shared, "x_shared"));
+    MOE_TRY(check_ptr(shared_out, "shared_out"));
+  }
+  Layout L = layout(*cfg, MOE_OP_GROUPED_FFN);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const moe_status_t s = run_ffn(*cfg, weights, L, ws, x_perm, expert_offsets, row_weight,
+                                 cfg->I_shared > 0 ? x_shared : nullptr, y_perm, shared_out, st);
+  trace_mark(st, -1);
+  return s;
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm, const int32_t* inv_row,
+                         const void* shared_out, void* out, void* ws, size_t ws_bytes,
+                         moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_TRY(check_ws(*cfg, MOE_OP_COMBINE, ws, ws_bytes));
+  if (cfg->T == 0) return MOE_OK;
+  MOE_TRY(check_ptr(y_perm, "y_perm"));
+  MOE_TRY(check_ptr4(inv_row, "inv_row"));
+  MOE_TRY(check_ptr(out, "out"));
+  if (shared_out) MOE_TRY(check_ptr(shared_out, "shared_out"));
+  if (out == y_perm) return fail(MOE_ERR_INVALID_ARG, "out must not alias y_perm");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  trace_mark(st, MOE_K_COMBINE);
+  MOE_CUDA(launch_combine(y_perm, inv_row, shared_out, out, cfg->T, cfg->k, cfg->H,
+                          cfg->T * cfg->k, err_word(ws), st));
+  trace_mark(st, -1);
+  return MOE_OK;
+}
+
+moe_status_t moe_forward(const moe_config_t* cfg, moe_weights_t weights, const void* x,
+                         const void* w_router, const float* logit_bias, void* out,
+                         int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
+                         moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_TRY(check_ws(*cfg, MOE_OP_FORWARD, ws, ws_bytes));
+  if (!weights) return fail(MOE_ERR_INVALID_ARG, "weights is NULL");
+  if (!same_shape(weights->cfg, *cfg))
+    return fail(MOE_ERR_INVALID_ARG, "weights were created for a different layer shape");
+  if (cfg->wtype != MOE_DTYPE_BF16)
+    return fail(MOE_ERR_UNSUPPORTED, "fp8 forward is not supported by this build");
+  if (cfg->T == 0) return MOE_OK;
+  MOE_TRY(check_ptr(x, "x"));
+  MOE_TRY(check_ptr(w_router, "w_router"));
+  MOE_TRY(check_ptr(out, "out"));
+  if (logit_bias) MOE_TRY(check_ptr4(logit_bias, "logit_bias"));
+  if (topk_ids_out) MOE_TRY(check_ptr4(topk_ids_out, "topk_ids_out"));
+  if (topk_w_out) MOE_TRY(check_ptr4(topk_w_out, "topk_w_out"));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const Layout L = layout(*cfg, MOE_OP_FORWARD);
+  uint32_t* err = err_word(ws);
+  int32_t* ids = topk_ids_out ? topk_ids_out : at<int32_t*>(ws, L.ids);
+  float* w = topk_w_out ? topk_w_out : at<float*>(ws, L.w);
+  int32_t* counts = at<int32_t*>(ws, L.counts);
+  int32_t* offsets = at<int32_t*>(ws, L.offsets);
+  int32_t* perm_token = at<int32_t*>(ws, L.perm_token);
+  int32_t* inv_row = at<int32_t*>(ws, L.inv_row);
+  float* row_weight = at<float*>(ws, L.row_weight);
+  void* x_perm = at<void*>(ws, L.x_perm);
+  void* y_perm = at<void*>(ws, L.y_perm);
+  void* shared_out = cfg->I_shared > 0 ? at<void*>(ws, L.shared_out) : nullptr;
+
+  MOE_TRY(run_route(*cfg, x, w_router, logit_bias, ids, w, nullptr, err, st));
+  MOE_TRY(run_permute(*cfg, L, ws, ids, w, x, counts, offsets, perm_token, inv_row, row_weight,
+                      x_perm, nullptr, st));
+  MOE_TRY(run_ffn(*cfg, weights, L, ws, x_perm, offsets, row_weight, x, y_perm, shared_out, st));
+  trace_mark(st, MOE_K_COMBINE);
+  MOE_CUDA(launch_combine(y_perm, inv_row, shared_out, out, cfg->T, cfg->k, cfg->H,
+                          cfg->T * cfg->k, err, st));
+  trace_mark(st, -1);
+  return MOE_OK;
+}
+
+moe_status_t moe_quantize_weight_fp8(const float* w, int64_t N, int64_t K, uint8_t* q,
+                                     float* scales, moe_stream_t stream) {
+  if (N <= 0 || K <= 0 || N % 128 || K % 128)
+    return fail(MOE_ERR_INVALID_ARG, "N and K must be positive multiples of 128");
+  MOE_TRY(check_ptr4(w, "w"));
+  MOE_TRY(check_ptr(q, "q", false));
+  MOE_TRY(check_ptr4(scales, "scales"));
+  if (K / 128 > 65535 || N / 128 > 65535) return fail(MOE_ERR_UNSUPPORTED, "matrix too large");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  trace_mark(st, MOE_K_QUANT);
+  MOE_CUDA(launch_quant_weight_fp8(w, N, K, q, scales, st));
+  trace_mark(st, -1);
+  return MOE_OK;
+}
+
+moe_status_t moe_quantize_act_fp8(const void* x, int64_t M, int64_t K, uint8_t* q, float* scales,
+                                  moe_stream_t stream) {
+  if (M < 0 || K <= 0 || K % 128)
+    return fail(MOE_ERR_INVALID_ARG, "M >= 0 and K a positive multiple of 128 required");
+  if (M == 0) return MOE_OK;
+  MOE_TRY(check_ptr(x, "x"));
+  MOE_TRY(check_ptr(q, "q", false));
+  if (reinterpret_cast<uintptr_t>(q) & 7) return fail(MOE_ERR_INVALID_ARG, "q is not 8-byte aligned");
+  MOE_TRY(check_ptr4(scales, "scales"));
+  if (M * (K / 128) * 16 / 256 >= (int64_t(1) << 31))
+    return fail(MOE_ERR_UNSUPPORTED, "matrix too large");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  trace_mark(st, MOE_K_QUANT);
+  MOE_CUDA(launch_quant_act_fp8(x, M, K, q, scales, st));
+  trace_mark(st, -1);
+  return MOE_OK;
+}
+
+}  // extern "C"

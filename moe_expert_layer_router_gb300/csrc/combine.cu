@@ -1,0 +1,84 @@
+// Combine: out[t] = sum_j y_perm[inv_row[t, j]] (+ shared_out[t]) -- the
+// expert results of each token gathered back to token order and summed in
+// fp32, slot order j = 0..k-1 then the shared expert, rounded once to bf16.
+// y_perm and shared_out are fp32 rows (the grouped down projection writes
+// them unrounded).  One block per token; each thread owns 8-column chunks and
+// issues the k row loads of a chunk back to back so they are in flight together.
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kMaxK = 16;
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void add4(float (&acc)[8], int o, const float4& v) {
+  acc[o] += v.x;
+  acc[o + 1] += v.y;
+  acc[o + 2] += v.z;
+  acc[o + 3] += v.w;
+}
+
+__global__ void __launch_bounds__(kThreads)
+    combine_kernel(const float4* __restrict__ y, const int32_t* __restrict__ inv_row,
+                   const float4* __restrict__ sh, uint4* __restrict__ out, int k, int H, int64_t R,
+                   uint32_t* err) {
+  __shared__ int64_t rows[kMaxK];
+  const int64_t t = blockIdx.x;
+  const int nch = H / 8;  // 8 columns: two float4 in, one uint4 of bf16 out
+  if (threadIdx.x < k) {
+    const int32_t r = inv_row[t * k + threadIdx.x];
+    int64_t rr = r;
+    if (r < 0 || r >= R) {
+      atomicOr(err, kErrBounds);
+      rr = -1;
+    }
+    rows[threadIdx.x] = rr;
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < nch; c += kThreads) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    float4 v[kMaxK][2];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j < k && rows[j] >= 0) {
+        const float4* src = y + rows[j] * (2 * nch) + 2 * c;
+        v[j][0] = __ldcs(src);
+        v[j][1] = __ldcs(src + 1);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j < k && rows[j] >= 0) {
+        add4(acc, 0, v[j][0]);
+        add4(acc, 4, v[j][1]);
+      }
+    }
+    if (sh) {
+      const float4* src = sh + t * (2 * nch) + 2 * c;
+      add4(acc, 0, __ldcs(src));
+      add4(acc, 4, __ldcs(src + 1));
+    }
+    out[t * nch + c] = make_uint4(pack2(acc[0], acc[1]), pack2(acc[2], acc[3]),
+                                  pack2(acc[4], acc[5]), pack2(acc[6], acc[7]));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const void* y_perm, const int32_t* inv_row, const void* shared_out,
+                           void* out, int64_t T, int k, int H, int64_t R, uint32_t* err,
+                           cudaStream_t stream) {
+  combine_kernel<<<static_cast<unsigned>(T), kThreads, 0, stream>>>(
+      static_cast<const float4*>(y_perm), inv_row, static_cast<const float4*>(shared_out),
+      static_cast<uint4*>(out), k, H, R, err);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,95 @@
+// Internal interface between the C-ABI host code (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace moe {
+
+// Bits of the sticky status word at the start of every workspace.
+constexpr uint32_t kErrBounds = 1u;    // an index outside its range was skipped
+constexpr uint32_t kErrTimeout = 2u;   // a bounded wait expired
+constexpr uint32_t kErrNoSelect = 4u;  // a token had fewer than k selectable logits (NaN)
+
+// A wait that takes longer than this is treated as a hang: the waiting role
+// records kErrTimeout, raises the CTA's abort flag and leaves its loop.
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+// Tile shapes shared by the host (tensor-map boxes, schedules) and kernels.
+constexpr int kTileM = 128;        // rows of one accumulator tile (UMMA M)
+constexpr int kTileK = 64;         // bf16 K per stage = one 128-byte swizzle row
+constexpr int kGemm1TileN = 128;   // h columns per GEMM1 tile (gate 128 + up 128 = UMMA N 256)
+constexpr int kGemm2TileN = 256;   // y columns per GEMM2 tile
+constexpr int kMaxExperts = 256;
+constexpr int kMaxGroups = kMaxExperts + 1;  // routed experts + the shared expert
+constexpr int kPermTok = 64;       // tokens per histogram / scatter block
+
+// Tile schedule of one grouped GEMM, in device memory (int32):
+//   [0]            number of tiles
+//   [1 .. G+1]     first tile of each processing slot (exclusive prefix, [G+1] = total)
+//   [G+2 .. 2G+1]  group processed in each slot (heaviest first)
+__host__ __device__ inline int sched_ints(int G) { return 2 * G + 2; }
+
+struct GemmArgs {
+  const CUtensorMap* b_maps;   // GEMM1: gate of group g at 2g, up at 2g+1; GEMM2: down at g
+  const int32_t* offsets;      // [E+1] routed row offsets
+  const int32_t* sched;        // tile schedule (see above)
+  void* out0;                  // routed output rows (GEMM1: bf16 h, GEMM2: fp32 y)
+  void* out1;                  // shared-expert output rows (same types)
+  const float* row_weight;     // GEMM2: per routed row scale, or null
+  uint32_t* err;               // sticky status word
+  int32_t E;
+  int32_t has_shared;
+  int32_t T;                   // rows of the shared group
+  int32_t K_routed, K_shared;  // reduction sizes
+  int32_t N_routed, N_shared;  // output columns
+};
+
+// --------------------------------------------------------------- launchers
+cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_w, int64_t T, int H,
+                          int E, int E_pad, int k, int score, int renormalize, float route_scale,
+                          const float* bias, int32_t* topk_ids, float* topk_w, float* logits_out,
+                          uint32_t* err, cudaStream_t stream);
+
+cudaError_t launch_hist(const int32_t* ids, int64_t T, int k, int E, int32_t* blk_counts,
+                        uint32_t* err, cudaStream_t stream);
+
+cudaError_t launch_scan(const int32_t* blk_counts, int nblk, int E, int32_t* blk_base,
+                        int32_t* counts, int32_t* offsets, cudaStream_t stream);
+
+cudaError_t launch_scatter(const int32_t* ids, const float* topk_w, const void* x, int64_t T,
+                           int k, int E, int H, int fp8, const int32_t* blk_base,
+                           const int32_t* offsets, int32_t* perm_token, int32_t* inv_row,
+                           float* row_weight, void* x_perm, float* x_perm_scales, uint32_t* err,
+                           cudaStream_t stream);
+
+cudaError_t launch_plan(const int32_t* offsets, int E, int has_shared, int64_t T, int n1_routed,
+                        int n1_shared, int n2_routed, int n2_shared, int32_t* sched1,
+                        int32_t* sched2, cudaStream_t stream);
+
+cudaError_t launch_grouped_gemm(bool swiglu, const CUtensorMap& map_a0, const CUtensorMap& map_a1,
+                                const GemmArgs& args, int grid, cudaStream_t stream);
+
+cudaError_t launch_combine(const void* y_perm, const int32_t* inv_row, const void* shared_out,
+                           void* out, int64_t T, int k, int H, int64_t R, uint32_t* err,
+                           cudaStream_t stream);
+
+cudaError_t launch_quant_weight_fp8(const float* w, int64_t N, int64_t K, uint8_t* q,
+                                    float* scales, cudaStream_t stream);
+
+cudaError_t launch_quant_act_fp8(const void* x, int64_t M, int64_t K, uint8_t* q, float* scales,
+                                 cudaStream_t stream);
+
+}  // namespace moe
+
+namespace moe {
+// Raises a kernel's dynamic shared-memory limit on the current device (once per device).
+cudaError_t ensure_smem_attr(const void* func, int bytes);
+
+// Kernel tracing (see moe_set_trace): records an event before kernel `id` on
+// `stream` (id = -1: after the last kernel of a call).  No-op without a trace.
+void trace_mark(cudaStream_t stream, int id);
+}  // namespace moe

@@ -1,0 +1,300 @@
+// Token-to-expert histogram and permutation (the per-expert token counts of
+// the dispatch metadata, "ASAP: A DiSaggregated and Asynchronous Inference
+// System for MoE Prefill", table 2), plus the tile planner of the grouped GEMMs.
+//
+// Deterministic and atomic-free across blocks:
+//   hist     block b (64 tokens) counts its (token, slot) entries per expert
+//            into shared memory -> blk_counts[e][b]
+//   scan     one warp per expert scans blk_counts[e][*] (exclusive) ->
+//            blk_base[e][b] and counts[e]; a block scan of counts -> offsets
+//   scatter  block b sets bit t of word mask[e] for each token t of the
+//            block that chose e; the rank of (t, e) inside the block is the
+//            popcount of the bits below t, so
+//              row(t, j) = offsets[e] + blk_base[e][b] + rank
+//            orders every expert's rows by ascending token index.  The same
+//            block then reads each of its tokens' hidden state once and
+//            writes it to the token's k rows (16-byte vector accesses), so x
+//            crosses HBM once on the way in.
+#include <cuda_fp8.h>
+
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kHistThreads = 256;
+constexpr int kScanThreads = 1024;
+constexpr int kScatterThreads = 256;
+constexpr int kMaxK = 16;
+
+__global__ void __launch_bounds__(kHistThreads)
+    hist_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int E, int nblk,
+                int32_t* __restrict__ blk_counts, uint32_t* err) {
+  __shared__ int cnt[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += kHistThreads) cnt[e] = 0;
+  __syncthreads();
+  const int64_t t0 = int64_t(blockIdx.x) * kPermTok;
+  const int n = static_cast<int>(T - t0 < kPermTok ? T - t0 : kPermTok) * k;
+  const int32_t* src = ids + t0 * k;
+  for (int i = threadIdx.x; i < n; i += kHistThreads) {
+    const int e = src[i];
+    if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) atomicAdd(&cnt[e], 1);
+    else atomicOr(err, kErrBounds);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kHistThreads) blk_counts[int64_t(e) * nblk + blockIdx.x] = cnt[e];
+}
+
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, v, d);
+    if (lane >= d) v += u;
+  }
+  return v;
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+    scan_kernel(const int32_t* __restrict__ blk_counts, int nblk, int E,
+                int32_t* __restrict__ blk_base, int32_t* __restrict__ counts,
+                int32_t* __restrict__ offsets) {
+  __shared__ int tot[kMaxExperts];
+  __shared__ int wsum[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = warp; e < E; e += kScanThreads / 32) {
+    const int32_t* src = blk_counts + int64_t(e) * nblk;
+    int32_t* dst = blk_base + int64_t(e) * nblk;
+    int carry = 0;
+    for (int b0 = 0; b0 < nblk; b0 += 32) {
+      const int b = b0 + lane;
+      const int v = b < nblk ? src[b] : 0;
+      const int inc = warp_incl_scan(v, lane);
+      if (b < nblk) dst[b] = carry + inc - v;
+      carry += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (lane == 0) tot[e] = carry;
+  }
+  __syncthreads();
+  // exclusive scan of the E totals (E <= 256 < blockDim)
+  const int v = threadIdx.x < E ? tot[threadIdx.x] : 0;
+  const int inc = warp_incl_scan(v, lane);
+  if (lane == 31) wsum[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int s = wsum[lane];
+    const int si = warp_incl_scan(s, lane);
+    wsum[lane] = si - s;
+  }
+  __syncthreads();
+  if (threadIdx.x < E) {
+    counts[threadIdx.x] = v;
+    offsets[threadIdx.x] = wsum[warp] + inc - v;
+    if (threadIdx.x == E - 1) offsets[E] = wsum[warp] + inc;
+  }
+}
+
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float a, float b, float c, float d) {
+  const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__global__ void __launch_bounds__(kScatterThreads)
+    scatter_kernel(const int32_t* __restrict__ ids, const float* __restrict__ topk_w,
+                   const __nv_bfloat16* __restrict__ x, int64_t T, int k, int E, int H, int nblk,
+                   int fp8, const int32_t* __restrict__ blk_base,
+                   const int32_t* __restrict__ offsets, int32_t* __restrict__ perm_token,
+                   int32_t* __restrict__ inv_row, float* __restrict__ row_weight,
+                   void* __restrict__ x_perm, float* __restrict__ x_perm_scales, uint32_t* err) {
+  __shared__ uint32_t mask[kMaxExperts][kPermTok / 32];
+  __shared__ int32_t rows_s[kPermTok * kMaxK];
+  for (int i = threadIdx.x; i < E * (kPermTok / 32); i += kScatterThreads)
+    (&mask[0][0])[i] = 0u;
+  __syncthreads();
+  const int64_t t0 = int64_t(blockIdx.x) * kPermTok;
+  const int nt = static_cast<int>(T - t0 < kPermTok ? T - t0 : kPermTok);
+  const int n = nt * k;
+  const int32_t* src = ids + t0 * k;
+  for (int i = threadIdx.x; i < n; i += kScatterThreads) {
+    const int tl = i / k;
+    const int e = src[i];
+    if (static_cast<unsigned>(e) < static_cast<unsigned>(E))
+      atomicOr(&mask[e][tl >> 5], 1u << (tl & 31));
+  }
+  __syncthreads();
+  const int64_t R = T * k;
+  for (int i = threadIdx.x; i < n; i += kScatterThreads) {
+    const int tl = i / k;
+    const int e = src[i];
+    int32_t row = -1;
+    if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) {
+      const int wd = tl >> 5;
+      int rank = __popc(mask[e][wd] & ((1u << (tl & 31)) - 1u));
+      for (int w = 0; w < wd; ++w) rank += __popc(mask[e][w]);
+      const int64_t r = int64_t(offsets[e]) + blk_base[int64_t(e) * nblk + blockIdx.x] + rank;
+      if (r >= 0 && r < R) row = static_cast<int32_t>(r);
+      else atomicOr(err, kErrBounds);
+    } else {
+      atomicOr(err, kErrBounds);
+    }
+    rows_s[i] = row;
+    inv_row[t0 * k + i] = row;
+    if (row >= 0) {
+      perm_token[row] = static_cast<int32_t>(t0 + tl);
+      if (row_weight) row_weight[row] = topk_w[t0 * k + i];
+    }
+  }
+  __syncthreads();
+  if (!x_perm) return;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = kScatterThreads / 32;
+  const int nch = H / 8;  // 16-byte chunks of 8 bf16 per row
+  if (!fp8) {
+    uint4* dst = static_cast<uint4*>(x_perm);
+    for (int tl = warp; tl < nt; tl += nwarps) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(x + (t0 + tl) * int64_t(H));
+      const int32_t* rr = rows_s + tl * k;
+      for (int c0 = 0; c0 < nch; c0 += 32 * 4) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int cc = c0 + u * 32 + lane;
+          if (cc < nch) v[u] = __ldcs(s4 + cc);
+        }
+        for (int j = 0; j < k; ++j) {
+          const int32_t row = rr[j];
+          if (row < 0) continue;
+          uint4* d4 = dst + int64_t(row) * nch;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int cc = c0 + u * 32 + lane;
+            if (cc < nch) d4[cc] = v[u];
+          }
+        }
+      }
+    }
+  } else {
+    // e4m3 codes, one fp32 scale per 128 features (16 chunks = 16 lanes).
+    uint2* dst = static_cast<uint2*>(x_perm);
+    const int ng = H / 128;
+    for (int tl = warp; tl < nt; tl += nwarps) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(x + (t0 + tl) * int64_t(H));
+      const int32_t* rr = rows_s + tl * k;
+      for (int c0 = 0; c0 < nch; c0 += 32) {
+        const int cc = c0 + lane;  // nch is a multiple of 16: half warps stay whole
+        const bool on = cc < nch;
+        const uint4 v = on ? __ldcs(s4 + cc) : make_uint4(0, 0, 0, 0);
+        float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                      bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+        for (int d = 8; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+        const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+        uint2 q;
+        q.x = cvt_e4m3x4(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s), __fdiv_rn(f[2], s), __fdiv_rn(f[3], s));
+        q.y = cvt_e4m3x4(__fdiv_rn(f[4], s), __fdiv_rn(f[5], s), __fdiv_rn(f[6], s), __fdiv_rn(f[7], s));
+        if (!on) continue;
+        for (int j = 0; j < k; ++j) {
+          const int32_t row = rr[j];
+          if (row < 0) continue;
+          dst[int64_t(row) * nch + cc] = q;
+          if ((cc & 15) == 0) x_perm_scales[int64_t(row) * ng + (cc >> 4)] = s;
+        }
+      }
+    }
+  }
+}
+
+// Tile schedules of GEMM1 and GEMM2 from the row offsets: per group
+// ceil(rows/128) x n_tiles tiles; groups ordered by descending tile count
+// (ties: lower group first) so the heaviest experts start first.
+__global__ void __launch_bounds__(256)
+    plan_kernel(const int32_t* __restrict__ offsets, int E, int has_shared, int64_t T,
+                int n1r, int n1s, int n2r, int n2s, int32_t* __restrict__ sched1,
+                int32_t* __restrict__ sched2) {
+  __shared__ int tiles[2][kMaxGroups];
+  __shared__ int order[2][kMaxGroups];
+  const int G = E + has_shared;
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    const int64_t rows = g < E ? int64_t(offsets[g + 1]) - offsets[g] : T;
+    const int mt = static_cast<int>((rows + kTileM - 1) / kTileM);
+    tiles[0][g] = mt * (g < E ? n1r : n1s);
+    tiles[1][g] = mt * (g < E ? n2r : n2s);
+  }
+  __syncthreads();
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    for (int w = 0; w < 2; ++w) {
+      const int tg = tiles[w][g];
+      int rank = 0;
+      for (int h = 0; h < G; ++h) {
+        const int th = tiles[w][h];
+        rank += (th > tg) || (th == tg && h < g);
+      }
+      order[w][rank] = g;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < 64) {
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int32_t* s = w ? sched2 : sched1;
+    int carry = 0;
+    for (int b0 = 0; b0 < G; b0 += 32) {
+      const int b = b0 + lane;
+      const int v = b < G ? tiles[w][order[w][b]] : 0;
+      const int inc = warp_incl_scan(v, lane);
+      if (b < G) {
+        s[1 + b] = carry + inc - v;
+        s[G + 2 + b] = order[w][b];
+      }
+      carry += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (lane == 0) {
+      s[0] = carry;
+      s[1 + G] = carry;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_hist(const int32_t* ids, int64_t T, int k, int E, int32_t* blk_counts,
+                        uint32_t* err, cudaStream_t stream) {
+  const int nblk = static_cast<int>((T + kPermTok - 1) / kPermTok);
+  hist_kernel<<<nblk, kHistThreads, 0, stream>>>(ids, T, k, E, nblk, blk_counts, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan(const int32_t* blk_counts, int nblk, int E, int32_t* blk_base,
+                        int32_t* counts, int32_t* offsets, cudaStream_t stream) {
+  scan_kernel<<<1, kScanThreads, 0, stream>>>(blk_counts, nblk, E, blk_base, counts, offsets);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const int32_t* ids, const float* topk_w, const void* x, int64_t T,
+                           int k, int E, int H, int fp8, const int32_t* blk_base,
+                           const int32_t* offsets, int32_t* perm_token, int32_t* inv_row,
+                           float* row_weight, void* x_perm, float* x_perm_scales, uint32_t* err,
+                           cudaStream_t stream) {
+  const int nblk = static_cast<int>((T + kPermTok - 1) / kPermTok);
+  scatter_kernel<<<nblk, kScatterThreads, 0, stream>>>(
+      ids, topk_w, static_cast<const __nv_bfloat16*>(x), T, k, E, H, nblk, fp8, blk_base, offsets,
+      perm_token, inv_row, row_weight, x_perm, x_perm_scales, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan(const int32_t* offsets, int E, int has_shared, int64_t T, int n1_routed,
+                        int n1_shared, int n2_routed, int n2_shared, int32_t* sched1,
+                        int32_t* sched2, cudaStream_t stream) {
+  plan_kernel<<<1, 256, 0, stream>>>(offsets, E, has_shared, T, n1_routed, n1_shared, n2_routed,
+                                     n2_shared, sched1, sched2);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

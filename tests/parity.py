@@ -1,0 +1,99 @@
+"""Helpers of the GPU parity tests: tolerances derived from the arithmetic,
+near-tie handling for routing, and seeded layer inputs on the device."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import workload as wl
+
+# bf16 layer output (the benchmark spec): max |err| <= 2e-2 * RMS(ref), mean relative (L1 ratio) <= 5e-3
+BF16_MAX_OVER_RMS = 2e-2
+BF16_MEAN_REL = 5e-3
+FP8_MAX_OVER_RMS = 6e-2
+
+
+def f64(t) -> np.ndarray:
+    if isinstance(t, np.ndarray):
+        return t.astype(np.float64)
+    return t.detach().float().cpu().numpy().astype(np.float64) if t.dtype != torch.float64 \
+        else t.detach().cpu().numpy()
+
+
+def assert_close_layer(got, ref, max_over_rms=BF16_MAX_OVER_RMS, mean_rel=BF16_MEAN_REL, what=""):
+    got = f64(got)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    if ref.size == 0:
+        return 0.0, 0.0
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    err = np.abs(got - ref)
+    m = float(err.max()) / rms if rms > 0 else float(err.max())
+    r = float(err.sum() / max(np.abs(ref).sum(), 1e-300))
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    assert m <= max_over_rms, f"{what}: max|err|/rms = {m:.3e} > {max_over_rms}"
+    assert r <= mean_rel, f"{what}: mean rel = {r:.3e} > {mean_rel}"
+    return m, r
+
+
+def logit_tolerance(x, w_router) -> np.ndarray:
+    """Bound on |fp32 logit - exact logit| per (token, expert): the sum runs in
+    16-term MMA blocks whose partial sums are accumulated H/16 times in fp32;
+    the classic bound gamma_n * sum|x_h W_eh| with n = H/16 + 16 and unit
+    roundoff 2^-23 (truncating accumulation), doubled."""
+    xa = np.abs(f64(x))
+    wa = np.abs(f64(w_router))
+    H = xa.shape[1]
+    n = H / 16 + 16
+    return 2.0 * n * 2.0 ** -23 * (xa @ wa.T) + 1e-30
+
+
+def near_tie_tokens(ref_logits, k, tau) -> np.ndarray:
+    """Tokens whose selection or order can flip under logit errors < tau: some pair
+    of adjacent entries among the exact top-(k+1) logits is closer than 2*tau."""
+    E = ref_logits.shape[1]
+    srt = -np.sort(-ref_logits, axis=1)[:, :min(k + 1, E)]
+    gaps = srt[:, :-1] - srt[:, 1:]
+    tau = np.asarray(tau, dtype=np.float64)
+    tau = tau.max(axis=1, keepdims=True) if tau.ndim == 2 else tau.reshape(-1, 1)
+    return (gaps < 2.0 * tau).any(axis=1) if gaps.shape[1] else np.zeros(len(srt), bool)
+
+
+def check_selection_valid(ids, logits_gpu, k):
+    """The GPU's ids are the k largest of its own fp32 logits, in descending
+    order, equal values in ascending index order (checked without the oracle)."""
+    ids = np.asarray(ids)
+    lg = np.asarray(logits_gpu, dtype=np.float64)
+    T, E = lg.shape
+    sel = np.take_along_axis(lg, ids, axis=1)
+    assert (np.diff(sel, axis=1) <= 0).all(), "selected logits not descending"
+    eq = np.diff(sel, axis=1) == 0
+    assert (~eq | (np.diff(ids, axis=1) > 0)).all(), "equal logits not in index order"
+    mask = np.ones_like(lg, dtype=bool)
+    np.put_along_axis(mask, ids, False, axis=1)
+    rest = np.where(mask, lg, -np.inf).max(axis=1)
+    assert (sel[:, -1] >= rest).all(), "an unselected logit exceeds a selected one"
+    for t in range(T):
+        assert len(set(ids[t].tolist())) == k
+
+
+class Layer:
+    """Seeded inputs of one layer config on a device (weights per expert)."""
+
+    def __init__(self, lc: wl.LayerConfig, device):
+        self.lc = lc
+        self.dev = device
+        self.x = wl.gen_x(lc, device)
+        self.wr = wl.gen_router(lc, device)
+        b = wl.gen_bias(lc)
+        self.bias = b.to(device) if b is not None else None
+        self.W = [tuple(wl.gen_expert(lc, e, w, device) for w in ("gate", "up", "down"))
+                  for e in range(lc.E)]
+        self.S = (tuple(wl.gen_shared(lc, w, device) for w in ("gate", "up", "down"))
+                  if lc.I_shared else None)
+
+    def experts_cpu(self, e):
+        return tuple(f64(t) for t in self.W[e])
+
+    def shared_cpu(self):
+        return tuple(f64(t) for t in self.S) if self.S is not None else None

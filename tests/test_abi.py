@@ -1,0 +1,131 @@
+"""The C-ABI library: it loads, exports every symbol the header declares, and
+rejects bad arguments on the host before anything reaches a GPU.  CPU only:
+every call here fails validation before its first CUDA call."""
+import ctypes as C
+import re
+
+import pytest
+
+import moe_expert_layer_router_gb300 as m
+from moe_expert_layer_router_gb300 import _native as N
+
+
+@pytest.fixture(scope="module")
+def L():
+    from moe_expert_layer_router_gb300 import build
+    build.build()
+    return m.load()
+
+
+def header_functions():
+    txt = open(N.HEADER).read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", txt)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = header_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(N._SIG), "binding and header disagree"
+
+
+def test_abi_version_and_strings(L):
+    assert L.moe_abi_version() == 1
+    for s in range(7):
+        assert L.moe_status_string(s)
+
+
+def test_config_struct_layout():
+    assert C.sizeof(N.MoeConfig) == 48
+    assert N.MoeConfig.route_scale.offset == 36
+
+
+def cfg(**kw):
+    base = dict(T=256, H=512, E=8, k=2, I=1024, I_shared=0, score="softmax")
+    base.update(kw)
+    return m.make_config(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(E=0), N.MOE_ERR_UNSUPPORTED), (dict(E=300), N.MOE_ERR_UNSUPPORTED),
+    (dict(k=0), N.MOE_ERR_INVALID_ARG), (dict(k=9), N.MOE_ERR_INVALID_ARG),
+    (dict(E=32, k=17), N.MOE_ERR_INVALID_ARG), (dict(H=500), N.MOE_ERR_UNSUPPORTED),
+    (dict(H=64), N.MOE_ERR_UNSUPPORTED), (dict(I=100), N.MOE_ERR_UNSUPPORTED),
+    (dict(I_shared=64), N.MOE_ERR_UNSUPPORTED), (dict(T=-1), N.MOE_ERR_INVALID_ARG),
+    (dict(T=1 << 29, k=8, E=8), N.MOE_ERR_UNSUPPORTED),
+])
+def test_bad_config_rejected(L, kw, status):
+    c = cfg(**kw)
+    n = C.c_size_t(0)
+    assert L.moe_workspace_size(C.byref(c), N.MOE_OP_FORWARD, C.byref(n)) == status
+    assert L.moe_last_error_message()
+
+
+def test_bad_enums_rejected(L):
+    for field, val in (("score", 7), ("renormalize", 2), ("wtype", 5)):
+        c = cfg()
+        setattr(c, field, val)
+        n = C.c_size_t(0)
+        assert L.moe_workspace_size(C.byref(c), 0, C.byref(n)) == N.MOE_ERR_INVALID_ARG
+    c = cfg()
+    c.route_scale = float("nan")
+    assert L.moe_workspace_size(C.byref(c), 0, C.byref(C.c_size_t())) == N.MOE_ERR_INVALID_ARG
+
+
+def test_workspace_sizes_grow_with_op(L):
+    c = cfg(T=1000, E=32, k=4, H=1024, I=512, I_shared=256)
+    sizes = {op: m.moe_workspace_size(c, op) for op in ("route", "permute", "grouped_ffn",
+                                                         "combine", "forward")}
+    assert all(v % 256 == 0 for v in sizes.values())
+    assert sizes["route"] == sizes["combine"] == 256
+    R = 1000 * 4
+    # forward holds x_perm and y_perm (bf16 [R, H]) at least
+    assert sizes["forward"] >= 2 * R * 1024 * 2 + sizes["grouped_ffn"]
+    assert sizes["grouped_ffn"] >= R * 512 * 2 + 1000 * 256 * 2
+
+
+def test_workspace_checks_before_launch(L):
+    c = cfg()
+    # NULL and misaligned workspaces fail before any device work
+    assert L.moe_route(C.byref(c), 16, 16, None, 16, 16, None, None, 0, None) == N.MOE_ERR_WORKSPACE
+    assert L.moe_route(C.byref(c), 16, 16, None, 16, 16, None, 0x1008, 4096, None) == N.MOE_ERR_WORKSPACE
+    assert L.moe_combine(C.byref(c), 16, 16, None, 32, 0x1000, 16, None) == N.MOE_ERR_WORKSPACE
+
+
+def test_pointer_checks_before_launch(L):
+    c = cfg()
+    ws = 0x10000
+    # NULL x, misaligned x, NULL outputs
+    assert L.moe_route(C.byref(c), None, 16, None, 16, 16, None, ws, 256, None) == N.MOE_ERR_INVALID_ARG
+    assert L.moe_route(C.byref(c), 0x1002, 16, None, 16, 16, None, ws, 256, None) == N.MOE_ERR_INVALID_ARG
+    assert L.moe_route(C.byref(c), 16, 16, None, None, 16, None, ws, 256, None) == N.MOE_ERR_INVALID_ARG
+    assert b"topk_ids" in L.moe_last_error_message()
+    assert L.moe_combine(C.byref(c), 16, 16, None, 16, ws, 256, None) == N.MOE_ERR_INVALID_ARG  # alias
+    assert L.moe_combine(C.byref(c), None, 16, None, 32, ws, 256, None) == N.MOE_ERR_INVALID_ARG
+
+
+def test_zero_tokens_is_a_noop(L):
+    c = cfg(T=0)
+    # T = 0 returns OK without touching any pointer or launching anything
+    assert L.moe_route(C.byref(c), None, None, None, None, None, None, 0x10000, 256, None) == N.MOE_OK
+    assert L.moe_combine(C.byref(c), None, None, None, None, 0x10000, 256, None) == N.MOE_OK
+
+
+def test_weights_create_validates(L):
+    c = cfg()
+    wl = N.MoeWeightList()
+    h = C.c_void_p()
+    assert L.moe_weights_create(C.byref(c), C.byref(wl), C.byref(h)) == N.MOE_ERR_INVALID_ARG
+    arr = (C.c_void_p * 8)(*([0x1000] * 7 + [0x1001]))
+    wl.gate = wl.up = wl.down = C.cast(arr, C.POINTER(C.c_void_p))
+    assert L.moe_weights_create(C.byref(c), C.byref(wl), C.byref(h)) == N.MOE_ERR_INVALID_ARG
+    assert b"gate[7]" in L.moe_last_error_message()
+    assert h.value is None
+    assert L.moe_weights_create(None, C.byref(wl), C.byref(h)) == N.MOE_ERR_INVALID_ARG
+
+
+def test_quantize_validation(L):
+    assert L.moe_quantize_weight_fp8(16, 100, 128, 16, 16, None) == N.MOE_ERR_INVALID_ARG
+    assert L.moe_quantize_act_fp8(16, 4, 100, 16, 16, None) == N.MOE_ERR_INVALID_ARG
+    assert L.moe_quantize_act_fp8(None, 0, 128, None, None, None) == N.MOE_OK

@@ -1,0 +1,75 @@
+"""moe_forward (route -> permute -> grouped FFN -> combine, one call) on the GPU
+against the oracle: whole outputs on small layers, and at the five workloads'
+full sizes, routing over every token plus sampled output rows computed one
+token at a time by the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import moe_expert_layer_router_gb300 as m
+import workload as wl
+from oracle import moe as om
+from parity import Layer, assert_close_layer, f64, logit_tolerance, near_tie_tokens
+
+pytestmark = pytest.mark.gpu
+
+
+def forward(L, lc):
+    cfg = m.config_from(lc)
+    W = m.ExpertWeights(cfg, [w[0] for w in L.W], [w[1] for w in L.W], [w[2] for w in L.W],
+                        shared=L.S)
+    ws = m.Workspace(cfg, "forward")
+    out, ids, w = m.moe_forward(cfg, W, L.x, L.wr, L.bias, return_routing=True, ws=ws)
+    torch.cuda.synchronize()
+    m.moe_get_device_error(ws)
+    return out, ids.cpu().numpy(), w.cpu().numpy()
+
+
+SMALL = [
+    wl.TINY,
+    wl.TINY.with_(name="tiny_sigmoid_shared", T=200, I_shared=256, score="sigmoid", route_scale=2.5),
+    wl.DSV3.with_(name="dsv3_shape_T64", T=64, E=32, k=4, I=256, I_shared=256),
+    wl.TINY.with_(name="skewish", T=700, E=16, k=3, H=384, I=128, zipf_bias=False),
+]
+
+
+@pytest.mark.parametrize("lc", SMALL, ids=lambda c: c.name)
+def test_forward_small_matches_oracle(lc):
+    dev = torch.device("cuda")
+    L = Layer(lc, dev)
+    out, ids, w = forward(L, lc)
+    ref = om.moe_layer(f64(L.x), f64(L.wr), None, L.experts_cpu, L.shared_cpu(), lc.k, lc.score,
+                       lc.renormalize, lc.route_scale)
+    tie = near_tie_tokens(ref["logits"], lc.k, logit_tolerance(L.x, L.wr))
+    assert (ids[~tie] == ref["ids"][~tie]).all()
+    keep = ~tie & (ids == ref["ids"]).all(axis=1)
+    assert_close_layer(out.float().cpu().numpy()[keep], ref["out"][keep], what=lc.name)
+
+
+FULL = [wl.QWEN3, wl.DSV3, wl.DSV3_SKEW]
+
+
+@pytest.mark.parametrize("lc", FULL, ids=lambda c: c.name)
+def test_forward_full_size_sampled(lc):
+    dev = torch.device("cuda")
+    L = Layer(lc, dev)
+    out, ids, w = forward(L, lc)
+    b = None if L.bias is None else f64(L.bias)
+    ref_lg = om.router_logits(f64(L.x), f64(L.wr), b)
+    ref_ids = om.select_topk(ref_lg, lc.k)
+    tie = near_tie_tokens(ref_lg, lc.k, logit_tolerance(L.x, L.wr))
+    assert (ids[~tie] == ref_ids[~tie]).all()
+    counts, _ = om.expert_histogram(ref_ids, lc.E)
+    if lc.zipf_bias:                                   # the workload's defining skew
+        assert 8.5 <= counts.max() / counts.mean() <= 11.5 and (counts == 0).sum() >= 4
+    g = np.random.default_rng(0)
+    cand = np.flatnonzero(~tie)
+    sample = np.sort(g.choice(cand, size=6, replace=False))
+    ref_w = om.routing_weights(ref_lg[sample], ref_ids[sample], lc.score, lc.renormalize,
+                               lc.route_scale)
+    ref = om.moe_tokens(f64(L.x[torch.from_numpy(sample).to(dev)]), ref_ids[sample], ref_w,
+                        L.experts_cpu, L.shared_cpu())
+    assert_close_layer(out[torch.from_numpy(sample).to(dev)], ref, what=f"{lc.name} sampled")
+    assert torch.isfinite(out.float()).all()
+    print(f"{lc.name}: T={lc.T} near-tie tokens {int(tie.sum())}, max/mean rows "
+          f"{counts.max() / counts.mean():.2f}")
