@@ -193,6 +193,29 @@ MOE_API moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_id
                          void* x_perm, float* x_perm_scales, void* ws, size_t ws_bytes,
                          moe_stream_t stream);
 
+/* moe_permute without a workspace: the same histogram and permutation, with
+ * the same outputs, for callers that cannot allocate device memory -- code
+ * recording a CUDA graph, runtimes whose memory is planned once at start-up,
+ * plugins that are handed only their input and output tensors.  The pages
+ * have no counterpart of this call; it is a property of this library.
+ * Scratch: a fixed device array inside the library (about 2 MB, held by every
+ * GPU that loads the library until exit), enough for E * ceil(T/64) <= 262144
+ * (e.g. T <= 65536 at E = 256); larger layers get MOE_ERR_UNSUPPORTED and must
+ * use moe_permute.  The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress) and should come before any stream capture.
+ * Calls allocate nothing.  All calls share the array: calls that run
+ * concurrently on the GPU race and must be ordered (one stream, or events).
+ *   device_status  optional device word (4-byte aligned) that receives the
+ *                  status bits (as moe_get_device_error reports them); NULL
+ *                  discards them.
+ * Every other argument is as for moe_permute. */
+MOE_API moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const int32_t* topk_ids,
+                                         const float* topk_w, const void* x,
+                                         int32_t* expert_counts, int32_t* expert_offsets,
+                                         int32_t* perm_token, int32_t* inv_row, float* row_weight,
+                                         void* x_perm, float* x_perm_scales,
+                                         uint32_t* device_status, moe_stream_t stream);
+
 /* Steps 3+4 -- grouped expert FFN (ASAP section 3.4.2 grouped matrix
  * multiplication; DWDP section 4.2 pointer-list weights):
  *   y_perm[r] = row_weight[r] * W_down[e] (silu(W_gate[e] x_perm[r]) * (W_up[e] x_perm[r]))

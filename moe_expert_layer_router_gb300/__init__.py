@@ -21,7 +21,7 @@ from . import _native as N
 from ._native import MoeConfig, MoeError
 
 __all__ = ["MoeConfig", "MoeError", "make_config", "config_from", "Workspace", "ExpertWeights",
-           "moe_route", "moe_permute", "moe_grouped_ffn", "moe_combine", "moe_forward",
+           "moe_route", "moe_permute", "moe_permute_noalloc", "moe_grouped_ffn", "moe_combine", "moe_forward",
            "moe_quantize_weight_fp8", "moe_quantize_act_fp8", "moe_get_device_error",
            "moe_workspace_size", "load"]
 
@@ -215,6 +215,40 @@ def moe_permute(cfg: MoeConfig, topk_ids, topk_w=None, x=None, *, ws=None, strea
                                 _ptr(o["perm_token"]), _ptr(o["inv_row"]), _ptr(o["row_weight"]),
                                 _ptr(o["x_perm"]), _ptr(o["x_perm_scales"]), ws.ptr, ws.nbytes,
                                 _stream(stream)), "moe_permute")
+    return o
+
+
+def moe_permute_noalloc(cfg: MoeConfig, topk_ids, topk_w=None, x=None, *, device_status=None,
+                        stream=None):
+    """moe_permute for callers that cannot allocate device scratch: the library's
+    fixed scratch array replaces the workspace (E * ceil(T/64) <= 262144).  The
+    outputs here are still allocated by torch for convenience; a caller that
+    cannot allocate passes its own buffers to the C entry point directly.
+    device_status: optional int32 [1] device tensor that receives the status bits."""
+    dev = topk_ids.device
+    T, k, E, H = cfg.T, cfg.k, cfg.E, cfg.H
+    R = T * k
+    _need(topk_ids, "topk_ids", torch.int32, (T, k), dev)
+    if topk_w is not None:
+        _need(topk_w, "topk_w", torch.float32, (T, k), dev)
+    fp8 = cfg.wtype == N.MOE_DTYPE_FP8_E4M3
+    o = {"expert_counts": torch.empty(E, dtype=torch.int32, device=dev),
+         "expert_offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+         "perm_token": torch.empty(R, dtype=torch.int32, device=dev),
+         "inv_row": torch.empty(T, k, dtype=torch.int32, device=dev),
+         "row_weight": torch.empty(R, dtype=torch.float32, device=dev) if topk_w is not None else None,
+         "x_perm": None, "x_perm_scales": None}
+    if x is not None:
+        _need(x, "x", torch.bfloat16, (T, H), dev)
+        o["x_perm"] = torch.empty(R, H, dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
+        if fp8:
+            o["x_perm_scales"] = torch.empty(R, H // 128, dtype=torch.float32, device=dev)
+    N.check(N.lib().moe_permute_noalloc(C.byref(cfg), _ptr(topk_ids), _ptr(topk_w), _ptr(x),
+                                        _ptr(o["expert_counts"]), _ptr(o["expert_offsets"]),
+                                        _ptr(o["perm_token"]), _ptr(o["inv_row"]),
+                                        _ptr(o["row_weight"]), _ptr(o["x_perm"]),
+                                        _ptr(o["x_perm_scales"]), _ptr(device_status),
+                                        _stream(stream)), "moe_permute_noalloc")
     return o
 
 

@@ -62,6 +62,7 @@ _SIG = {
     "moe_quantize_weight_fp8": (C.c_int, [_P, C.c_int64, C.c_int64, _P, _P, _P]),
     "moe_quantize_act_fp8": (C.c_int, [_P, C.c_int64, C.c_int64, _P, _P, _P]),
     "moe_set_trace": (C.c_int, [C.POINTER(MoeTrace)]),
+    "moe_permute_noalloc": (C.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 
 _lib = None

@@ -32,6 +32,10 @@ static moe_status_t fail(moe_status_t s, const char* fmt, ...) {
   return s;
 }
 
+// Lets other translation units report host-side failures through
+// moe_last_error_message().
+void set_last_error_text(const char* msg) { g_last_error = msg ? msg : ""; }
+
 static moe_status_t cuda_fail(cudaError_t e, const char* where) {
   return fail(MOE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
 }

@@ -89,6 +89,9 @@ namespace moe {
 // Raises a kernel's dynamic shared-memory limit on the current device (once per device).
 cudaError_t ensure_smem_attr(const void* func, int bytes);
 
+// Sets the text returned by moe_last_error_message() on the calling thread.
+void set_last_error_text(const char* msg);
+
 // Kernel tracing (see moe_set_trace): records an event before kernel `id` on
 // `stream` (id = -1: after the last kernel of a call).  No-op without a trace.
 void trace_mark(cudaStream_t stream, int id);
