@@ -80,7 +80,11 @@ DSV3 = LayerConfig("dsv3", T=16384, H=7168, E=256, k=8, I=2048, I_shared=2048,
 DSV3_SKEW = DSV3.with_(name="dsv3_skewed", T=sum(skewed_lengths(0)), zipf_bias=True)
 DSV3_FP8 = DSV3.with_(name="dsv3_fp8", T=512, wtype="fp8_e4m3")
 
-CONFIGS = {c.name: c for c in (TINY, QWEN3, DSV3, DSV3_SKEW, DSV3_FP8)}
+# Profiling slice: DeepSeek-V3 expert shapes and rows per expert (T*k/E = 512), a
+# quarter of the experts and tokens, so that one ncu capture holds a few GB.
+DSV3_SLICE = DSV3.with_(name="dsv3_slice", T=4096, E=64)
+
+CONFIGS = {c.name: c for c in (TINY, QWEN3, DSV3, DSV3_SKEW, DSV3_FP8, DSV3_SLICE)}
 
 
 # ---------------------------------------------------------------- tensors
