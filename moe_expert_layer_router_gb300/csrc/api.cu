@@ -66,6 +66,19 @@ static int sm_count() {
   return n;
 }
 
+static int gemm_grid() {
+  static std::mutex mu;
+  static std::unordered_map<int, int> cache;
+  const int n = sm_count();
+  const int d = current_device();
+  std::lock_guard<std::mutex> g(mu);
+  auto it = cache.find(d);
+  if (it != cache.end()) return it->second;
+  const int grid = grouped_gemm_grid(n);
+  cache[d] = grid;
+  return grid;
+}
+
 cudaError_t ensure_smem_attr(const void* func, int bytes) {
   static std::mutex mu;
   static std::unordered_map<const void*, uint64_t> done;  // device bitmask per kernel
@@ -354,11 +367,11 @@ moe_status_t moe_weights_create(const moe_config_t* cfg, const moe_weight_list_t
     const bool sh = g == E;
     const uint64_t inter = sh ? Is : I;
     MOE_TRY(encode_2d(&m1[2 * g], true, sh ? wl->shared_gate : wl->gate[g], H, inter, kTileK,
-                      kGemm1TileN));
+                      kGemmBRows / 2));
     MOE_TRY(encode_2d(&m1[2 * g + 1], true, sh ? wl->shared_up : wl->up[g], H, inter, kTileK,
-                      kGemm1TileN));
+                      kGemmBRows / 2));
     MOE_TRY(encode_2d(&m2[g], true, sh ? wl->shared_down : wl->down[g], inter, H, kTileK,
-                      kGemm2TileN));
+                      kGemmBRows));
   }
   void* table = nullptr;
   const size_t bytes = maps.size() * sizeof(CUtensorMap);
@@ -462,7 +475,7 @@ static moe_status_t run_ffn(const moe_config_t& c, const moe_weights* W, const L
   g1.K_shared = c.H;
   g1.N_routed = c.I;
   g1.N_shared = c.I_shared;
-  const int grid = sm_count();
+  const int grid = gemm_grid();
   trace_mark(st, MOE_K_GEMM1);
   MOE_CUDA(launch_grouped_gemm(true, a0, a1, g1, grid, st));
 

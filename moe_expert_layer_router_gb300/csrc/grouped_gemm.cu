@@ -1,4 +1,5 @@
-// Persistent grouped GEMM on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+// Persistent grouped GEMM on the sm_103a tensor cores: CTA pairs (tcgen05
+// cta_group::2), TMEM accumulators, TMA loads.
 //
 // One launch covers every expert of a layer: the hidden-state rows of expert
 // e (its segment of the permuted activations) times that expert's weight
@@ -9,39 +10,59 @@
 // High-Performance LLM Inference on NVL72", section 4.2).  The shared expert
 // is one more group whose rows are the unpermuted tokens.
 //
-//   GEMM1 (kSwiGLU):  h = silu(A W_gate^T) * (A W_up^T)      tile 128 x (128 gate + 128 up), bf16 out
-//   GEMM2:            y = row_weight * (A W_down^T)          tile 128 x 256, fp32 out
+//   GEMM1 (kSwiGLU):  h = silu(A W_gate^T) * (A W_up^T)   bf16 out
+//   GEMM2:            y = row_weight * (A W_down^T)       fp32 out
 // (y stays fp32 so that the k expert rows of a token are rounded to bf16 only
 // once, after the combine has summed them.)
 //
-// Warp roles (192 threads, one CTA per SM):
-//   warp 0      TMA producer (one lane): A tile + B tile(s) per 64-wide K step
-//   warp 1      TMEM allocator; one lane issues tcgen05.mma (128 x 256 x 16)
-//   warps 2..5  epilogue: TMEM -> registers -> SwiGLU (bf16) / row scale (fp32) -> HBM
-// Shared memory holds a 4-stage ring of 48 KB stages; TMEM holds two 128x256
-// fp32 accumulators so the epilogue of tile i overlaps the MMAs of tile i+1.
-// Tiles come from a device-built schedule (heaviest group first) and are
-// dealt to the persistent CTAs round robin.
+// Work unit: a 256-row x 256-column pair tile computed by the two CTAs of a
+// cluster with one 256x256x16 MMA per 16-wide K step.  Each CTA loads its own
+// 128 rows of A and one half of B, so a stage is 32 KB per CTA (instead of 48
+// KB for a single-CTA 128x256 tile) and the ring holds 6 stages.  B halves:
+//   GEMM1: CTA r loads W_gate and W_up rows [128 n + 64 r, +64) (64 + 64 rows),
+//          so TMEM columns are [gate | up] of output columns 128 n + 64 r + [0,64)
+//   GEMM2: CTA r loads W_down rows [256 n + 128 r, +128)
+// An expert's last tile, when at most 128 rows are left, is a half tile: an
+// M=128 pair MMA (64 rows per CTA, half the time of M=256).  Its TMEM layout
+// (measured): CTA r holds rows 64 r + [0,64); lanes 0-63 carry the first 128
+// output columns of the pair and lanes 64-127 the same rows' other 128, both in
+// TMEM columns 0-127.  Either way every epilogue thread owns one output row and
+// holds both the gate and the up value of each of its columns.
+//
+// Warp roles per CTA (192 threads, one CTA per SM):
+//   warp 0      TMA producer (one lane), completing on the even CTA's barriers
+//   warp 1      pair-collective TMEM allocation; in the even CTA one lane
+//               issues the pair MMAs and multicasts their completion
+//   warps 2..5  epilogue: TMEM -> registers -> SwiGLU / row scale -> HBM
+// TMEM holds two 256-column fp32 accumulators, so the epilogue of tile i
+// overlaps the MMAs of tile i+1.  Tiles come from a device-built schedule
+// (heaviest group first) and are dealt to the persistent pairs round robin.
 #include "moe_internal.h"
 #include "ptx.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kThreads = 192;
-constexpr int kABytes = kTileM * kTileK * 2;  // 16 KB
-constexpr int kBRows = 256;                   // UMMA N
-constexpr int kBBytes = kBRows * kTileK * 2;  // 32 KB
+constexpr int kPairRows = kGemmTileRows;      // 256 rows per pair tile (128 per CTA)
+static_assert(kPairRows == 2 * kTileM, "a pair tile is two CTA tiles");
+static_assert(2 * kGemmBRows == 256 && kGemm1TileN == kGemmBRows && kGemm2TileN == 2 * kGemmBRows,
+              "each CTA loads one 128-row half of the 256-row B operand");
+constexpr int kABytes = kTileM * kTileK * 2;  // 16 KB: this CTA's 128 rows
+constexpr int kBBytes = kGemmBRows * kTileK * 2;  // 16 KB: this CTA's half of B (TMA box)
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr uint32_t kIdesc = ptx::idesc_bf16(kTileM, kBRows);
-constexpr uint32_t kTmemCols = 512;  // two 256-column fp32 accumulators
+constexpr int kTileN = 256;                   // UMMA N (both CTAs' B halves)
+constexpr uint32_t kIdescFull = ptx::idesc_bf16(kPairRows, kTileN);
+constexpr uint32_t kIdescHalf = ptx::idesc_bf16(kTileM, kTileN);
+constexpr uint32_t kTmemCols = 512;           // two 256-column fp32 accumulators
+constexpr uint16_t kBothCtas = 0x3;
 
 struct __align__(8) SmemCtl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t full[kStages];    // even CTA: both CTAs' loads of a stage landed
+  uint64_t empty[kStages];   // both CTAs: the pair MMAs of a stage are done
+  uint64_t tfull[2];         // both CTAs: an accumulator is complete
+  uint64_t tempty[2];        // even CTA: both epilogues drained an accumulator
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -53,10 +74,10 @@ constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + sizeof(Smem
 
 struct Tile {
   int g, m_blk, n_blk, rows, row0, K, N;
+  bool half;  // at most 128 rows left: M=128 pair MMA, 64 rows per CTA
 };
 
-__device__ __forceinline__ Tile decode_tile(int t, const SmemCtl& c, const GemmArgs& a, int G,
-                                            int tile_n) {
+__device__ __forceinline__ Tile decode_tile(int t, const SmemCtl& c, const GemmArgs& a, int G) {
   const int32_t* ts = c.sched + 1;
   int lo = 0, hi = G - 1;
   while (lo < hi) {  // last slot whose first tile is <= t
@@ -71,10 +92,10 @@ __device__ __forceinline__ Tile decode_tile(int t, const SmemCtl& c, const GemmA
   x.row0 = routed ? c.offsets[x.g] : 0;
   x.K = routed ? a.K_routed : a.K_shared;
   x.N = routed ? a.N_routed : a.N_shared;
-  const int mt = (x.rows + kTileM - 1) / kTileM;
+  const int mt = (x.rows + kPairRows - 1) / kPairRows;
   x.n_blk = local / mt;
   x.m_blk = local - x.n_blk * mt;
-  (void)tile_n;
+  x.half = x.rows - x.m_blk * kPairRows <= kTileM;
   return x;
 }
 
@@ -85,8 +106,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Bounded wait without the abort short-cut: used only while draining copies
-// that are certain to complete, before the CTA exits.
+// Bounded wait without the abort short-cut, used only while draining work
+// that is certain to complete before the CTA exits.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
   const uint64_t t0 = ptx::globaltimer();
   while (!ptx::mbar_try_wait(bar, parity)) {
@@ -98,7 +119,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint3
 }
 
 template <bool kSwiGLU>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a0,
                              const __grid_constant__ CUtensorMap map_a1, const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -110,8 +131,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();  // 0: issues the pair MMAs
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
   const int G = args.E + args.has_shared;
-  const int tile_n = kSwiGLU ? kGemm1TileN : kGemm2TileN;
 
   for (int i = threadIdx.x; i < sched_ints(G); i += kThreads) c.sched[i] = args.sched[i];
   for (int i = threadIdx.x; i <= args.E; i += kThreads) c.offsets[i] = args.offsets[i];
@@ -122,15 +146,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&c.tfull[s], 1);
-      ptx::mbar_init(&c.tempty[s], 4);
+      ptx::mbar_init(&c.tempty[s], 8);  // 4 epilogue warps in each CTA
     }
     ptx::mbar_init(&c.drain, 1);
     c.abort = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(&c.tmem_base, kTmemCols);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc_pair(&c.tmem_base, kTmemCols);
+    ptx::tmem_relinquish_pair();
   }
   if (threadIdx.x == 0) {
     ptx::prefetch_tmap(&map_a0);
@@ -138,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
+  ptx::cluster_sync();  // both CTAs' barriers exist before anyone signals them
   ptx::tc_fence_after();
   const uint32_t tmem_base = c.tmem_base;
   const int num_tiles = c.sched[0];
@@ -145,52 +170,65 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ------------------------------------------------ TMA producer
+      // ------------------------------------------------ TMA producer (both CTAs)
+      const uint32_t full0 = ptx::mapa(ptx::smem_u32(&c.full[0]), 0);
       uint32_t it = 0;
-      for (int t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
-        const Tile x = decode_tile(t, c, args, G, tile_n);
+      for (int t = pair; t < num_tiles && !*abort; t += num_pairs) {
+        const Tile x = decode_tile(t, c, args, G);
         const void* map_a = x.g < args.E ? static_cast<const void*>(&map_a0)
                                          : static_cast<const void*>(&map_a1);
-        const CUtensorMap* mb = kSwiGLU ? args.b_maps + 2 * x.g : args.b_maps + x.g;
-        const int a_row = x.row0 + x.m_blk * kTileM;
+        const CUtensorMap* mb;
+        int b_row;
+        if (kSwiGLU) {  // CTA r: gate and up rows [128 n + 64 r, +64)
+          mb = args.b_maps + 2 * x.g;
+          b_row = x.n_blk * kGemm1TileN + int(rank) * (kGemmBRows / 2);
+        } else {        // CTA r: W_down rows [256 n + 128 r, +128)
+          mb = args.b_maps + x.g;
+          b_row = x.n_blk * kGemm2TileN + int(rank) * kGemmBRows;
+        }
+        // A rows of this CTA: 128 (full tile) or 64 (half tile; the box still
+        // brings 128 rows, the MMA reads the first 64)
+        const int a_row = x.row0 + x.m_blk * kPairRows + int(rank) * (x.half ? kTileM / 2 : kTileM);
         const int kb_n = x.K / kTileK;
         bool ok = true;
         for (int kb = 0; kb < kb_n; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
           if (!ptx::mbar_wait(&c.empty[s], ph ^ 1, abort, args.err)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(&c.full[s], kStageBytes);
-          ptx::tma_load_2d(a_tiles + s * kABytes, map_a, &c.full[s], kb * kTileK, a_row);
+          if (leader) ptx::mbar_arrive_expect_tx(&c.full[s], 2 * kStageBytes);
+          const uint32_t fb = full0 + s * 8;
+          ptx::tma_load_2d_pair(a_tiles + s * kABytes, map_a, fb, kb * kTileK, a_row);
           uint8_t* bs = b_tiles + s * kBBytes;
           if (kSwiGLU) {
-            ptx::tma_load_2d(bs, mb, &c.full[s], kb * kTileK, x.n_blk * kGemm1TileN);
-            ptx::tma_load_2d(bs + kBBytes / 2, mb + 1, &c.full[s], kb * kTileK,
-                             x.n_blk * kGemm1TileN);
+            ptx::tma_load_2d_pair(bs, mb, fb, kb * kTileK, b_row);
+            ptx::tma_load_2d_pair(bs + kBBytes / 2, mb + 1, fb, kb * kTileK, b_row);
           } else {
-            ptx::tma_load_2d(bs, mb, &c.full[s], kb * kTileK, x.n_blk * kGemm2TileN);
+            ptx::tma_load_2d_pair(bs, mb, fb, kb * kTileK, b_row);
           }
         }
         if (!ok) break;
       }
-      if (*abort) {
-        // Let every load already issued land before the CTA leaves.
+      if (*abort && leader) {
+        // Both CTAs' loads of a stage complete on the even CTA's barrier: wait
+        // for the stages issued last so no copy is in flight at exit.
         const uint32_t first = it > kStages ? it - kStages : 0;
         for (uint32_t j = first; j < it; ++j)
           drain_wait(&c.full[j % kStages], (j / kStages) & 1, args.err);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------ MMA issuer
+    if (lane == 0 && leader) {
+      // ------------------------------------------------ pair MMA issuer
       uint32_t it = 0;
       int local = 0;
-      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
-        const Tile x = decode_tile(t, c, args, G, tile_n);
+      for (int t = pair; t < num_tiles; t += num_pairs, ++local) {
+        const Tile x = decode_tile(t, c, args, G);
         const int acc = local & 1;
         const uint32_t acc_ph = (local >> 1) & 1;
         if (!ptx::mbar_wait(&c.tempty[acc], acc_ph ^ 1, abort, args.err)) break;
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * kBRows;
+        const uint32_t d_tmem = tmem_base + acc * kTileN;
+        const uint32_t idesc = x.half ? kIdescHalf : kIdescFull;
         const int kb_n = x.K / kTileK;
         bool ok = true;
         for (int kb = 0; kb < kb_n; ++kb, ++it) {
@@ -202,71 +240,87 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t db = ptx::sw128_desc(ptx::smem_u32(b_tiles + s * kBBytes));
 #pragma unroll
           for (int k = 0; k < kTileK / 16; ++k)
-            ptx::mma_f16(d_tmem, da + 2 * k, db + 2 * k, kIdesc, (kb | k) != 0);
-          ptx::mma_commit(&c.empty[s]);
+            ptx::mma_f16_pair(d_tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+          ptx::mma_commit_pair_mc(&c.empty[s], kBothCtas);
         }
         if (!ok) break;
-        ptx::mma_commit(&c.tfull[acc]);
+        ptx::mma_commit_pair_mc(&c.tfull[acc], kBothCtas);
       }
-      // Every MMA issued by this thread has finished once `drain` flips.
-      ptx::mma_commit(&c.drain);
+      // Every pair MMA issued by this thread has finished once `drain` flips.
+      ptx::mma_commit_pair_mc(&c.drain, 0x1);
       drain_wait(&c.drain, 0, args.err);
     }
   } else {
     // -------------------------------------------------- epilogue (warps 2..5)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;
+    const uint32_t tempty0 = ptx::mapa(ptx::smem_u32(&c.tempty[0]), 0);
     int local = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
-      const Tile x = decode_tile(t, c, args, G, tile_n);
+    for (int t = pair; t < num_tiles; t += num_pairs, ++local) {
+      const Tile x = decode_tile(t, c, args, G);
       const int acc = local & 1;
       const uint32_t acc_ph = (local >> 1) & 1;
       if (!ptx::mbar_wait(&c.tfull[acc], acc_ph, abort, args.err)) break;
       ptx::tc_fence_after();
-      const int m = x.m_blk * kTileM + r;
+      // Row of this thread and, for half tiles, which 128-column half of the
+      // pair's N it holds (warp-uniform: lane quarters 0-1 vs 2-3).
+      const int hs = x.half ? (r >> 6) : 0;
+      const int m = x.m_blk * kPairRows +
+                    (x.half ? int(rank) * (kTileM / 2) + (r & 63) : int(rank) * kTileM + r);
       const bool valid = m < x.rows;
       const bool routed = x.g < args.E;
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBRows;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN;
       if (kSwiGLU) {
+        // full tile: TMEM columns [g | u] of output columns 128 n + [0,64), then
+        // [g | u] of 128 n + [64,128); half tile: one [g | u] block, the one of
+        // CTA-half hs.
         __nv_bfloat16* dst = nullptr;
         if (valid)
           dst = (routed ? static_cast<__nv_bfloat16*>(args.out0) + int64_t(x.row0 + m) * x.N
                         : static_cast<__nv_bfloat16*>(args.out1) + int64_t(m) * x.N) +
                 x.n_blk * kGemm1TileN;
+        const int nblocks = x.half ? 1 : 2;
 #pragma unroll 1
-        for (int cb = 0; cb < kGemm1TileN / 32; ++cb) {
-          uint32_t gr[32], ur[32];
-          ptx::tmem_ld32(taddr + cb * 32, gr);
-          ptx::tmem_ld32(taddr + kGemm1TileN + cb * 32, ur);
-          ptx::tmem_ld_wait();
-          if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + cb * 32);
+        for (int blk = 0; blk < nblocks; ++blk) {
+          const int out_col = (x.half ? hs : blk) * 64;
+#pragma unroll 1
+          for (int cb = 0; cb < 2; ++cb) {
+            uint32_t gr[32], ur[32];
+            ptx::tmem_ld32(taddr + blk * 128 + cb * 32, gr);
+            ptx::tmem_ld32(taddr + blk * 128 + 64 + cb * 32, ur);
+            ptx::tmem_ld_wait();
+            if (valid) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + out_col + cb * 32);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint32_t p[4];
+              for (int v = 0; v < 4; ++v) {
+                uint32_t p[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int i = v * 8 + e * 2;
-                const float h0 = silu_f(__uint_as_float(gr[i])) * __uint_as_float(ur[i]);
-                const float h1 = silu_f(__uint_as_float(gr[i + 1])) * __uint_as_float(ur[i + 1]);
-                p[e] = pack_bf16(h0, h1);
+                for (int e = 0; e < 4; ++e) {
+                  const int i = v * 8 + e * 2;
+                  const float h0 = silu_f(__uint_as_float(gr[i])) * __uint_as_float(ur[i]);
+                  const float h1 = silu_f(__uint_as_float(gr[i + 1])) * __uint_as_float(ur[i + 1]);
+                  p[e] = pack_bf16(h0, h1);
+                }
+                d4[v] = make_uint4(p[0], p[1], p[2], p[3]);
               }
-              d4[v] = make_uint4(p[0], p[1], p[2], p[3]);
             }
           }
         }
       } else {
+        // full tile: 256 TMEM columns = output columns 256 n + [0,256);
+        // half tile: 128 TMEM columns = output columns 256 n + 128 hs + [0,128)
         float w = 1.0f;
         float* dst = nullptr;
         if (valid) {
           if (routed && args.row_weight) w = args.row_weight[x.row0 + m];
           dst = (routed ? static_cast<float*>(args.out0) + int64_t(x.row0 + m) * x.N
                         : static_cast<float*>(args.out1) + int64_t(m) * x.N) +
-                x.n_blk * kGemm2TileN;
+                x.n_blk * kGemm2TileN + hs * 128;
         }
+        const int ncb = (x.half ? 128 : kGemm2TileN) / 32;
 #pragma unroll 1
-        for (int cb = 0; cb < kGemm2TileN / 32; ++cb) {
-          if (x.n_blk * kGemm2TileN + cb * 32 >= x.N) break;  // warp-uniform
+        for (int cb = 0; cb < ncb; ++cb) {
+          if (x.n_blk * kGemm2TileN + hs * 128 + cb * 32 >= x.N) break;  // warp-uniform
           uint32_t yr[32];
           ptx::tmem_ld32(taddr + cb * 32, yr);
           ptx::tmem_ld_wait();
@@ -281,15 +335,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&c.tempty[acc]);
+      if (lane == 0) ptx::mbar_arrive_cluster(tempty0 + acc * 8);
     }
   }
 
   ptx::tc_fence_before();
   __syncthreads();
+  ptx::cluster_sync();  // the pair's MMAs, copies and remote arrivals are over
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, kTmemCols);
+    ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -303,7 +358,39 @@ cudaError_t launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const Gemm
   return cudaGetLastError();
 }
 
+template <bool kSwiGLU>
+int max_pairs() {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_bf16_kernel<kSwiGLU>, &cfg) != cudaSuccess)
+    return 0;
+  return n;
+}
+
 }  // namespace
+
+int grouped_gemm_grid(int sm_count) {
+  // One CTA pair for every pair of SMs that can hold one at the same time.
+  ensure_smem_attr(reinterpret_cast<const void*>(grouped_gemm_bf16_kernel<true>),
+                   static_cast<int>(kSmemBytes));
+  ensure_smem_attr(reinterpret_cast<const void*>(grouped_gemm_bf16_kernel<false>),
+                   static_cast<int>(kSmemBytes));
+  int pairs = max_pairs<true>();
+  const int p2 = max_pairs<false>();
+  if (p2 > 0 && (pairs <= 0 || p2 < pairs)) pairs = p2;
+  if (pairs <= 0 || pairs > sm_count / 2) pairs = sm_count / 2;
+  return 2 * (pairs > 0 ? pairs : 1);
+}
 
 cudaError_t launch_grouped_gemm(bool swiglu, const CUtensorMap& map_a0, const CUtensorMap& map_a1,
                                 const GemmArgs& args, int grid, cudaStream_t stream) {

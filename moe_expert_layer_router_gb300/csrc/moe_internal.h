@@ -26,6 +26,8 @@ constexpr int kGemm2TileN = 256;   // y columns per GEMM2 tile
 constexpr int kMaxExperts = 256;
 constexpr int kMaxGroups = kMaxExperts + 1;  // routed experts + the shared expert
 constexpr int kPermTok = 64;       // tokens per histogram / scatter block
+constexpr int kGemmTileRows = 256; // rows of one grouped-GEMM work tile (a CTA pair)
+constexpr int kGemmBRows = 128;    // weight rows one CTA of the pair loads per stage (TMA box)
 
 // Tile schedule of one grouped GEMM, in device memory (int32):
 //   [0]            number of tiles
@@ -65,6 +67,10 @@ cudaError_t launch_scatter(const int32_t* ids, const float* topk_w, const void* 
                            const int32_t* offsets, int32_t* perm_token, int32_t* inv_row,
                            float* row_weight, void* x_perm, float* x_perm_scales, uint32_t* err,
                            cudaStream_t stream);
+
+// Grid (a multiple of 2) of the grouped GEMMs: as many CTA pairs as the
+// device can hold at once.
+int grouped_gemm_grid(int sm_count);
 
 cudaError_t launch_plan(const int32_t* offsets, int E, int has_shared, int64_t T, int n1_routed,
                         int n1_shared, int n2_routed, int n2_shared, int32_t* sched1,

@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(kScatterThreads)
 }
 
 // Tile schedules of GEMM1 and GEMM2 from the row offsets: per group
-// ceil(rows/128) x n_tiles tiles; groups ordered by descending tile count
+// ceil(rows/256) x n_tiles tiles; groups ordered by descending tile count
 // (ties: lower group first) so the heaviest experts start first.
 __global__ void __launch_bounds__(256)
     plan_kernel(const int32_t* __restrict__ offsets, int E, int has_shared, int64_t T,
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(256)
   const int G = E + has_shared;
   for (int g = threadIdx.x; g < G; g += blockDim.x) {
     const int64_t rows = g < E ? int64_t(offsets[g + 1]) - offsets[g] : T;
-    const int mt = static_cast<int>((rows + kTileM - 1) / kTileM);
+    const int mt = static_cast<int>((rows + kGemmTileRows - 1) / kGemmTileRows);
     tiles[0][g] = mt * (g < E ? n1r : n1s);
     tiles[1][g] = mt * (g < E ? n2r : n2s);
   }
