@@ -176,7 +176,9 @@ def describe(lc) -> str:
 
 
 class Layer:
-    """Seeded layer on one device; every expert matrix in its own allocation."""
+    """Seeded layer on one device; every expert matrix in its own allocation.
+    fp8 layers: the fp32 weights are block-quantised by the library once, before
+    any timing (W holds the fp32 originals, which the oracle baseline uses)."""
 
     def __init__(self, lc, dev):
         import moe_expert_layer_router_gb300 as m
@@ -190,8 +192,19 @@ class Layer:
         self.S = (tuple(wl.gen_shared(lc, w, dev) for w in ("gate", "up", "down"))
                   if lc.I_shared else None)
         self.cfg = m.config_from(lc)
-        self.weights = m.ExpertWeights(self.cfg, [w[0] for w in self.W], [w[1] for w in self.W],
-                                       [w[2] for w in self.W], shared=self.S)
+        if lc.wtype == "fp8_e4m3":
+            Q = [tuple(m.moe_quantize_weight_fp8(t) for t in w3) for w3 in self.W]
+            SQ = tuple(m.moe_quantize_weight_fp8(t) for t in self.S) if self.S else None
+            self.Q, self.SQ = Q, SQ
+            self.weights = m.ExpertWeights(
+                self.cfg, [q[0][0] for q in Q], [q[1][0] for q in Q], [q[2][0] for q in Q],
+                shared=tuple(t[0] for t in SQ) if SQ else None,
+                scales=([q[0][1] for q in Q], [q[1][1] for q in Q], [q[2][1] for q in Q]),
+                shared_scales=tuple(t[1] for t in SQ) if SQ else None)
+        else:
+            self.weights = m.ExpertWeights(self.cfg, [w[0] for w in self.W],
+                                           [w[1] for w in self.W], [w[2] for w in self.W],
+                                           shared=self.S)
 
 
 # ------------------------------------------------------------------ oracle baseline

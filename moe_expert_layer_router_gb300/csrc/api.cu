@@ -203,8 +203,10 @@ static size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
 struct Layout {
   size_t blk_counts = 0, blk_base = 0;        // permute
   size_t sched1 = 0, sched2 = 0, h = 0, hs = 0;  // grouped ffn
+  size_t h_sc = 0, hs_sc = 0;                 // fp8: scales of h and of the shared h
   size_t ids = 0, w = 0, counts = 0, offsets = 0, perm_token = 0, inv_row = 0, row_weight = 0,
          x_perm = 0, y_perm = 0, shared_out = 0;  // forward
+  size_t x_perm_sc = 0, xq = 0, xq_sc = 0;    // forward, fp8: x_perm scales, quantised x
   size_t total = 0;
 };
 
@@ -225,11 +227,17 @@ static Layout layout(const moe_config_t& c, int op) {
     L.blk_counts = take(size_t(nblk) * c.E * 4);
     L.blk_base = take(size_t(nblk) * c.E * 4);
   }
+  const bool fp8 = c.wtype == MOE_DTYPE_FP8_E4M3;
+  const size_t esz = fp8 ? 1 : 2;  // bytes per element of x_perm and h
   if (ffn) {
     L.sched1 = take(size_t(sched_ints(G)) * 4);
     L.sched2 = take(size_t(sched_ints(G)) * 4);
-    L.h = take(size_t(R) * c.I * 2);
-    L.hs = take(size_t(T) * c.I_shared * 2);
+    L.h = take(size_t(R) * c.I * esz);
+    L.hs = take(size_t(T) * c.I_shared * esz);
+    if (fp8) {
+      L.h_sc = take(size_t(R) * (c.I / 128) * 4);
+      L.hs_sc = take(size_t(T) * (c.I_shared / 128) * 4);
+    }
   }
   if (op == MOE_OP_FORWARD) {
     L.ids = take(size_t(R) * 4);
@@ -239,7 +247,12 @@ static Layout layout(const moe_config_t& c, int op) {
     L.perm_token = take(size_t(R) * 4);
     L.inv_row = take(size_t(R) * 4);
     L.row_weight = take(size_t(R) * 4);
-    L.x_perm = take(size_t(R) * c.H * 2);
+    L.x_perm = take(size_t(R) * c.H * esz);
+    if (fp8) {
+      L.x_perm_sc = take(size_t(R) * (c.H / 128) * 4);
+      L.xq = take(size_t(T) * c.H);
+      L.xq_sc = take(size_t(T) * (c.H / 128) * 4);
+    }
     L.y_perm = take(size_t(R) * c.H * 4);
     L.shared_out = take(size_t(T) * c.H * 4);
   }
@@ -270,9 +283,11 @@ static uint32_t* err_word(void* ws) { return static_cast<uint32_t*>(ws); }
 struct moe_weights {
   moe_config_t cfg;
   int device;
-  void* table;          // device: CUtensorMap maps1[2G], maps2[G]
+  void* table;          // device: CUtensorMap maps1[2G], maps2[G] (+ fp8: scale pointers)
   CUtensorMap* maps1;
   CUtensorMap* maps2;
+  const float** scales1;  // fp8: gate of group g at 2g, up at 2g+1
+  const float** scales2;  // fp8: down of group g at g
 };
 
 using namespace moe;
@@ -338,10 +353,15 @@ moe_status_t moe_weights_create(const moe_config_t* cfg, const moe_weight_list_t
   MOE_TRY(check_config(cfg));
   if (!wl || !out) return fail(MOE_ERR_INVALID_ARG, "weights or out is NULL");
   *out = nullptr;
-  if (cfg->wtype != MOE_DTYPE_BF16)
-    return fail(MOE_ERR_UNSUPPORTED, "fp8 expert weights are not supported by this build");
+  const bool fp8 = cfg->wtype == MOE_DTYPE_FP8_E4M3;
+  if (fp8 && (cfg->H / 128 > kFp8MaxKBlocks || cfg->I / 128 > kFp8MaxKBlocks ||
+              cfg->I_shared / 128 > kFp8MaxKBlocks))
+    return fail(MOE_ERR_UNSUPPORTED, "fp8 layers need H, I and I_shared <= %d",
+                128 * kFp8MaxKBlocks);
   if (!wl->gate || !wl->up || !wl->down)
     return fail(MOE_ERR_INVALID_ARG, "gate/up/down pointer arrays must not be NULL");
+  if (fp8 && (!wl->gate_scales || !wl->up_scales || !wl->down_scales))
+    return fail(MOE_ERR_INVALID_ARG, "fp8 weights need gate/up/down scale pointer arrays");
   const int E = cfg->E;
   for (int e = 0; e < E; ++e) {
     char nm[64];
@@ -351,32 +371,61 @@ moe_status_t moe_weights_create(const moe_config_t* cfg, const moe_weight_list_t
     MOE_TRY(check_ptr(wl->up[e], nm));
     snprintf(nm, sizeof nm, "down[%d]", e);
     MOE_TRY(check_ptr(wl->down[e], nm));
+    if (fp8) {
+      snprintf(nm, sizeof nm, "gate_scales[%d]", e);
+      MOE_TRY(check_ptr4(wl->gate_scales[e], nm));
+      snprintf(nm, sizeof nm, "up_scales[%d]", e);
+      MOE_TRY(check_ptr4(wl->up_scales[e], nm));
+      snprintf(nm, sizeof nm, "down_scales[%d]", e);
+      MOE_TRY(check_ptr4(wl->down_scales[e], nm));
+    }
   }
   const bool shared = cfg->I_shared > 0;
   if (shared) {
     MOE_TRY(check_ptr(wl->shared_gate, "shared_gate"));
     MOE_TRY(check_ptr(wl->shared_up, "shared_up"));
     MOE_TRY(check_ptr(wl->shared_down, "shared_down"));
+    if (fp8) {
+      MOE_TRY(check_ptr4(wl->shared_gate_scales, "shared_gate_scales"));
+      MOE_TRY(check_ptr4(wl->shared_up_scales, "shared_up_scales"));
+      MOE_TRY(check_ptr4(wl->shared_down_scales, "shared_down_scales"));
+    }
   }
   const int G = E + (shared ? 1 : 0);
   std::vector<CUtensorMap> maps(3 * G);
+  std::vector<const float*> scales(fp8 ? 3 * G : 0);
   CUtensorMap* m1 = maps.data();
   CUtensorMap* m2 = maps.data() + 2 * G;
   const uint64_t H = cfg->H, I = cfg->I, Is = cfg->I_shared;
   for (int g = 0; g < G; ++g) {
     const bool sh = g == E;
     const uint64_t inter = sh ? Is : I;
-    MOE_TRY(encode_2d(&m1[2 * g], true, sh ? wl->shared_gate : wl->gate[g], H, inter, kTileK,
-                      kGemmBRows / 2));
-    MOE_TRY(encode_2d(&m1[2 * g + 1], true, sh ? wl->shared_up : wl->up[g], H, inter, kTileK,
-                      kGemmBRows / 2));
-    MOE_TRY(encode_2d(&m2[g], true, sh ? wl->shared_down : wl->down[g], inter, H, kTileK,
-                      kGemmBRows));
+    const void* wg = sh ? wl->shared_gate : wl->gate[g];
+    const void* wu = sh ? wl->shared_up : wl->up[g];
+    const void* wd = sh ? wl->shared_down : wl->down[g];
+    if (!fp8) {
+      // bf16 pair tiles: each CTA loads 64 gate + 64 up rows, or 128 down rows
+      MOE_TRY(encode_2d(&m1[2 * g], true, wg, H, inter, kTileK, kGemmBRows / 2));
+      MOE_TRY(encode_2d(&m1[2 * g + 1], true, wu, H, inter, kTileK, kGemmBRows / 2));
+      MOE_TRY(encode_2d(&m2[g], true, wd, inter, H, kTileK, kGemmBRows));
+    } else {
+      // fp8: 128 weight rows x 128 K bytes per box
+      MOE_TRY(encode_2d(&m1[2 * g], false, wg, H, inter, 128, kFp8WRows));
+      MOE_TRY(encode_2d(&m1[2 * g + 1], false, wu, H, inter, 128, kFp8WRows));
+      MOE_TRY(encode_2d(&m2[g], false, wd, inter, H, 128, kFp8WRows));
+      scales[2 * g] = sh ? wl->shared_gate_scales : wl->gate_scales[g];
+      scales[2 * g + 1] = sh ? wl->shared_up_scales : wl->up_scales[g];
+      scales[2 * G + g] = sh ? wl->shared_down_scales : wl->down_scales[g];
+    }
   }
   void* table = nullptr;
-  const size_t bytes = maps.size() * sizeof(CUtensorMap);
-  MOE_CUDA(cudaMalloc(&table, bytes));
-  cudaError_t e = cudaMemcpy(table, maps.data(), bytes, cudaMemcpyHostToDevice);
+  const size_t map_bytes = maps.size() * sizeof(CUtensorMap);
+  const size_t sc_bytes = scales.size() * sizeof(const float*);
+  MOE_CUDA(cudaMalloc(&table, map_bytes + sc_bytes));
+  cudaError_t e = cudaMemcpy(table, maps.data(), map_bytes, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && sc_bytes)
+    e = cudaMemcpy(static_cast<uint8_t*>(table) + map_bytes, scales.data(), sc_bytes,
+                   cudaMemcpyHostToDevice);
   if (e != cudaSuccess) {
     cudaFree(table);
     return cuda_fail(e, "cudaMemcpy(weight table)");
@@ -387,6 +436,9 @@ moe_status_t moe_weights_create(const moe_config_t* cfg, const moe_weight_list_t
   w->table = table;
   w->maps1 = static_cast<CUtensorMap*>(table);
   w->maps2 = static_cast<CUtensorMap*>(table) + 2 * G;
+  const float** sp = reinterpret_cast<const float**>(static_cast<uint8_t*>(table) + map_bytes);
+  w->scales1 = fp8 ? sp : nullptr;
+  w->scales2 = fp8 ? sp + 2 * G : nullptr;
   *out = w;
   return MOE_OK;
 }
@@ -454,7 +506,8 @@ static moe_status_t run_ffn(const moe_config_t& c, const moe_weights* W, const L
   const int n1r = c.I / kGemm1TileN, n1s = c.I_shared / kGemm1TileN;
   const int n2 = (c.H + kGemm2TileN - 1) / kGemm2TileN;
   trace_mark(st, MOE_K_PLAN);
-  MOE_CUDA(launch_plan(offsets, c.E, shared ? 1 : 0, c.T, n1r, n1s, n2, n2, s1, s2, st));
+  MOE_CUDA(launch_plan(offsets, c.E, shared ? 1 : 0, c.T, n1r, n1s, n2, n2, s1, s2, kGemmTileRows,
+                       st));
 
   CUtensorMap a0, a1;
   MOE_TRY(encode_2d(&a0, true, x_perm, c.H, R, kTileK, kTileM));
@@ -495,6 +548,79 @@ static moe_status_t run_ffn(const moe_config_t& c, const moe_weights* W, const L
   g2.N_shared = c.H;
   trace_mark(st, MOE_K_GEMM2);
   MOE_CUDA(launch_grouped_gemm(false, b0, b1, g2, grid, st));
+  return MOE_OK;
+}
+
+// fp8: e4m3 rows (x_perm, x_shared) with 1x128 scales -> GEMM1 (e4m3 h + scales
+// in the workspace) -> GEMM2 (fp32 y_perm / shared_out).
+static moe_status_t run_ffn_fp8(const moe_config_t& c, const moe_weights* W, const Layout& L,
+                                void* ws, const void* x_perm, const float* x_perm_scales,
+                                const int32_t* offsets, const float* row_weight,
+                                const void* x_shared, const float* x_shared_scales, void* y_perm,
+                                void* shared_out, cudaStream_t st) {
+  uint32_t* err = err_word(ws);
+  const bool shared = c.I_shared > 0 && x_shared != nullptr;
+  const int64_t R = c.T * c.k;
+  int32_t* s1 = at<int32_t*>(ws, L.sched1);
+  int32_t* s2 = at<int32_t*>(ws, L.sched2);
+  uint8_t* h = at<uint8_t*>(ws, L.h);
+  uint8_t* hs = at<uint8_t*>(ws, L.hs);
+  float* h_sc = at<float*>(ws, L.h_sc);
+  float* hs_sc = at<float*>(ws, L.hs_sc);
+  const int n1r = c.I / kFp8WRows, n1s = c.I_shared / kFp8WRows, n2 = c.H / kFp8WRows;
+  trace_mark(st, MOE_K_PLAN);
+  MOE_CUDA(launch_plan(offsets, c.E, shared ? 1 : 0, c.T, n1r, n1s, n2, n2, s1, s2,
+                       kFp8TileTokens, st));
+  const int grid = sm_count();
+  // token rows: 32 rows x 128 bytes per box
+  CUtensorMap t0, t1;
+  MOE_TRY(encode_2d(&t0, false, x_perm, c.H, R, 128, 32));
+  if (shared) MOE_TRY(encode_2d(&t1, false, x_shared, c.H, c.T, 128, 32));
+  else t1 = t0;
+  Fp8GemmArgs g1{};
+  g1.w_maps = W->maps1;
+  g1.w_scales = W->scales1;
+  g1.offsets = offsets;
+  g1.sched = s1;
+  g1.tok_scales0 = x_perm_scales;
+  g1.tok_scales1 = shared ? x_shared_scales : x_perm_scales;
+  g1.out0 = h;
+  g1.out1 = hs;
+  g1.out_scales0 = h_sc;
+  g1.out_scales1 = hs_sc;
+  g1.row_weight = nullptr;
+  g1.err = err;
+  g1.E = c.E;
+  g1.has_shared = shared ? 1 : 0;
+  g1.T = static_cast<int32_t>(c.T);
+  g1.K_routed = c.H;
+  g1.K_shared = c.H;
+  g1.N_routed = c.I;
+  g1.N_shared = c.I_shared;
+  trace_mark(st, MOE_K_GEMM1);
+  MOE_CUDA(launch_grouped_gemm_fp8(true, t0, t1, g1, grid, st));
+
+  CUtensorMap u0, u1;
+  MOE_TRY(encode_2d(&u0, false, h, c.I, R, 128, 32));
+  if (shared) MOE_TRY(encode_2d(&u1, false, hs, c.I_shared, c.T, 128, 32));
+  else u1 = u0;
+  Fp8GemmArgs g2 = g1;
+  g2.w_maps = W->maps2;
+  g2.w_scales = W->scales2;
+  g2.sched = s2;
+  g2.tok_scales0 = h_sc;
+  g2.tok_scales1 = shared ? hs_sc : h_sc;
+  g2.out0 = y_perm;
+  g2.out1 = shared_out;
+  g2.out_scales0 = nullptr;
+  g2.out_scales1 = nullptr;
+  g2.row_weight = row_weight;
+  g2.K_routed = c.I;
+  g2.K_shared = c.I_shared;
+  g2.N_routed = c.H;
+  g2.N_shared = c.H;
+  trace_mark(st, MOE_K_GEMM2);
+  MOE_CUDA(launch_grouped_gemm_fp8(false, u0, u1, g2, grid, st));
   return MOE_OK;
 }
 
@@ -572,11 +698,12 @@ moe_status_t moe_grouped_ffn(const moe_config_t* cfg, moe_weights_t weights, con
   if (!weights) return fail(MOE_ERR_INVALID_ARG, "weights is NULL");
   if (!same_shape(weights->cfg, *cfg))
     return fail(MOE_ERR_INVALID_ARG, "weights were created for a different layer shape");
-  if (cfg->wtype != MOE_DTYPE_BF16)
-    return fail(MOE_ERR_UNSUPPORTED, "fp8 grouped FFN is not supported by this build");
-  (void)x_perm_scales;
-  (void)x_shared_scales;
+  const bool fp8 = cfg->wtype == MOE_DTYPE_FP8_E4M3;
   if (cfg->T == 0) return MOE_OK;
+  if (fp8) {
+    MOE_TRY(check_ptr4(x_perm_scales, "x_perm_scales"));
+    if (x_shared && cfg->I_shared > 0) MOE_TRY(check_ptr4(x_shared_scales, "x_shared_scales"));
+  }
   MOE_TRY(check_ptr(x_perm, "x_perm"));
   MOE_TRY(check_ptr4(expert_offsets, "expert_offsets"));
   MOE_TRY(check_ptr(y_perm, "y_perm"));
@@ -587,8 +714,12 @@ moe_status_t moe_grouped_ffn(const moe_config_t* cfg, moe_weights_t weights, con
   }
   Layout L = layout(*cfg, MOE_OP_GROUPED_FFN);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const moe_status_t s = run_ffn(*cfg, weights, L, ws, x_perm, expert_offsets, row_weight,
-                                 cfg->I_shared > 0 ? x_shared : nullptr, y_perm, shared_out, st);
+  const void* xs = cfg->I_shared > 0 ? x_shared : nullptr;
+  const moe_status_t s =
+      fp8 ? run_ffn_fp8(*cfg, weights, L, ws, x_perm, x_perm_scales, expert_offsets, row_weight,
+                        xs, x_shared_scales, y_perm, shared_out, st)
+          : run_ffn(*cfg, weights, L, ws, x_perm, expert_offsets, row_weight, xs, y_perm,
+                    shared_out, st);
   trace_mark(st, -1);
   return s;
 }
@@ -621,8 +752,7 @@ moe_status_t moe_forward(const moe_config_t* cfg, moe_weights_t weights, const v
   if (!weights) return fail(MOE_ERR_INVALID_ARG, "weights is NULL");
   if (!same_shape(weights->cfg, *cfg))
     return fail(MOE_ERR_INVALID_ARG, "weights were created for a different layer shape");
-  if (cfg->wtype != MOE_DTYPE_BF16)
-    return fail(MOE_ERR_UNSUPPORTED, "fp8 forward is not supported by this build");
+  const bool fp8 = cfg->wtype == MOE_DTYPE_FP8_E4M3;
   if (cfg->T == 0) return MOE_OK;
   MOE_TRY(check_ptr(x, "x"));
   MOE_TRY(check_ptr(w_router, "w_router"));
@@ -645,9 +775,22 @@ moe_status_t moe_forward(const moe_config_t* cfg, moe_weights_t weights, const v
   void* shared_out = cfg->I_shared > 0 ? at<void*>(ws, L.shared_out) : nullptr;
 
   MOE_TRY(run_route(*cfg, x, w_router, logit_bias, ids, w, nullptr, err, st));
+  float* x_perm_sc = fp8 ? at<float*>(ws, L.x_perm_sc) : nullptr;
   MOE_TRY(run_permute(*cfg, L, ws, ids, w, x, counts, offsets, perm_token, inv_row, row_weight,
-                      x_perm, nullptr, st));
-  MOE_TRY(run_ffn(*cfg, weights, L, ws, x_perm, offsets, row_weight, x, y_perm, shared_out, st));
+                      x_perm, x_perm_sc, st));
+  if (!fp8) {
+    MOE_TRY(run_ffn(*cfg, weights, L, ws, x_perm, offsets, row_weight, x, y_perm, shared_out, st));
+  } else {
+    // the shared expert reads every token: quantise x once more, unpermuted
+    uint8_t* xq = cfg->I_shared > 0 ? at<uint8_t*>(ws, L.xq) : nullptr;
+    float* xq_sc = cfg->I_shared > 0 ? at<float*>(ws, L.xq_sc) : nullptr;
+    if (xq) {
+      trace_mark(st, MOE_K_QUANT);
+      MOE_CUDA(launch_quant_act_fp8(x, cfg->T, cfg->H, xq, xq_sc, st));
+    }
+    MOE_TRY(run_ffn_fp8(*cfg, weights, L, ws, x_perm, x_perm_sc, offsets, row_weight, xq, xq_sc,
+                        y_perm, shared_out, st));
+  }
   trace_mark(st, MOE_K_COMBINE);
   MOE_CUDA(launch_combine(y_perm, inv_row, shared_out, out, cfg->T, cfg->k, cfg->H,
                           cfg->T * cfg->k, err, st));

@@ -28,6 +28,9 @@ constexpr int kMaxGroups = kMaxExperts + 1;  // routed experts + the shared expe
 constexpr int kPermTok = 64;       // tokens per histogram / scatter block
 constexpr int kGemmTileRows = 256; // rows of one grouped-GEMM work tile (a CTA pair)
 constexpr int kGemmBRows = 128;    // weight rows one CTA of the pair loads per stage (TMA box)
+constexpr int kFp8TileTokens = 64; // tokens per fp8 grouped-GEMM tile (the MMA's N side)
+constexpr int kFp8WRows = 128;     // weight rows per fp8 tile (the MMA's M side)
+constexpr int kFp8MaxKBlocks = 64; // fp8: at most 64 K blocks of 128 (H, I <= 8192)
 
 // Tile schedule of one grouped GEMM, in device memory (int32):
 //   [0]            number of tiles
@@ -48,6 +51,25 @@ struct GemmArgs {
   int32_t T;                   // rows of the shared group
   int32_t K_routed, K_shared;  // reduction sizes
   int32_t N_routed, N_shared;  // output columns
+};
+
+// fp8 grouped GEMM (weights on the MMA's M side, tokens on N).
+struct Fp8GemmArgs {
+  const CUtensorMap* w_maps;      // GEMM1: gate of group g at 2g, up at 2g+1; GEMM2: down at g
+  const float* const* w_scales;   // same indexing; each [rows/128, K/128] fp32
+  const int32_t* offsets;         // [E+1] routed row offsets
+  const int32_t* sched;           // tile schedule (64-token tiles)
+  const float* tok_scales0;       // routed token scales [T*k, K/128]
+  const float* tok_scales1;       // shared-expert token scales [T, K/128]
+  void* out0;                     // routed out: GEMM1 e4m3 h [T*k, I], GEMM2 fp32 y [T*k, H]
+  void* out1;                     // shared out: GEMM1 e4m3 h [T, I_s], GEMM2 fp32 [T, H]
+  float* out_scales0;             // GEMM1: h scales [T*k, I/128]
+  float* out_scales1;             // GEMM1: shared h scales [T, I_s/128]
+  const float* row_weight;        // GEMM2: per routed row scale, or null
+  uint32_t* err;
+  int32_t E, has_shared, T;
+  int32_t K_routed, K_shared;     // reduction sizes
+  int32_t N_routed, N_shared;     // output columns (GEMM1: I, I_s; GEMM2: H, H)
 };
 
 // --------------------------------------------------------------- launchers
@@ -74,7 +96,11 @@ int grouped_gemm_grid(int sm_count);
 
 cudaError_t launch_plan(const int32_t* offsets, int E, int has_shared, int64_t T, int n1_routed,
                         int n1_shared, int n2_routed, int n2_shared, int32_t* sched1,
-                        int32_t* sched2, cudaStream_t stream);
+                        int32_t* sched2, int tile_rows, cudaStream_t stream);
+
+cudaError_t launch_grouped_gemm_fp8(bool gate_up, const CUtensorMap& tok_map0,
+                                    const CUtensorMap& tok_map1, const Fp8GemmArgs& args, int grid,
+                                    cudaStream_t stream);
 
 cudaError_t launch_grouped_gemm(bool swiglu, const CUtensorMap& map_a0, const CUtensorMap& map_a1,
                                 const GemmArgs& args, int grid, cudaStream_t stream);

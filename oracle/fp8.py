@@ -146,3 +146,26 @@ def moe_layer_fp8(x, w_router, bias, experts, shared, k, score, renormalize=True
     return dict(logits=lg, ids=ids, weights=w, counts=counts, offsets=offsets,
                 perm_token=perm_token, inv_row=inv_row, x_codes=xq, x_scales=xs,
                 y_perm=y_perm, shared_out=s, out=out)
+
+
+def moe_tokens_fp8(x_rows, ids, w, experts, shared):
+    """Brute-force per-token evaluation of the fp8 layer (no permutation): each
+    token's bf16 row is quantised in 1x128 groups, run through its selected
+    experts (dequantised weights from ``experts(e)``, h quantised per row) and
+    the shared expert, and summed with its gate weights."""
+    x = np.asarray(moe._f64(x_rows), dtype=np.float32)
+    q, s = quantize_act_groups(x)
+    xd = dequant_act(q, s)
+    ids = np.asarray(ids)
+    w = moe._f64(w)
+    out = np.zeros(xd.shape, dtype=np.float64)
+    cache = {}
+    for t in range(xd.shape[0]):
+        for j in range(ids.shape[1]):
+            e = int(ids[t, j])
+            if e not in cache:
+                cache[e] = experts(e)
+            out[t] += w[t, j] * swiglu_ffn_fp8(xd[t:t + 1], *cache[e])[0]
+        if shared is not None:
+            out[t] += swiglu_ffn_fp8(xd[t:t + 1], *shared)[0]
+    return out

@@ -346,3 +346,14 @@ def test_fp8_layer_without_quantisation_equals_bf16_layer():
     c = fp8.moe_layer_fp8(x, wr, None, lambda e: W[e], sh, k, "sigmoid", True, 2.5)
     rel = np.abs(c["out"] - b["out"]).mean() / np.abs(b["out"]).mean()
     assert 1e-4 < rel < 0.1                                       # quantisation noise, bounded
+
+
+def test_fp8_bruteforce_equals_grouped_fp8_layer():
+    T, H, E, k, I = 11, 256, 4, 2, 128
+    x, wr, W, sh = _layer_inputs(T, H, E, k, I, 128)
+    Wd = [tuple(fp8.dequant_weight(*fp8.quantize_weight_blocks(m_.astype(np.float32))) for m_ in w3)
+          for w3 in W]
+    shd = tuple(fp8.dequant_weight(*fp8.quantize_weight_blocks(m_.astype(np.float32))) for m_ in sh)
+    r = fp8.moe_layer_fp8(x, wr, None, lambda e: Wd[e], shd, k, "sigmoid", True, 2.5)
+    bf = fp8.moe_tokens_fp8(x, r["ids"], r["weights"], lambda e: Wd[e], shd)
+    np.testing.assert_allclose(bf, r["out"], rtol=1e-12, atol=1e-12)
