@@ -113,7 +113,7 @@ class ClockSampler:
                 try:
                     ts = time.mktime(time.strptime(p[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
                     ts += float("0." + p[0].split(".")[1]) if "." in p[0] else 0.0
-                    rows.append((ts, float(p[2]), float(p[3]), p[6:10]))
+                    rows.append((ts, float(p[2]), float(p[3]), p[6:10], float(p[4])))
                 except Exception:
                     continue
         except Exception:
@@ -125,6 +125,7 @@ class ClockSampler:
         reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v == "Active"})
         return {"sm_mhz": statistics.median(r[1] for r in inside),
                 "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "power_w_median": statistics.median(r[4] for r in inside),
                 "samples": len(inside)}
 
 
@@ -207,7 +208,28 @@ class Layer:
                                            shared=self.S)
 
 
+def route_ids(layer, ws, dev):
+    """The routing decision of the layer's batch (one extra moe_route call, untimed)."""
+    import moe_expert_layer_router_gb300 as m
+    ids, _, _ = m.moe_route(layer.cfg, layer.x, layer.wr, layer.bias)
+    torch.cuda.synchronize(dev)
+    return ids
+
+
 # ------------------------------------------------------------------ oracle baseline
+_QCACHE = {}
+
+
+def _oracle_fp8_weights(key, t):
+    """The oracle's own 128x128 block quantisation of an fp32 weight matrix
+    (input preparation, outside any timing; cached: the fp8 weights are the
+    layer's inputs)."""
+    from oracle import fp8 as of8
+    if key not in _QCACHE:
+        _QCACHE[key] = of8.quantize_weight_blocks(t.cpu().numpy())
+    return _QCACHE[key]
+
+
 def oracle_sample(lc, layer, tokens):
     """Time the CPU oracle on `tokens` of the workload; returns (seconds, n)."""
     from oracle import moe as om
@@ -218,14 +240,30 @@ def oracle_sample(lc, layer, tokens):
     # the weights the sample needs, moved to host memory outside the timing
     lg = om.router_logits(x, wr, b)
     need = sorted(set(om.select_topk(lg, lc.k).reshape(-1).tolist()))
-    host = {e: tuple(t.cpu() for t in layer.W[e]) for e in need}
-    sh = tuple(t.cpu() for t in layer.S) if layer.S is not None else None
+    fp8 = lc.wtype == "fp8_e4m3"
+    if fp8:
+        host = {e: tuple(_oracle_fp8_weights((e, i), t) for i, t in enumerate(layer.W[e]))
+                for e in need}
+        sh = (tuple(_oracle_fp8_weights(("s", i), t) for i, t in enumerate(layer.S))
+              if layer.S is not None else None)
+    else:
+        host = {e: tuple(t.cpu() for t in layer.W[e]) for e in need}
+        sh = tuple(t.cpu() for t in layer.S) if layer.S is not None else None
     t0 = time.perf_counter()
-    om.moe_layer(x, wr, b, lambda e: host[e], sh, lc.k, lc.score, lc.renormalize, lc.route_scale)
+    if fp8:
+        from oracle import fp8 as of8
+        of8.moe_layer_fp8(x, wr, b, lambda e: tuple(of8.dequant_weight(*q) for q in host[e]),
+                          tuple(of8.dequant_weight(*q) for q in sh) if sh is not None else None,
+                          lc.k, lc.score, lc.renormalize, lc.route_scale)
+    else:
+        om.moe_layer(x, wr, b, lambda e: host[e], sh, lc.k, lc.score, lc.renormalize,
+                     lc.route_scale)
     return time.perf_counter() - t0, len(tokens)
 
 
-def cpu_baseline(lc, layer, n_tokens=8):
+def cpu_baseline(lc, layer, n_tokens=None):
+    if n_tokens is None:
+        n_tokens = 2 if lc.wtype == "fp8_e4m3" else 8
     g = np.random.default_rng(1)
     tokens = sorted(g.choice(lc.T, size=n_tokens, replace=False).tolist())
     secs, n = oracle_sample(lc, layer, tokens)
@@ -332,9 +370,32 @@ def run_ours(args, lc, rank, world, dev):
     flops = lc.flops()
     tflops = flops * world / (ms * 1e-3) / 1e12
     g1_ms = kernels_ms.get("gemm1_gate_up_swiglu")
-    g1_flops = 4.0 * lc.R * lc.H * lc.I + 4.0 * lc.T * lc.H * lc.I_shared
-    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    g1_tf = g1_flops / (g1_ms * 1e-3) / 1e12 if g1_ms else None
+    if lc.wtype == "fp8_e4m3":
+        # small-batch fp8: GEMM1 streams the gate/up weights of every expert that
+        # received a token (HBM-bound); algorithmic bytes per launch
+        counts = torch.bincount(route_ids(layer, ws, dev).reshape(-1).long(), minlength=lc.E)
+        active = int((counts > 0).sum().item())
+        g1_bytes = (2.0 * active * lc.I * lc.H * (1 + 4.0 / 128 / 128)
+                    + 2.0 * lc.I_shared * lc.H * (1 + 4.0 / 128 / 128)
+                    + (lc.R + lc.T) * lc.H * (1 + 4.0 / 128)
+                    + (lc.R * lc.I + lc.T * lc.I_shared) * (1 + 4.0 / 128))
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        g1_ach = g1_bytes / (g1_ms * 1e-3) / 1e9 if g1_ms else None
+        roof = {"kernel": "gemm1_gate_up_swiglu (fp8)", "bound": "hbm", "achieved": g1_ach,
+                "peak": peak, "unit": "GB/s", "frac": (g1_ach / peak) if g1_ach else None,
+                "peak_kind": f"HBM copy, of {peak_src}", "algorithmic_bytes_per_launch": g1_bytes,
+                "experts_with_tokens": active,
+                "traffic": recorded_traffic("gemm1_gate_up_swiglu", lc.name)}
+    else:
+        g1_flops = 4.0 * lc.R * lc.H * lc.I + 4.0 * lc.T * lc.H * lc.I_shared
+        peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        g1_tf = g1_flops / (g1_ms * 1e-3) / 1e12 if g1_ms else None
+        roof = {"kernel": "gemm1_gate_up_swiglu", "bound": "tensor",
+                "achieved": g1_tf, "peak": peak, "unit": "TFLOP/s",
+                "frac": (g1_tf / peak) if g1_tf else None,
+                "peak_kind": f"bf16 sustained, of {peak_src}",
+                "algorithmic_flop_per_launch": g1_flops,
+                "traffic": recorded_traffic("gemm1_gate_up_swiglu", lc.name)}
     res = {
         "metric": METRIC,
         "value": tokens / (ms * 1e-3),
@@ -346,7 +407,7 @@ def run_ours(args, lc, rank, world, dev):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "fp8_e4m3 (fp32 accumulate)" if lc.wtype == "fp8_e4m3" else "bf16",
         "data": "synthetic (seeded counter-based generator; x ~N(0,1), weights ~N(0,0.02))",
         "config": {"workload": describe(lc), "tokens_per_gpu": lc.T,
                    "parallelism": "replicas" if world > 1 else "single GPU",
@@ -356,12 +417,7 @@ def run_ours(args, lc, rank, world, dev):
                         "bf16_sustained": 100 * tflops / world / peak, "source": peak_src},
         "kernels_ms": {k: round(v, 4) for k, v in sorted(kernels_ms.items(),
                                                            key=lambda kv: -kv[1])},
-        "roofline": {"kernel": "gemm1_gate_up_swiglu", "bound": "tensor",
-                     "achieved": g1_tf, "peak": peak, "unit": "TFLOP/s",
-                     "frac": (g1_tf / peak) if g1_tf else None,
-                     "peak_kind": f"bf16 sustained, of {peak_src}",
-                     "algorithmic_flop_per_launch": g1_flops,
-                     "traffic": recorded_traffic("gemm1_gate_up_swiglu", lc.name)},
+        "roofline": roof,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": layer.x.numel() * 2, "d2h_bytes_per_step": out.numel() * 2},
@@ -393,9 +449,16 @@ def run_reference(args, lc, rank, world, dev):
            if lc.I_shared else None)
     g = np.random.default_rng(2)
     per = args.ref_tokens
+    # fp8: draw the per-step samples from a small fixed pool of tokens, so the
+    # (untimed, cached) oracle quantisation of their experts' weights is done once
+    pool = (sorted(g.choice(lc.T, size=4, replace=False).tolist())
+            if lc.wtype == "fp8_e4m3" else None)
     times, n_tok = [], 0
     for i in range(args.warmup + args.steps):
-        toks = sorted(g.choice(lc.T, size=per, replace=False).tolist())
+        if pool is not None:
+            toks = sorted(g.choice(pool, size=min(per, len(pool)), replace=False).tolist())
+        else:
+            toks = sorted(g.choice(lc.T, size=per, replace=False).tolist())
         s, n = oracle_sample(lc, L, toks)
         if i >= args.warmup:
             times.append(s)
@@ -421,7 +484,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="dsv3", choices=sorted(wl.CONFIGS))
-    ap.add_argument("--cpu-tokens", type=int, default=8)
+    ap.add_argument("--cpu-tokens", type=int, default=None)
     ap.add_argument("--ref-tokens", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

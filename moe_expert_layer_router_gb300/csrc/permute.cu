@@ -14,7 +14,9 @@
 //            orders every expert's rows by ascending token index.  The same
 //            block then reads each of its tokens' hidden state once and
 //            writes it to the token's k rows (16-byte vector accesses), so x
-//            crosses HBM once on the way in.
+//            crosses HBM once on the way in.  For small batches a second grid
+//            dimension splits the columns (in multiples of 128) over more
+//            blocks; each recomputes the ranks, the first writes the maps.
 #include <cuda_fp8.h>
 
 #include "moe_internal.h"
@@ -127,6 +129,7 @@ __global__ void __launch_bounds__(kScatterThreads)
   }
   __syncthreads();
   const int64_t R = T * k;
+  const bool write_maps = blockIdx.y == 0;
   for (int i = threadIdx.x; i < n; i += kScatterThreads) {
     const int tl = i / k;
     const int e = src[i];
@@ -137,15 +140,17 @@ __global__ void __launch_bounds__(kScatterThreads)
       for (int w = 0; w < wd; ++w) rank += __popc(mask[e][w]);
       const int64_t r = int64_t(offsets[e]) + blk_base[int64_t(e) * nblk + blockIdx.x] + rank;
       if (r >= 0 && r < R) row = static_cast<int32_t>(r);
-      else atomicOr(err, kErrBounds);
-    } else {
+      else if (write_maps) atomicOr(err, kErrBounds);
+    } else if (write_maps) {
       atomicOr(err, kErrBounds);
     }
     rows_s[i] = row;
-    inv_row[t0 * k + i] = row;
-    if (row >= 0) {
-      perm_token[row] = static_cast<int32_t>(t0 + tl);
-      if (row_weight) row_weight[row] = topk_w[t0 * k + i];
+    if (write_maps) {
+      inv_row[t0 * k + i] = row;
+      if (row >= 0) {
+        perm_token[row] = static_cast<int32_t>(t0 + tl);
+        if (row_weight) row_weight[row] = topk_w[t0 * k + i];
+      }
     }
   }
   __syncthreads();
@@ -153,18 +158,23 @@ __global__ void __launch_bounds__(kScatterThreads)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = kScatterThreads / 32;
-  const int nch = H / 8;  // 16-byte chunks of 8 bf16 per row
+  const int nch = H / 8;  // 8-element chunks per row (16 B of bf16 in, 16 or 8 B out)
+  // this block's column slice, in whole 128-column groups: chunks [c_lo, c_hi)
+  const int groups = H / 128;
+  const int g_lo = static_cast<int>(int64_t(groups) * blockIdx.y / gridDim.y);
+  const int g_hi = static_cast<int>(int64_t(groups) * (blockIdx.y + 1) / gridDim.y);
+  const int c_lo = g_lo * 16, c_hi = g_hi * 16;
   if (!fp8) {
     uint4* dst = static_cast<uint4*>(x_perm);
     for (int tl = warp; tl < nt; tl += nwarps) {
       const uint4* s4 = reinterpret_cast<const uint4*>(x + (t0 + tl) * int64_t(H));
       const int32_t* rr = rows_s + tl * k;
-      for (int c0 = 0; c0 < nch; c0 += 32 * 4) {
+      for (int c0 = c_lo; c0 < c_hi; c0 += 32 * 4) {
         uint4 v[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int cc = c0 + u * 32 + lane;
-          if (cc < nch) v[u] = __ldcs(s4 + cc);
+          if (cc < c_hi) v[u] = __ldcs(s4 + cc);
         }
         for (int j = 0; j < k; ++j) {
           const int32_t row = rr[j];
@@ -173,7 +183,7 @@ __global__ void __launch_bounds__(kScatterThreads)
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int cc = c0 + u * 32 + lane;
-            if (cc < nch) d4[cc] = v[u];
+            if (cc < c_hi) d4[cc] = v[u];
           }
         }
       }
@@ -185,9 +195,9 @@ __global__ void __launch_bounds__(kScatterThreads)
     for (int tl = warp; tl < nt; tl += nwarps) {
       const uint4* s4 = reinterpret_cast<const uint4*>(x + (t0 + tl) * int64_t(H));
       const int32_t* rr = rows_s + tl * k;
-      for (int c0 = 0; c0 < nch; c0 += 32) {
-        const int cc = c0 + lane;  // nch is a multiple of 16: half warps stay whole
-        const bool on = cc < nch;
+      for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+        const int cc = c0 + lane;  // slices are multiples of 16 chunks: half warps stay whole
+        const bool on = cc < c_hi;
         const uint4 v = on ? __ldcs(s4 + cc) : make_uint4(0, 0, 0, 0);
         float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
                       bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
@@ -283,7 +293,14 @@ cudaError_t launch_scatter(const int32_t* ids, const float* topk_w, const void* 
                            float* row_weight, void* x_perm, float* x_perm_scales, uint32_t* err,
                            cudaStream_t stream) {
   const int nblk = static_cast<int>((T + kPermTok - 1) / kPermTok);
-  scatter_kernel<<<nblk, kScatterThreads, 0, stream>>>(
+  // enough blocks to keep every SM streaming, in whole 128-column slices
+  int sm = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev);
+  int ysplit = (2 * sm + nblk - 1) / nblk;
+  if (ysplit > H / 128) ysplit = H / 128;
+  if (ysplit < 1 || !x_perm) ysplit = 1;
+  scatter_kernel<<<dim3(nblk, ysplit), kScatterThreads, 0, stream>>>(
       ids, topk_w, static_cast<const __nv_bfloat16*>(x), T, k, E, H, nblk, fp8, blk_base, offsets,
       perm_token, inv_row, row_weight, x_perm, x_perm_scales, err);
   return cudaGetLastError();

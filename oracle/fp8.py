@@ -44,7 +44,8 @@ def decode(codes) -> np.ndarray:
 
 def encode(v) -> np.ndarray:
     """float -> e4m3 code, round to nearest (ties to the even code), saturating
-    finite values beyond 448 to 448; NaN -> 0x7F."""
+    finite values beyond 448 to 448; NaN -> 0x7F.  Nearest entry of the table of
+    all 127 non-negative finite magnitudes."""
     v = np.asarray(v, dtype=np.float64)
     a = np.abs(v)
     # index of the largest magnitude <= a
@@ -54,6 +55,30 @@ def encode(v) -> np.ndarray:
     dhi = _MAG[hi] - a
     pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi != lo) & ((lo & 1) == 1))
     code = np.where(pick_hi, hi, lo)
+    code = np.where(a >= E4M3_MAX, 126, code)
+    code = code | np.where(np.signbit(v), 0x80, 0)
+    code = np.where(np.isnan(v), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def encode_bitfield(v) -> np.ndarray:
+    """Second, independent e4m3 encoder (used to pin `encode`), from the bit
+    fields: below 2^-6 the value is m * 2^-9 with m = rint(|v| * 2^9) (m = 8 is
+    the smallest normal, code 0x08); otherwise |v| = f * 2^e with f in [1, 2),
+    the 3-bit mantissa is rint((f - 1) * 8) (round half to even), a carry to 8
+    bumps the exponent, and the code is (e + 7) << 3 | mantissa."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    with np.errstate(invalid="ignore", over="ignore"):
+        fr, ex = np.frexp(a)                     # a = fr * 2^ex, fr in [0.5, 1)
+        e = ex - 1                               # a = (2 fr) * 2^e
+        mant = np.rint((2.0 * fr - 1.0) * 8.0)   # round half to even
+        carry = mant >= 8.0
+        e = np.where(carry, e + 1, e)
+        mant = np.where(carry, 0.0, mant)
+        normal = np.clip(((e + 7) << 3) + mant.astype(np.int64), 0, 126)
+        sub = np.rint(a * 512.0)                 # multiples of 2^-9 (8 -> 0x08)
+        code = np.where(a < 2.0 ** -6, sub, normal).astype(np.int64)
     code = np.where(a >= E4M3_MAX, 126, code)
     code = code | np.where(np.signbit(v), 0x80, 0)
     code = np.where(np.isnan(v), 0x7F, code)

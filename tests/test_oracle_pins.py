@@ -357,3 +357,13 @@ def test_fp8_bruteforce_equals_grouped_fp8_layer():
     r = fp8.moe_layer_fp8(x, wr, None, lambda e: Wd[e], shd, k, "sigmoid", True, 2.5)
     bf = fp8.moe_tokens_fp8(x, r["ids"], r["weights"], lambda e: Wd[e], shd)
     np.testing.assert_allclose(bf, r["out"], rtol=1e-12, atol=1e-12)
+
+
+def test_e4m3_table_encoder_equals_bitfield_encoder():
+    mags = fp8.decode(np.arange(127, dtype=np.uint8))
+    mids = (mags[1:] + mags[:-1]) / 2
+    v = np.concatenate([rng.normal(size=50000) * 30, rng.normal(size=20000) * 1e-2,
+                        rng.normal(size=5000) * 1e-3, mids, -mids, mags, -mags,
+                        np.nextafter(mids, 0), np.nextafter(mids, 1e9), [0.0, -0.0, 448.0, 449.0,
+                        1e9, -1e9, 2.0 ** -6, 2.0 ** -10, 2.0 ** -11]])
+    assert (fp8.encode(v) == fp8.encode_bitfield(v)).all()

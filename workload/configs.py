@@ -83,8 +83,10 @@ DSV3_FP8 = DSV3.with_(name="dsv3_fp8", T=512, wtype="fp8_e4m3")
 # Profiling slice: DeepSeek-V3 expert shapes and rows per expert (T*k/E = 512), a
 # quarter of the experts and tokens, so that one ncu capture holds a few GB.
 DSV3_SLICE = DSV3.with_(name="dsv3_slice", T=4096, E=64)
+# fp8 profiling slice: 16 tokens per expert as in the 512-token fp8 batch, 1/4 of the experts
+DSV3_FP8_SLICE = DSV3_FP8.with_(name="dsv3_fp8_slice", T=128, E=64)
 
-CONFIGS = {c.name: c for c in (TINY, QWEN3, DSV3, DSV3_SKEW, DSV3_FP8, DSV3_SLICE)}
+CONFIGS = {c.name: c for c in (TINY, QWEN3, DSV3, DSV3_SKEW, DSV3_FP8, DSV3_SLICE, DSV3_FP8_SLICE)}
 
 
 # ---------------------------------------------------------------- tensors
