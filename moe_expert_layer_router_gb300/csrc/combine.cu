@@ -25,7 +25,9 @@ __device__ __forceinline__ void add4(float (&acc)[8], int o, const float4& v) {
   acc[o + 3] += v.w;
 }
 
-__global__ void __launch_bounds__(kThreads)
+// 128 threads, up to 8 blocks (32 warps) per SM: enough loads in flight to
+// keep HBM busy without holding all k rows in registers at once.
+__global__ void __launch_bounds__(kThreads, 8)
     combine_kernel(const float4* __restrict__ y, const int32_t* __restrict__ inv_row,
                    const float4* __restrict__ sh, uint4* __restrict__ out, int k, int H, int64_t R,
                    uint32_t* err) {
@@ -44,20 +46,25 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   for (int c = threadIdx.x; c < nch; c += kThreads) {
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    float4 v[kMaxK][2];
+    // slots in order j = 0..k-1, four rows' loads in flight at a time
+    for (int j0 = 0; j0 < k; j0 += 4) {
+      float4 v[4][2];
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (j < k && rows[j] >= 0) {
-        const float4* src = y + rows[j] * (2 * nch) + 2 * c;
-        v[j][0] = __ldcs(src);
-        v[j][1] = __ldcs(src + 1);
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u;
+        if (j < k && rows[j] >= 0) {
+          const float4* src = y + rows[j] * (2 * nch) + 2 * c;
+          v[u][0] = __ldcs(src);
+          v[u][1] = __ldcs(src + 1);
+        }
       }
-    }
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (j < k && rows[j] >= 0) {
-        add4(acc, 0, v[j][0]);
-        add4(acc, 4, v[j][1]);
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u;
+        if (j < k && rows[j] >= 0) {
+          add4(acc, 0, v[u][0]);
+          add4(acc, 4, v[u][1]);
+        }
       }
     }
     if (sh) {

@@ -70,7 +70,11 @@ struct __align__(8) SmemCtl {
   int32_t offsets[kMaxExperts + 1];
 };
 
-constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + sizeof(SmemCtl);
+// Epilogue staging: each epilogue warp transposes its 32 rows x 32 columns
+// through shared memory so global stores cover whole lines of a few rows.
+constexpr int kStageOutBytes = 4096;  // per epilogue warp (32 rows x 128 B)
+constexpr size_t kSmemBytes =
+    1024 + size_t(kStages) * kStageBytes + 4 * kStageOutBytes + sizeof(SmemCtl);
 
 struct Tile {
   int g, m_blk, n_blk, rows, row0, K, N;
@@ -127,7 +131,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* a_tiles = smem;
   uint8_t* b_tiles = smem + kStages * kABytes;
-  SmemCtl& c = *reinterpret_cast<SmemCtl*>(smem + kStages * kStageBytes);
+  uint8_t* out_stage = smem + kStages * kStageBytes;
+  SmemCtl& c = *reinterpret_cast<SmemCtl*>(out_stage + 4 * kStageOutBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -263,74 +268,90 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ptx::mbar_wait(&c.tfull[acc], acc_ph, abort, args.err)) break;
       ptx::tc_fence_after();
       // Row of this thread and, for half tiles, which 128-column half of the
-      // pair's N it holds (warp-uniform: lane quarters 0-1 vs 2-3).
+      // pair's N it holds (warp-uniform: lane quarters 0-1 vs 2-3).  Rows of
+      // this warp are m_base + 0..31.
       const int hs = x.half ? (r >> 6) : 0;
-      const int m = x.m_blk * kPairRows +
-                    (x.half ? int(rank) * (kTileM / 2) + (r & 63) : int(rank) * kTileM + r);
+      const int m_base = x.m_blk * kPairRows +
+                         (x.half ? int(rank) * (kTileM / 2) + ((q * 32) & 63) : int(rank) * kTileM + q * 32);
+      const int m = m_base + lane;
       const bool valid = m < x.rows;
       const bool routed = x.g < args.E;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN;
       if (kSwiGLU) {
         // full tile: TMEM columns [g | u] of output columns 128 n + [0,64), then
         // [g | u] of 128 n + [64,128); half tile: one [g | u] block, the one of
-        // CTA-half hs.
-        __nv_bfloat16* dst = nullptr;
-        if (valid)
-          dst = (routed ? static_cast<__nv_bfloat16*>(args.out0) + int64_t(x.row0 + m) * x.N
-                        : static_cast<__nv_bfloat16*>(args.out1) + int64_t(m) * x.N) +
-                x.n_blk * kGemm1TileN;
+        // CTA-half hs.  Each 32-column chunk: 32 rows x 64 B staged, then written
+        // 8 rows x 64 B per store instruction.
+        uint4* st16 = reinterpret_cast<uint4*>(out_stage + (warp - 2) * kStageOutBytes);
+        __nv_bfloat16* base = routed ? static_cast<__nv_bfloat16*>(args.out0) +
+                                           int64_t(x.row0) * x.N
+                                     : static_cast<__nv_bfloat16*>(args.out1);
         const int nblocks = x.half ? 1 : 2;
 #pragma unroll 1
         for (int blk = 0; blk < nblocks; ++blk) {
-          const int out_col = (x.half ? hs : blk) * 64;
+          const int out_col = x.n_blk * kGemm1TileN + (x.half ? hs : blk) * 64;
 #pragma unroll 1
           for (int cb = 0; cb < 2; ++cb) {
             uint32_t gr[32], ur[32];
             ptx::tmem_ld32(taddr + blk * 128 + cb * 32, gr);
             ptx::tmem_ld32(taddr + blk * 128 + 64 + cb * 32, ur);
             ptx::tmem_ld_wait();
-            if (valid) {
-              uint4* d4 = reinterpret_cast<uint4*>(dst + out_col + cb * 32);
 #pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                uint32_t p[4];
+            for (int v = 0; v < 4; ++v) {
+              uint32_t p[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int i = v * 8 + e * 2;
-                  const float h0 = silu_f(__uint_as_float(gr[i])) * __uint_as_float(ur[i]);
-                  const float h1 = silu_f(__uint_as_float(gr[i + 1])) * __uint_as_float(ur[i + 1]);
-                  p[e] = pack_bf16(h0, h1);
-                }
-                d4[v] = make_uint4(p[0], p[1], p[2], p[3]);
+              for (int e = 0; e < 4; ++e) {
+                const int i = v * 8 + e * 2;
+                const float h0 = silu_f(__uint_as_float(gr[i])) * __uint_as_float(ur[i]);
+                const float h1 = silu_f(__uint_as_float(gr[i + 1])) * __uint_as_float(ur[i + 1]);
+                p[e] = pack_bf16(h0, h1);
               }
+              st16[lane * 4 + (v ^ ((lane >> 1) & 3))] = make_uint4(p[0], p[1], p[2], p[3]);
             }
+            __syncwarp();
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+              const int i = it * 8 + (lane >> 2), vv = lane & 3;
+              const uint4 val = st16[i * 4 + (vv ^ ((i >> 1) & 3))];
+              if (m_base + i < x.rows)
+                *reinterpret_cast<uint4*>(base + int64_t(m_base + i) * x.N + out_col + cb * 32 +
+                                          vv * 8) = val;
+            }
+            __syncwarp();
           }
         }
       } else {
         // full tile: 256 TMEM columns = output columns 256 n + [0,256);
-        // half tile: 128 TMEM columns = output columns 256 n + 128 hs + [0,128)
-        float w = 1.0f;
-        float* dst = nullptr;
-        if (valid) {
-          if (routed && args.row_weight) w = args.row_weight[x.row0 + m];
-          dst = (routed ? static_cast<float*>(args.out0) + int64_t(x.row0 + m) * x.N
-                        : static_cast<float*>(args.out1) + int64_t(m) * x.N) +
-                x.n_blk * kGemm2TileN + hs * 128;
-        }
+        // half tile: 128 TMEM columns = output columns 256 n + 128 hs + [0,128).
+        // Each 32-column chunk: 32 rows x 128 B staged, then written 4 rows x
+        // 128 B per store instruction.
+        float4* st4 = reinterpret_cast<float4*>(out_stage + (warp - 2) * kStageOutBytes);
+        float* base = routed ? static_cast<float*>(args.out0) + int64_t(x.row0) * x.N
+                             : static_cast<float*>(args.out1);
+        const float w = (valid && routed && args.row_weight) ? args.row_weight[x.row0 + m] : 1.0f;
+        const int col0 = x.n_blk * kGemm2TileN + hs * 128;
         const int ncb = (x.half ? 128 : kGemm2TileN) / 32;
 #pragma unroll 1
         for (int cb = 0; cb < ncb; ++cb) {
-          if (x.n_blk * kGemm2TileN + hs * 128 + cb * 32 >= x.N) break;  // warp-uniform
+          if (col0 + cb * 32 >= x.N) break;  // warp-uniform
           uint32_t yr[32];
           ptx::tmem_ld32(taddr + cb * 32, yr);
           ptx::tmem_ld_wait();
-          if (valid) {
-            float4* d4 = reinterpret_cast<float4*>(dst + cb * 32);
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              d4[v] = make_float4(w * __uint_as_float(yr[4 * v]), w * __uint_as_float(yr[4 * v + 1]),
-                                  w * __uint_as_float(yr[4 * v + 2]), w * __uint_as_float(yr[4 * v + 3]));
+          for (int v = 0; v < 8; ++v)
+            st4[lane * 8 + (v ^ (lane & 7))] =
+                make_float4(w * __uint_as_float(yr[4 * v]), w * __uint_as_float(yr[4 * v + 1]),
+                            w * __uint_as_float(yr[4 * v + 2]), w * __uint_as_float(yr[4 * v + 3]));
+          __syncwarp();
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int i = it * 4 + (lane >> 3), vv = lane & 7;
+            const float4 val = st4[i * 8 + (vv ^ (i & 7))];
+            if (m_base + i < x.rows)
+              *reinterpret_cast<float4*>(base + int64_t(m_base + i) * x.N + col0 + cb * 32 +
+                                         vv * 4) = val;
           }
+          __syncwarp();
         }
       }
       ptx::tc_fence_before();
