@@ -252,6 +252,22 @@ MOE_API moe_status_t moe_forward(const moe_config_t* cfg, moe_weights_t weights,
                          int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
                          moe_stream_t stream);
 
+/* moe_forward with options.  flags:
+ *   MOE_FORWARD_FUSED_DISPATCH  bf16 layers: the grouped gate/up GEMM reads each
+ *     expert's rows straight from x by token index (TMA row gathers, four rows
+ *     per copy) instead of from a permuted copy of x, so the permutation step
+ *     writes only its index maps -- the fused dispatch + expert GEMM of "Memory-
+ *     Compute Disaggregation for Large-Model Inference: AFD Architecture
+ *     Analysis and Performance Validation", section 5 (operator fusion).  Same
+ *     results; on GB300 the row gathers are slower than one permuted copy plus
+ *     tile loads, so it is off by default.  Ignored for fp8 layers.
+ * Unknown flag bits give MOE_ERR_INVALID_ARG. */
+#define MOE_FORWARD_FUSED_DISPATCH 0x1u
+MOE_API moe_status_t moe_forward_ex(const moe_config_t* cfg, moe_weights_t weights, const void* x,
+                                    const void* w_router, const float* logit_bias, void* out,
+                                    int32_t* topk_ids_out, float* topk_w_out, uint32_t flags,
+                                    void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* fp8 weight preparation: 128x128 block quantisation of an fp32 [N, K] matrix
  * (N, K multiples of 128): scales[N/128, K/128] = amax/448 (1 for an all-zero
  * block), q = e4m3 rn_satfinite(w/s), computed in fp32.  Asynchronous. */

@@ -21,7 +21,8 @@ from . import _native as N
 from ._native import MoeConfig, MoeError
 
 __all__ = ["MoeConfig", "MoeError", "make_config", "config_from", "Workspace", "ExpertWeights",
-           "moe_route", "moe_permute", "moe_permute_noalloc", "moe_grouped_ffn", "moe_combine", "moe_forward",
+           "moe_route", "moe_permute", "moe_permute_noalloc", "moe_grouped_ffn", "moe_combine",
+           "moe_forward",
            "moe_quantize_weight_fp8", "moe_quantize_act_fp8", "moe_get_device_error",
            "moe_workspace_size", "load"]
 
@@ -295,9 +296,10 @@ def moe_combine(cfg: MoeConfig, y_perm, inv_row, shared_out=None, *, ws=None, st
 
 
 def moe_forward(cfg: MoeConfig, weights: ExpertWeights, x, w_router, bias=None, *, out=None,
-                return_routing=False, ws=None, stream=None):
+                return_routing=False, fused_dispatch=False, ws=None, stream=None):
     """The whole layer.  Returns out bf16 [T,H] (and (topk_ids, topk_w) when
-    return_routing)."""
+    return_routing).  fused_dispatch: GEMM1 gathers its rows from x instead of
+    a permuted copy (moe_forward_ex with MOE_FORWARD_FUSED_DISPATCH)."""
     dev = x.device
     _need(x, "x", torch.bfloat16, (cfg.T, cfg.H), dev)
     _need(w_router, "w_router", torch.bfloat16, (cfg.E, cfg.H), dev)
@@ -312,9 +314,10 @@ def moe_forward(cfg: MoeConfig, weights: ExpertWeights, x, w_router, bias=None, 
         ids = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=dev)
         w = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=dev)
     ws = _ws(ws, cfg, "forward", dev)
-    N.check(N.lib().moe_forward(C.byref(cfg), weights.handle, _ptr(x), _ptr(w_router), _ptr(bias),
-                                _ptr(out), _ptr(ids), _ptr(w), ws.ptr, ws.nbytes,
-                                _stream(stream)), "moe_forward")
+    flags = N.MOE_FORWARD_FUSED_DISPATCH if fused_dispatch else 0
+    N.check(N.lib().moe_forward_ex(C.byref(cfg), weights.handle, _ptr(x), _ptr(w_router),
+                                   _ptr(bias), _ptr(out), _ptr(ids), _ptr(w), flags, ws.ptr,
+                                   ws.nbytes, _stream(stream)), "moe_forward_ex")
     return (out, ids, w) if return_routing else out
 
 

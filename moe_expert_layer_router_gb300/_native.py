@@ -18,6 +18,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUD
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 MOE_DTYPE_BF16, MOE_DTYPE_FP8_E4M3 = 0, 1
 MOE_OP_ROUTE, MOE_OP_PERMUTE, MOE_OP_GROUPED_FFN, MOE_OP_COMBINE, MOE_OP_FORWARD = range(5)
+MOE_FORWARD_FUSED_DISPATCH = 0x1
 
 
 class MoeConfig(C.Structure):
@@ -59,6 +60,7 @@ _SIG = {
     "moe_grouped_ffn": (C.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
     "moe_combine": (C.c_int, [_CFG, _P, _P, _P, _P, _P, C.c_size_t, _P]),
     "moe_forward": (C.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
+    "moe_forward_ex": (C.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, C.c_uint32, _P, C.c_size_t, _P]),
     "moe_quantize_weight_fp8": (C.c_int, [_P, C.c_int64, C.c_int64, _P, _P, _P]),
     "moe_quantize_act_fp8": (C.c_int, [_P, C.c_int64, C.c_int64, _P, _P, _P]),
     "moe_set_trace": (C.c_int, [C.POINTER(MoeTrace)]),

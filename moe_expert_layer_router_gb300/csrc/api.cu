@@ -492,10 +492,13 @@ static moe_status_t run_permute(const moe_config_t& c, const Layout& L, void* ws
   return MOE_OK;
 }
 
+// bf16 grouped FFN.  GEMM1's routed rows come from x_perm (tile loads) or,
+// when gather_rows (row -> token) is given, straight from the unpermuted
+// tokens x_perm = x by TMA row gathers (the permuted copy is never written).
 static moe_status_t run_ffn(const moe_config_t& c, const moe_weights* W, const Layout& L, void* ws,
                             const void* x_perm, const int32_t* offsets, const float* row_weight,
                             const void* x_shared, void* y_perm, void* shared_out,
-                            cudaStream_t st) {
+                            cudaStream_t st, const int32_t* gather_rows = nullptr) {
   uint32_t* err = err_word(ws);
   const bool shared = c.I_shared > 0 && x_shared != nullptr;
   const int64_t R = c.T * c.k;
@@ -510,7 +513,8 @@ static moe_status_t run_ffn(const moe_config_t& c, const moe_weights* W, const L
                        st));
 
   CUtensorMap a0, a1;
-  MOE_TRY(encode_2d(&a0, true, x_perm, c.H, R, kTileK, kTileM));
+  if (gather_rows) MOE_TRY(encode_2d(&a0, true, x_perm, c.H, c.T, kTileK, 1));
+  else MOE_TRY(encode_2d(&a0, true, x_perm, c.H, R, kTileK, kTileM));
   if (shared) MOE_TRY(encode_2d(&a1, true, x_shared, c.H, c.T, kTileK, kTileM));
   else a1 = a0;
   GemmArgs g1{};
@@ -520,7 +524,9 @@ static moe_status_t run_ffn(const moe_config_t& c, const moe_weights* W, const L
   g1.out0 = h;
   g1.out1 = hs;
   g1.row_weight = nullptr;
+  g1.gather_rows = gather_rows;
   g1.err = err;
+  g1.R = static_cast<int32_t>(R);
   g1.E = c.E;
   g1.has_shared = shared ? 1 : 0;
   g1.T = static_cast<int32_t>(c.T);
@@ -537,6 +543,7 @@ static moe_status_t run_ffn(const moe_config_t& c, const moe_weights* W, const L
   if (shared) MOE_TRY(encode_2d(&b1, true, hs, c.I_shared, c.T, kTileK, kTileM));
   else b1 = b0;
   GemmArgs g2 = g1;
+  g2.gather_rows = nullptr;
   g2.b_maps = W->maps2;
   g2.sched = s2;
   g2.out0 = y_perm;
@@ -747,6 +754,16 @@ moe_status_t moe_forward(const moe_config_t* cfg, moe_weights_t weights, const v
                          const void* w_router, const float* logit_bias, void* out,
                          int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
                          moe_stream_t stream) {
+  return moe_forward_ex(cfg, weights, x, w_router, logit_bias, out, topk_ids_out, topk_w_out, 0,
+                        ws, ws_bytes, stream);
+}
+
+moe_status_t moe_forward_ex(const moe_config_t* cfg, moe_weights_t weights, const void* x,
+                            const void* w_router, const float* logit_bias, void* out,
+                            int32_t* topk_ids_out, float* topk_w_out, uint32_t flags, void* ws,
+                            size_t ws_bytes, moe_stream_t stream) {
+  if (flags & ~uint32_t(MOE_FORWARD_FUSED_DISPATCH))
+    return fail(MOE_ERR_INVALID_ARG, "unknown forward flags 0x%x", flags);
   MOE_TRY(check_config(cfg));
   MOE_TRY(check_ws(*cfg, MOE_OP_FORWARD, ws, ws_bytes));
   if (!weights) return fail(MOE_ERR_INVALID_ARG, "weights is NULL");
@@ -770,6 +787,7 @@ moe_status_t moe_forward(const moe_config_t* cfg, moe_weights_t weights, const v
   int32_t* perm_token = at<int32_t*>(ws, L.perm_token);
   int32_t* inv_row = at<int32_t*>(ws, L.inv_row);
   float* row_weight = at<float*>(ws, L.row_weight);
+  const bool fused = (flags & MOE_FORWARD_FUSED_DISPATCH) && !fp8;
   void* x_perm = at<void*>(ws, L.x_perm);
   void* y_perm = at<void*>(ws, L.y_perm);
   void* shared_out = cfg->I_shared > 0 ? at<void*>(ws, L.shared_out) : nullptr;
@@ -777,8 +795,12 @@ moe_status_t moe_forward(const moe_config_t* cfg, moe_weights_t weights, const v
   MOE_TRY(run_route(*cfg, x, w_router, logit_bias, ids, w, nullptr, err, st));
   float* x_perm_sc = fp8 ? at<float*>(ws, L.x_perm_sc) : nullptr;
   MOE_TRY(run_permute(*cfg, L, ws, ids, w, x, counts, offsets, perm_token, inv_row, row_weight,
-                      x_perm, x_perm_sc, st));
-  if (!fp8) {
+                      fused ? nullptr : x_perm, x_perm_sc, st));
+  if (fused) {
+    // fused dispatch: GEMM1 gathers each expert's rows from x by token index
+    MOE_TRY(run_ffn(*cfg, weights, L, ws, x, offsets, row_weight, x, y_perm, shared_out, st,
+                    perm_token));
+  } else if (!fp8) {
     MOE_TRY(run_ffn(*cfg, weights, L, ws, x_perm, offsets, row_weight, x, y_perm, shared_out, st));
   } else {
     // the shared expert reads every token: quantise x once more, unpermuted

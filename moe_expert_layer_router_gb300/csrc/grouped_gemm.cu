@@ -122,6 +122,31 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint3
   }
 }
 
+// B operand of this CTA for a tile: GEMM1 -- gate and up rows [128 n + 64 r,
+// +64) (two boxes); GEMM2 -- W_down rows [256 n + 128 r, +128).
+template <bool kSwiGLU>
+__device__ __forceinline__ void b_operand(const Tile& x, uint32_t rank, const GemmArgs& args,
+                                          const CUtensorMap*& mb, int& b_row) {
+  if (kSwiGLU) {
+    mb = args.b_maps + 2 * x.g;
+    b_row = x.n_blk * kGemm1TileN + int(rank) * (kGemmBRows / 2);
+  } else {
+    mb = args.b_maps + x.g;
+    b_row = x.n_blk * kGemm2TileN + int(rank) * kGemmBRows;
+  }
+}
+
+template <bool kSwiGLU>
+__device__ __forceinline__ void load_b_impl(uint8_t* bs, const CUtensorMap* mb, uint32_t fb,
+                                            int kb, int b_row) {
+  if (kSwiGLU) {
+    ptx::tma_load_2d_pair(bs, mb, fb, kb * kTileK, b_row);
+    ptx::tma_load_2d_pair(bs + kBBytes / 2, mb + 1, fb, kb * kTileK, b_row);
+  } else {
+    ptx::tma_load_2d_pair(bs, mb, fb, kb * kTileK, b_row);
+  }
+}
+
 template <bool kSwiGLU>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a0,
@@ -174,52 +199,94 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   volatile int* abort = &c.abort;
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------ TMA producer (both CTAs)
-      const uint32_t full0 = ptx::mapa(ptx::smem_u32(&c.full[0]), 0);
-      uint32_t it = 0;
-      for (int t = pair; t < num_tiles && !*abort; t += num_pairs) {
+    // -------------------------------------------------- TMA producer (both CTAs)
+    const uint32_t full0 = ptx::mapa(ptx::smem_u32(&c.full[0]), 0);
+    uint32_t it = 0;
+    if (args.gather_rows == nullptr) {
+      // tile loads: one lane issues everything
+      if (lane == 0) {
+        for (int t = pair; t < num_tiles && !*abort; t += num_pairs) {
+          const Tile x = decode_tile(t, c, args, G);
+          const void* map_a = x.g < args.E ? static_cast<const void*>(&map_a0)
+                                           : static_cast<const void*>(&map_a1);
+          const CUtensorMap* mb;
+          int b_row;
+          b_operand<kSwiGLU>(x, rank, args, mb, b_row);
+          // A rows of this CTA: 128 (full tile) or 64 (half tile; the box still
+          // brings 128 rows, the MMA reads the first 64)
+          const int a_row = x.row0 + x.m_blk * kPairRows +
+                            int(rank) * (x.half ? kTileM / 2 : kTileM);
+          const int kb_n = x.K / kTileK;
+          bool ok = true;
+          for (int kb = 0; kb < kb_n; ++kb, ++it) {
+            const int s = it % kStages;
+            const uint32_t ph = (it / kStages) & 1;
+            if (!ptx::mbar_wait(&c.empty[s], ph ^ 1, abort, args.err)) { ok = false; break; }
+            if (leader) ptx::mbar_arrive_expect_tx(&c.full[s], 2 * kStageBytes);
+            const uint32_t fb = full0 + s * 8;
+            ptx::tma_load_2d_pair(a_tiles + s * kABytes, map_a, fb, kb * kTileK, a_row);
+            load_b_impl<kSwiGLU>(b_tiles + s * kBBytes, mb, fb, kb, b_row);
+          }
+          if (!ok) break;
+        }
+      }
+    } else {
+      // GEMM1 fed straight from the unpermuted tokens: each lane gathers 4 of
+      // this CTA's routed A rows per stage by token index.  Lane 0 takes every
+      // barrier decision and broadcasts it, so the warp never diverges.
+      bool stop = false;
+      for (int t = pair; t < num_tiles && !stop; t += num_pairs) {
         const Tile x = decode_tile(t, c, args, G);
-        const void* map_a = x.g < args.E ? static_cast<const void*>(&map_a0)
-                                         : static_cast<const void*>(&map_a1);
+        const bool routed = x.g < args.E;
+        const int cta_rows = x.half ? kTileM / 2 : kTileM;
+        const void* map_a = routed ? static_cast<const void*>(&map_a0)
+                                   : static_cast<const void*>(&map_a1);
         const CUtensorMap* mb;
         int b_row;
-        if (kSwiGLU) {  // CTA r: gate and up rows [128 n + 64 r, +64)
-          mb = args.b_maps + 2 * x.g;
-          b_row = x.n_blk * kGemm1TileN + int(rank) * (kGemmBRows / 2);
-        } else {        // CTA r: W_down rows [256 n + 128 r, +128)
-          mb = args.b_maps + x.g;
-          b_row = x.n_blk * kGemm2TileN + int(rank) * kGemmBRows;
+        b_operand<kSwiGLU>(x, rank, args, mb, b_row);
+        const int a_row = x.row0 + x.m_blk * kPairRows + int(rank) * cta_rows;
+        // gathers bring exactly the rows used; tile loads (shared expert) 128
+        const uint32_t a_bytes = routed ? uint32_t(cta_rows) * 128u : uint32_t(kABytes);
+        int tok[4] = {0, 0, 0, 0};
+        const bool g_lane = routed && lane < cta_rows / 4;
+        if (g_lane) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int pr = a_row + 4 * lane + j;  // permuted row; past the segment: any token
+            tok[j] = pr < args.R ? __ldg(args.gather_rows + pr) : 0;
+          }
         }
-        // A rows of this CTA: 128 (full tile) or 64 (half tile; the box still
-        // brings 128 rows, the MMA reads the first 64)
-        const int a_row = x.row0 + x.m_blk * kPairRows + int(rank) * (x.half ? kTileM / 2 : kTileM);
         const int kb_n = x.K / kTileK;
-        bool ok = true;
         for (int kb = 0; kb < kb_n; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
-          if (!ptx::mbar_wait(&c.empty[s], ph ^ 1, abort, args.err)) { ok = false; break; }
-          if (leader) ptx::mbar_arrive_expect_tx(&c.full[s], 2 * kStageBytes);
-          const uint32_t fb = full0 + s * 8;
-          ptx::tma_load_2d_pair(a_tiles + s * kABytes, map_a, fb, kb * kTileK, a_row);
-          uint8_t* bs = b_tiles + s * kBBytes;
-          if (kSwiGLU) {
-            ptx::tma_load_2d_pair(bs, mb, fb, kb * kTileK, b_row);
-            ptx::tma_load_2d_pair(bs + kBBytes / 2, mb + 1, fb, kb * kTileK, b_row);
-          } else {
-            ptx::tma_load_2d_pair(bs, mb, fb, kb * kTileK, b_row);
+          int ok = 1;
+          if (lane == 0) ok = ptx::mbar_wait(&c.empty[s], ph ^ 1, abort, args.err) ? 1 : 0;
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) {
+            stop = true;
+            break;
           }
+          const uint32_t fb = full0 + s * 8;
+          if (lane == 0 && leader) ptx::mbar_arrive_expect_tx(&c.full[s], 2 * (a_bytes + kBBytes));
+          if (routed) {
+            if (g_lane)
+              ptx::tma_gather4_pair(a_tiles + s * kABytes + lane * 512, map_a, fb, kb * kTileK,
+                                    tok[0], tok[1], tok[2], tok[3]);
+          } else if (lane == 0) {
+            ptx::tma_load_2d_pair(a_tiles + s * kABytes, map_a, fb, kb * kTileK, a_row);
+          }
+          if (lane == 0) load_b_impl<kSwiGLU>(b_tiles + s * kBBytes, mb, fb, kb, b_row);
         }
-        if (!ok) break;
+        if (__shfl_sync(0xffffffffu, *abort ? 1 : 0, 0)) stop = true;
       }
-      if (*abort && leader) {
-        // Both CTAs' loads of a stage complete on the even CTA's barrier: wait
-        // for the stages issued last so no copy is in flight at exit.
-        const uint32_t first = it > kStages ? it - kStages : 0;
-        for (uint32_t j = first; j < it; ++j)
-          drain_wait(&c.full[j % kStages], (j / kStages) & 1, args.err);
-      }
+    }
+    if (lane == 0 && *abort && leader) {
+      // Both CTAs' loads of a stage complete on the even CTA's barrier: wait
+      // for the stages issued last so no copy is in flight at exit.
+      const uint32_t first = it > kStages ? it - kStages : 0;
+      for (uint32_t j = first; j < it; ++j)
+        drain_wait(&c.full[j % kStages], (j / kStages) & 1, args.err);
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {

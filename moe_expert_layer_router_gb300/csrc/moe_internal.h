@@ -45,7 +45,10 @@ struct GemmArgs {
   void* out0;                  // routed output rows (GEMM1: bf16 h, GEMM2: fp32 y)
   void* out1;                  // shared-expert output rows (same types)
   const float* row_weight;     // GEMM2: per routed row scale, or null
+  const int32_t* gather_rows;  // GEMM1: row -> token map; routed A rows are gathered from the
+                               // unpermuted tokens (map_a0 has one-row boxes), or null
   uint32_t* err;               // sticky status word
+  int32_t R;                   // routed rows (T*k)
   int32_t E;
   int32_t has_shared;
   int32_t T;                   // rows of the shared group

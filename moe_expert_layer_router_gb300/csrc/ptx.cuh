@@ -245,6 +245,21 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const void* map, uin
       : "memory");
 }
 
+// Four rows (r0..r3, any order) x one box of columns starting at c0, gathered
+// into this CTA's shared memory (consecutive 128-byte rows; the tensor map's
+// box is one row high), completing on an mbarrier of either CTA of the pair.
+__device__ __forceinline__ void tma_gather4_pair(void* dst, const void* map, uint32_t bar,
+                                                 int32_t c0, int32_t r0, int32_t r1, int32_t r2,
+                                                 int32_t r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4"
+      ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(r0), "r"(r1), "r"(r2),
+      "r"(r3)
+      : "memory");
+}
+
 // Pair-collective tensor-memory management: one warp of EACH CTA of the pair
 // executes these together; the same columns are allocated in both CTAs.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {

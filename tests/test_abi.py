@@ -129,3 +129,12 @@ def test_quantize_validation(L):
     assert L.moe_quantize_weight_fp8(16, 100, 128, 16, 16, None) == N.MOE_ERR_INVALID_ARG
     assert L.moe_quantize_act_fp8(16, 4, 100, 16, 16, None) == N.MOE_ERR_INVALID_ARG
     assert L.moe_quantize_act_fp8(None, 0, 128, None, None, None) == N.MOE_OK
+
+
+def test_forward_ex_rejects_unknown_flags(L):
+    c = cfg()
+    ws = 0x10000
+    nb = C.c_size_t()
+    assert L.moe_workspace_size(C.byref(c), N.MOE_OP_FORWARD, C.byref(nb)) == 0
+    rc = L.moe_forward_ex(C.byref(c), None, 16, 16, None, 16, None, None, 0x8, ws, nb.value, None)
+    assert rc == N.MOE_ERR_INVALID_ARG and b"flags" in L.moe_last_error_message()

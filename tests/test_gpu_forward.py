@@ -14,12 +14,13 @@ from parity import Layer, assert_close_layer, f64, logit_tolerance, near_tie_tok
 pytestmark = pytest.mark.gpu
 
 
-def forward(L, lc):
+def forward(L, lc, fused=False):
     cfg = m.config_from(lc)
     W = m.ExpertWeights(cfg, [w[0] for w in L.W], [w[1] for w in L.W], [w[2] for w in L.W],
                         shared=L.S)
     ws = m.Workspace(cfg, "forward")
-    out, ids, w = m.moe_forward(cfg, W, L.x, L.wr, L.bias, return_routing=True, ws=ws)
+    out, ids, w = m.moe_forward(cfg, W, L.x, L.wr, L.bias, return_routing=True,
+                                fused_dispatch=fused, ws=ws)
     torch.cuda.synchronize()
     m.moe_get_device_error(ws)
     return out, ids.cpu().numpy(), w.cpu().numpy()
@@ -33,11 +34,12 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["x_perm", "fused_dispatch"])
 @pytest.mark.parametrize("lc", SMALL, ids=lambda c: c.name)
-def test_forward_small_matches_oracle(lc):
+def test_forward_small_matches_oracle(lc, fused):
     dev = torch.device("cuda")
     L = Layer(lc, dev)
-    out, ids, w = forward(L, lc)
+    out, ids, w = forward(L, lc, fused)
     ref = om.moe_layer(f64(L.x), f64(L.wr), None, L.experts_cpu, L.shared_cpu(), lc.k, lc.score,
                        lc.renormalize, lc.route_scale)
     tie = near_tie_tokens(ref["logits"], lc.k, logit_tolerance(L.x, L.wr))
@@ -46,14 +48,15 @@ def test_forward_small_matches_oracle(lc):
     assert_close_layer(out.float().cpu().numpy()[keep], ref["out"][keep], what=lc.name)
 
 
-FULL = [wl.QWEN3, wl.DSV3, wl.DSV3_SKEW]
+FULL = [(wl.QWEN3, False), (wl.DSV3, False), (wl.DSV3_SKEW, False), (wl.DSV3, True)]
 
 
-@pytest.mark.parametrize("lc", FULL, ids=lambda c: c.name)
-def test_forward_full_size_sampled(lc):
+@pytest.mark.parametrize("lc,fused", FULL,
+                         ids=lambda c: c.name if hasattr(c, "name") else ("fused" if c else ""))
+def test_forward_full_size_sampled(lc, fused):
     dev = torch.device("cuda")
     L = Layer(lc, dev)
-    out, ids, w = forward(L, lc)
+    out, ids, w = forward(L, lc, fused)
     b = None if L.bias is None else f64(L.bias)
     ref_lg = om.router_logits(f64(L.x), f64(L.wr), b)
     ref_ids = om.select_topk(ref_lg, lc.k)
