@@ -139,17 +139,25 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+# Source files that decide each profiled kernel's code: its own translation
+# unit plus the shared headers.
+KERNEL_SOURCES = {
+    "bf16": ("grouped_gemm.cu", "moe_internal.h", "ptx.cuh"),
+    "fp8": ("grouped_gemm_fp8.cu", "moe_internal.h", "ptx.cuh"),
+}
+
+
+def kernel_source_hash(kind: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_expert_layer_router_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES[kind]:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str):
+def recorded_traffic(kernel: str, workload: str, kind: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None when
-    the summary is missing or was taken on other kernel sources."""
+    the summary is missing or was taken on other sources of that kernel."""
     p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_ncu.md")
     if not os.path.exists(p):
         return None
@@ -158,7 +166,7 @@ def recorded_traffic(kernel: str, workload: str):
         if ln.startswith("- ") and ":" in ln:
             k, _, v = ln[2:].partition(":")
             vals[k.strip()] = v.strip().strip("`")
-    if vals.get("kernel_source_sha") != kernel_source_hash():
+    if vals.get("kernel_source_sha") != kernel_source_hash(kind):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
@@ -385,7 +393,7 @@ def run_ours(args, lc, rank, world, dev):
                 "peak": peak, "unit": "GB/s", "frac": (g1_ach / peak) if g1_ach else None,
                 "peak_kind": f"HBM copy, of {peak_src}", "algorithmic_bytes_per_launch": g1_bytes,
                 "experts_with_tokens": active,
-                "traffic": recorded_traffic("gemm1_gate_up_swiglu", lc.name)}
+                "traffic": recorded_traffic("gemm1_gate_up_swiglu", lc.name, "fp8")}
     else:
         g1_flops = 4.0 * lc.R * lc.H * lc.I + 4.0 * lc.T * lc.H * lc.I_shared
         peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
@@ -395,7 +403,7 @@ def run_ours(args, lc, rank, world, dev):
                 "frac": (g1_tf / peak) if g1_tf else None,
                 "peak_kind": f"bf16 sustained, of {peak_src}",
                 "algorithmic_flop_per_launch": g1_flops,
-                "traffic": recorded_traffic("gemm1_gate_up_swiglu", lc.name)}
+                "traffic": recorded_traffic("gemm1_gate_up_swiglu", lc.name, "bf16")}
     res = {
         "metric": METRIC,
         "value": tokens / (ms * 1e-3),
