@@ -31,6 +31,7 @@ SMALL = [
     wl.TINY.with_(name="tiny_sigmoid_shared", T=200, I_shared=256, score="sigmoid", route_scale=2.5),
     wl.DSV3.with_(name="dsv3_shape_T64", T=64, E=32, k=4, I=256, I_shared=256),
     wl.TINY.with_(name="skewish", T=700, E=16, k=3, H=384, I=128, zipf_bias=False),
+    wl.TINY.with_(name="one_token_k1", T=1, k=1),
 ]
 
 
@@ -46,6 +47,20 @@ def test_forward_small_matches_oracle(lc, fused):
     assert (ids[~tie] == ref["ids"][~tie]).all()
     keep = ~tie & (ids == ref["ids"]).all(axis=1)
     assert_close_layer(out.float().cpu().numpy()[keep], ref["out"][keep], what=lc.name)
+
+
+def test_forward_empty_batch_is_a_noop():
+    """T = 0: the call succeeds, launches nothing and leaves the status word clear."""
+    dev = torch.device("cuda")
+    L = Layer(wl.TINY, dev)
+    lc0 = wl.TINY.with_(name="empty", T=0)
+    cfg = m.config_from(lc0)
+    W = m.ExpertWeights(cfg, [w[0] for w in L.W], [w[1] for w in L.W], [w[2] for w in L.W])
+    ws = m.Workspace(cfg, "forward")
+    out = m.moe_forward(cfg, W, L.x[:0], L.wr, L.bias, ws=ws)
+    torch.cuda.synchronize()
+    assert tuple(out.shape) == (0, lc0.H)
+    assert m.moe_get_device_error(ws) == 0
 
 
 FULL = [(wl.QWEN3, False), (wl.DSV3, False), (wl.DSV3_SKEW, False), (wl.DSV3, True)]
