@@ -510,7 +510,7 @@ static moe_status_t run_ffn(const moe_config_t& c, const moe_weights* W, const L
   const int n2 = (c.H + kGemm2TileN - 1) / kGemm2TileN;
   trace_mark(st, MOE_K_PLAN);
   MOE_CUDA(launch_plan(offsets, c.E, shared ? 1 : 0, c.T, n1r, n1s, n2, n2, s1, s2, kGemmTileRows,
-                       st));
+                       kGemmTileRows, st));
 
   CUtensorMap a0, a1;
   if (gather_rows) MOE_TRY(encode_2d(&a0, true, x_perm, c.H, c.T, kTileK, 1));
@@ -577,7 +577,7 @@ static moe_status_t run_ffn_fp8(const moe_config_t& c, const moe_weights* W, con
   const int n1r = c.I / kFp8WRows, n1s = c.I_shared / kFp8WRows, n2 = c.H / kFp8WRows;
   trace_mark(st, MOE_K_PLAN);
   MOE_CUDA(launch_plan(offsets, c.E, shared ? 1 : 0, c.T, n1r, n1s, n2, n2, s1, s2,
-                       kFp8TileTokens, st));
+                       kFp8Tile1Tokens, kFp8Tile2Tokens, st));
   const int grid = sm_count();
   // token rows: 32 rows x 128 bytes per box
   CUtensorMap t0, t1;

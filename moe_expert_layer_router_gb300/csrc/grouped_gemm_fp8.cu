@@ -14,7 +14,11 @@
 // separate tcgen05 kind::f8f6f4 product (4 MMAs of K = 32) into its own TMEM
 // partial; the epilogue warps add it into fp32 registers scaled by
 //   s_w[row block, k block] * s_x[token, k block]
-// (the weight scale is one value per tile and K block).  Partials rotate
+// (the weight scale is one value per tile and K block).  A tile walks its K
+// blocks starting at block (tile index mod K blocks): at any moment the CTAs
+// then read different 128-byte columns of their weight slabs, which spreads
+// the weight stream over the HBM channels when the row pitch is a power of
+// two (W_down: 2 KB).  Partials rotate
 // through 4 (GEMM1) or 8 (GEMM2) TMEM buffers so the MMAs run ahead.
 //
 //   GEMM1 (kGateUp): 128 W_gate rows and the same 128 W_up rows of expert e;
@@ -38,17 +42,20 @@ constexpr int kKB = 128;                    // K elements (bytes) per block = on
 constexpr int kWRows = 128;                 // weight rows per tile (UMMA M)
 constexpr int kWBytes = kWRows * kKB;       // 16 KB per weight box
 constexpr int kTokBox = 32;                 // token rows per TMA box
-constexpr int kTokMax = kFp8TileTokens;     // 64 tokens per tile (two boxes)
-constexpr int kTokBytes = kTokMax * kKB;    // 8 KB token region per stage
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxKB = kFp8MaxKBlocks;      // K blocks per row (H or I up to 8192)
 
+// GEMM1: 64-token tiles (two boxes), 5 stages of 40 KB.  GEMM2: 32-token
+// tiles (one box), 10 stages of 20 KB, so 160 KB of weights are in flight per
+// SM against HBM latency.
 template <bool kGateUp>
 struct Cfg {
-  static constexpr int kStages = kGateUp ? 5 : 8;
+  static constexpr int kTok = kGateUp ? kFp8Tile1Tokens : kFp8Tile2Tokens;  // tokens per tile
+  static constexpr int kTokBytes = kTok * kKB;                               // token region per stage
+  static constexpr int kStages = kGateUp ? 5 : 10;
   static constexpr int kStageBytes = (kGateUp ? 2 : 1) * kWBytes + kTokBytes;
-  static constexpr int kBufCols = (kGateUp ? 2 : 1) * kTokMax;  // TMEM columns per partial
-  static constexpr int kBufs = kTmemCols / kBufCols;            // 4 or 8
+  static constexpr int kBufCols = (kGateUp ? 2 : 1) * 64;   // TMEM columns per partial
+  static constexpr int kBufs = kTmemCols / kBufCols;        // 4 or 8
 };
 
 template <bool kGateUp>
@@ -60,8 +67,8 @@ struct __align__(8) SmemCtl {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  float tok_scale[kTokMax * kMaxKB];  // s_x of the current tile's tokens, [token][k block]
-  float red[4][kTokMax];              // per-warp amax of h (GEMM1)
+  float tok_scale[Cfg<kGateUp>::kTok * kMaxKB];  // s_x of the tile's tokens, [token][k block]
+  float red[4][Cfg<kGateUp>::kTok];              // per-warp amax of h (GEMM1)
 };
 
 template <bool kGateUp>
@@ -74,7 +81,7 @@ struct Tile {
   int g, tok_blk, w_blk, rows, row0, K;
 };
 
-__device__ __forceinline__ Tile decode_tile(int t, const Fp8GemmArgs& a, int G) {
+__device__ __forceinline__ Tile decode_tile(int t, const Fp8GemmArgs& a, int G, int tok) {
   const int32_t* ts = a.sched + 1;
   int lo = 0, hi = G - 1;
   while (lo < hi) {
@@ -88,7 +95,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const Fp8GemmArgs& a, int G) 
   x.rows = routed ? __ldg(a.offsets + x.g + 1) - __ldg(a.offsets + x.g) : a.T;
   x.row0 = routed ? __ldg(a.offsets + x.g) : 0;
   x.K = routed ? a.K_routed : a.K_shared;
-  const int mt = (x.rows + kTokMax - 1) / kTokMax;
+  const int mt = (x.rows + tok - 1) / tok;
   x.w_blk = local / mt;
   x.tok_blk = local - x.w_blk * mt;
   return x;
@@ -169,28 +176,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------- TMA producer
       uint32_t it = 0;
       for (int t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
-        const Tile x = decode_tile(t, args, G);
+        const Tile x = decode_tile(t, args, G, C::kTok);
         const bool routed = x.g < args.E;
         const void* map_t = routed ? static_cast<const void*>(&map_b0)
                                    : static_cast<const void*>(&map_b1);
-        const int left = x.rows - x.tok_blk * kTokMax;
-        const int n_tok = left < kTokMax ? left : kTokMax;
+        const int left = x.rows - x.tok_blk * C::kTok;
+        const int n_tok = left < C::kTok ? left : C::kTok;
         const int n_box = (n_tok + kTokBox - 1) / kTokBox;
-        const int tok_row = x.row0 + x.tok_blk * kTokMax;
+        const int tok_row = x.row0 + x.tok_blk * C::kTok;
         const CUtensorMap* mw = kGateUp ? args.w_maps + 2 * x.g : args.w_maps + x.g;
         const int w_row = x.w_blk * kWRows;
         const uint32_t bytes = (kGateUp ? 2 : 1) * kWBytes + n_box * kTokBox * kKB;
         const int kb_n = x.K / kKB;
         bool ok = true;
+        const int rot = t % kb_n;
         for (int kb = 0; kb < kb_n; ++kb, ++it) {
           const int s = it % C::kStages;
           const uint32_t ph = (it / C::kStages) & 1;
+          const int kbe = kb + rot < kb_n ? kb + rot : kb + rot - kb_n;
           if (!ptx::mbar_wait(&c.empty[s], ph ^ 1, abort, args.err)) { ok = false; break; }
           ptx::mbar_arrive_expect_tx(&c.full[s], bytes);
-          ptx::tma_load_2d(stage_w(s, 0), mw, &c.full[s], kb * kKB, w_row);
-          if (kGateUp) ptx::tma_load_2d(stage_w(s, 1), mw + 1, &c.full[s], kb * kKB, w_row);
+          ptx::tma_load_2d(stage_w(s, 0), mw, &c.full[s], kbe * kKB, w_row);
+          if (kGateUp) ptx::tma_load_2d(stage_w(s, 1), mw + 1, &c.full[s], kbe * kKB, w_row);
           for (int bx = 0; bx < n_box; ++bx)
-            ptx::tma_load_2d(stage_t(s) + bx * kTokBox * kKB, map_t, &c.full[s], kb * kKB,
+            ptx::tma_load_2d(stage_t(s) + bx * kTokBox * kKB, map_t, &c.full[s], kbe * kKB,
                              tok_row + bx * kTokBox);
         }
         if (!ok) break;
@@ -206,9 +215,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------- MMA issuer
       uint32_t it = 0, pb = 0;
       for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-        const Tile x = decode_tile(t, args, G);
-        const int left = x.rows - x.tok_blk * kTokMax;
-        const int n_tok = left < kTokMax ? left : kTokMax;
+        const Tile x = decode_tile(t, args, G, C::kTok);
+        const int left = x.rows - x.tok_blk * C::kTok;
+        const int n_tok = left < C::kTok ? left : C::kTok;
         const int n_mma = ((n_tok + kTokBox - 1) / kTokBox) * kTokBox;  // 32 or 64
         const uint32_t idesc = ptx::idesc_e4m3(kWRows, n_mma);
         const int kb_n = x.K / kKB;
@@ -228,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dw = ptx::sw128_desc(ptx::smem_u32(stage_w(s, w)));
 #pragma unroll
             for (int k = 0; k < kKB / 32; ++k)
-              ptx::mma_f8(d0 + w * kTokMax, dw + 2 * k, dt + 2 * k, idesc, k != 0);
+              ptx::mma_f8(d0 + w * 64, dw + 2 * k, dt + 2 * k, idesc, k != 0);  // up partial at +64
           }
           ptx::mma_commit(&c.empty[s]);
           ptx::mma_commit(&c.pfull[b]);
@@ -245,12 +254,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int et = threadIdx.x - 64;             // 0..127 among the epilogue threads
     uint32_t pb = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-      const Tile x = decode_tile(t, args, G);
+      const Tile x = decode_tile(t, args, G, C::kTok);
       const bool routed = x.g < args.E;
-      const int left = x.rows - x.tok_blk * kTokMax;
-      const int n_tok = left < kTokMax ? left : kTokMax;
+      const int left = x.rows - x.tok_blk * C::kTok;
+      const int n_tok = left < C::kTok ? left : C::kTok;
       const int kb_n = x.K / kKB;
-      const int tok_row = x.row0 + x.tok_blk * kTokMax;
+      const int tok_row = x.row0 + x.tok_blk * C::kTok;
       // stage the tile's token scales [token][k block] in shared memory
       const float* ts = routed ? args.tok_scales0 : args.tok_scales1;
       epi_sync();
@@ -261,32 +270,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       epi_sync();
       const float* ws0 = args.w_scales[kGateUp ? 2 * x.g : x.g] + int64_t(x.w_blk) * kb_n;
       const float* ws1 = kGateUp ? args.w_scales[2 * x.g + 1] + int64_t(x.w_blk) * kb_n : ws0;
-      float acc0[kTokMax], acc1[kGateUp ? kTokMax : 1];
+      float acc0[C::kTok], acc1[kGateUp ? C::kTok : 1];
 #pragma unroll
-      for (int j = 0; j < kTokMax; ++j) acc0[j] = 0.0f;
+      for (int j = 0; j < C::kTok; ++j) acc0[j] = 0.0f;
 #pragma unroll
-      for (int j = 0; j < (kGateUp ? kTokMax : 1); ++j) acc1[j] = 0.0f;
+      for (int j = 0; j < (kGateUp ? C::kTok : 1); ++j) acc1[j] = 0.0f;
       bool ok = true;
+      const int rot = t % kb_n;
       for (int kb = 0; kb < kb_n; ++kb, ++pb) {
+        const int kbe = kb + rot < kb_n ? kb + rot : kb + rot - kb_n;
         const int b = pb % C::kBufs;
         const uint32_t bph = (pb / C::kBufs) & 1;
         if (!ptx::mbar_wait(&c.pfull[b], bph, abort, args.err)) { ok = false; break; }
         ptx::tc_fence_after();
-        const float sw0 = __ldg(ws0 + kb);
-        const float sw1 = kGateUp ? __ldg(ws1 + kb) : 0.0f;
+        const float sw0 = __ldg(ws0 + kbe);
+        const float sw1 = kGateUp ? __ldg(ws1 + kbe) : 0.0f;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * C::kBufCols;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int half = 0; half < C::kTok / 32; ++half) {
           if (half * 32 < n_tok) {  // warp-uniform
             uint32_t p0[32];
             ptx::tmem_ld32(taddr + half * 32, p0);
             if constexpr (kGateUp) {
               uint32_t p1[32];
-              ptx::tmem_ld32(taddr + kTokMax + half * 32, p1);
+              ptx::tmem_ld32(taddr + 64 + half * 32, p1);
               ptx::tmem_ld_wait();
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
-                const float sx = c.tok_scale[(half * 32 + j) * kMaxKB + kb];
+                const float sx = c.tok_scale[(half * 32 + j) * kMaxKB + kbe];
                 acc0[half * 32 + j] += __uint_as_float(p0[j]) * (sw0 * sx);
                 acc1[half * 32 + j] += __uint_as_float(p1[j]) * (sw1 * sx);
               }
@@ -294,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::tmem_ld_wait();
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
-                const float sx = c.tok_scale[(half * 32 + j) * kMaxKB + kb];
+                const float sx = c.tok_scale[(half * 32 + j) * kMaxKB + kbe];
                 acc0[half * 32 + j] += __uint_as_float(p0[j]) * (sw0 * sx);
               }
             }
@@ -313,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n_i = routed ? args.N_routed : args.N_shared;  // I or I_shared
         const int col = x.w_blk * kWRows + r;
 #pragma unroll
-        for (int j = 0; j < kTokMax; ++j) {
+        for (int j = 0; j < C::kTok; ++j) {
           acc0[j] = silu_f(acc0[j]) * acc1[j];
           float a = fabsf(acc0[j]);
 #pragma unroll
@@ -322,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         epi_sync();
 #pragma unroll
-        for (int j = 0; j < kTokMax; ++j) {
+        for (int j = 0; j < C::kTok; ++j) {
           if (j < n_tok) {
             const float amax = fmaxf(fmaxf(c.red[0][j], c.red[1][j]), fmaxf(c.red[2][j], c.red[3][j]));
             const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
@@ -337,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n_o = args.N_routed;  // H for both groups
         const int col = x.w_blk * kWRows + r;
 #pragma unroll
-        for (int j = 0; j < kTokMax; ++j) {
+        for (int j = 0; j < C::kTok; ++j) {
           if (j < n_tok) {
             const int64_t row = tok_row + j;
             const float w = (routed && args.row_weight) ? __ldg(args.row_weight + row) : 1.0f;

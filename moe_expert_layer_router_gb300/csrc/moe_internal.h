@@ -28,7 +28,8 @@ constexpr int kMaxGroups = kMaxExperts + 1;  // routed experts + the shared expe
 constexpr int kPermTok = 64;       // tokens per histogram / scatter block
 constexpr int kGemmTileRows = 256; // rows of one grouped-GEMM work tile (a CTA pair)
 constexpr int kGemmBRows = 128;    // weight rows one CTA of the pair loads per stage (TMA box)
-constexpr int kFp8TileTokens = 64; // tokens per fp8 grouped-GEMM tile (the MMA's N side)
+constexpr int kFp8Tile1Tokens = 64; // tokens per fp8 GEMM1 tile (the MMA's N side)
+constexpr int kFp8Tile2Tokens = 32; // tokens per fp8 GEMM2 tile
 constexpr int kFp8WRows = 128;     // weight rows per fp8 tile (the MMA's M side)
 constexpr int kFp8MaxKBlocks = 64; // fp8: at most 64 K blocks of 128 (H, I <= 8192)
 
@@ -99,7 +100,7 @@ int grouped_gemm_grid(int sm_count);
 
 cudaError_t launch_plan(const int32_t* offsets, int E, int has_shared, int64_t T, int n1_routed,
                         int n1_shared, int n2_routed, int n2_shared, int32_t* sched1,
-                        int32_t* sched2, int tile_rows, cudaStream_t stream);
+                        int32_t* sched2, int tile_rows1, int tile_rows2, cudaStream_t stream);
 
 cudaError_t launch_grouped_gemm_fp8(bool gate_up, const CUtensorMap& tok_map0,
                                     const CUtensorMap& tok_map1, const Fp8GemmArgs& args, int grid,

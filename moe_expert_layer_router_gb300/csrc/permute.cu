@@ -228,15 +228,16 @@ __global__ void __launch_bounds__(kScatterThreads)
 __global__ void __launch_bounds__(256)
     plan_kernel(const int32_t* __restrict__ offsets, int E, int has_shared, int64_t T,
                 int n1r, int n1s, int n2r, int n2s, int32_t* __restrict__ sched1,
-                int32_t* __restrict__ sched2, int tile_rows) {
+                int32_t* __restrict__ sched2, int tile_rows1, int tile_rows2) {
   __shared__ int tiles[2][kMaxGroups];
   __shared__ int order[2][kMaxGroups];
   const int G = E + has_shared;
   for (int g = threadIdx.x; g < G; g += blockDim.x) {
     const int64_t rows = g < E ? int64_t(offsets[g + 1]) - offsets[g] : T;
-    const int mt = static_cast<int>((rows + tile_rows - 1) / tile_rows);
-    tiles[0][g] = mt * (g < E ? n1r : n1s);
-    tiles[1][g] = mt * (g < E ? n2r : n2s);
+    const int mt1 = static_cast<int>((rows + tile_rows1 - 1) / tile_rows1);
+    const int mt2 = static_cast<int>((rows + tile_rows2 - 1) / tile_rows2);
+    tiles[0][g] = mt1 * (g < E ? n1r : n1s);
+    tiles[1][g] = mt2 * (g < E ? n2r : n2s);
   }
   __syncthreads();
   for (int g = threadIdx.x; g < G; g += blockDim.x) {
@@ -308,9 +309,9 @@ cudaError_t launch_scatter(const int32_t* ids, const float* topk_w, const void* 
 
 cudaError_t launch_plan(const int32_t* offsets, int E, int has_shared, int64_t T, int n1_routed,
                         int n1_shared, int n2_routed, int n2_shared, int32_t* sched1,
-                        int32_t* sched2, int tile_rows, cudaStream_t stream) {
+                        int32_t* sched2, int tile_rows1, int tile_rows2, cudaStream_t stream) {
   plan_kernel<<<1, 256, 0, stream>>>(offsets, E, has_shared, T, n1_routed, n1_shared, n2_routed,
-                                     n2_shared, sched1, sched2, tile_rows);
+                                     n2_shared, sched1, sched2, tile_rows1, tile_rows2);
   return cudaGetLastError();
 }
 
