@@ -468,7 +468,7 @@ static moe_status_t run_route(const moe_config_t& c, const void* x, const void* 
   MOE_TRY(encode_2d(&mw, true, w_router, c.H, c.E, kTileK, E_pad));
   trace_mark(st, MOE_K_ROUTER);
   MOE_CUDA(launch_router(mx, mw, c.T, c.H, c.E, E_pad, c.k, c.score, c.renormalize, c.route_scale,
-                         bias, ids, w, logits, err, st));
+                         bias, ids, w, logits, err, sm_count(), st));
   return MOE_OK;
 }
 

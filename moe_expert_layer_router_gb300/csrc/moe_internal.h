@@ -80,7 +80,7 @@ struct Fp8GemmArgs {
 cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_w, int64_t T, int H,
                           int E, int E_pad, int k, int score, int renormalize, float route_scale,
                           const float* bias, int32_t* topk_ids, float* topk_w, float* logits_out,
-                          uint32_t* err, cudaStream_t stream);
+                          uint32_t* err, int sm_count, cudaStream_t stream);
 
 cudaError_t launch_hist(const int32_t* ids, int64_t T, int k, int E, int32_t* blk_counts,
                         uint32_t* err, cudaStream_t stream);
