@@ -498,7 +498,8 @@ static moe_status_t run_permute(const moe_config_t& c, const Layout& L, void* ws
 static moe_status_t run_ffn(const moe_config_t& c, const moe_weights* W, const Layout& L, void* ws,
                             const void* x_perm, const int32_t* offsets, const float* row_weight,
                             const void* x_shared, void* y_perm, void* shared_out,
-                            cudaStream_t st, const int32_t* gather_rows = nullptr) {
+                            cudaStream_t st, const int32_t* gather_rows = nullptr,
+                            float* y_scales = nullptr, float* shared_scales = nullptr) {
   uint32_t* err = err_word(ws);
   const bool shared = c.I_shared > 0 && x_shared != nullptr;
   const int64_t R = c.T * c.k;
@@ -548,6 +549,8 @@ static moe_status_t run_ffn(const moe_config_t& c, const moe_weights* W, const L
   g2.sched = s2;
   g2.out0 = y_perm;
   g2.out1 = shared_out;
+  g2.out_scales0 = y_scales;  // non-null: fp16 y with power-of-two scales
+  g2.out_scales1 = shared_scales;
   g2.row_weight = row_weight;
   g2.K_routed = c.I;
   g2.K_shared = c.I_shared;
@@ -796,12 +799,22 @@ moe_status_t moe_forward_ex(const moe_config_t* cfg, moe_weights_t weights, cons
   float* x_perm_sc = fp8 ? at<float*>(ws, L.x_perm_sc) : nullptr;
   MOE_TRY(run_permute(*cfg, L, ws, ids, w, x, counts, offsets, perm_token, inv_row, row_weight,
                       fused ? nullptr : x_perm, x_perm_sc, st));
+  // bf16 layers keep y and the shared output as fp16 with a power-of-two
+  // scale per 32 columns, inside the fp32-sized workspace regions: the
+  // scales follow the fp16 rows
+  const int64_t R = cfg->T * cfg->k;
+  float* y_sc = fp8 ? nullptr : reinterpret_cast<float*>(static_cast<uint8_t*>(y_perm) +
+                                                         size_t(R) * cfg->H * 2);
+  float* sh_sc = (fp8 || !shared_out) ? nullptr
+                                      : reinterpret_cast<float*>(static_cast<uint8_t*>(shared_out) +
+                                                                 size_t(cfg->T) * cfg->H * 2);
   if (fused) {
     // fused dispatch: GEMM1 gathers each expert's rows from x by token index
     MOE_TRY(run_ffn(*cfg, weights, L, ws, x, offsets, row_weight, x, y_perm, shared_out, st,
-                    perm_token));
+                    perm_token, y_sc, sh_sc));
   } else if (!fp8) {
-    MOE_TRY(run_ffn(*cfg, weights, L, ws, x_perm, offsets, row_weight, x, y_perm, shared_out, st));
+    MOE_TRY(run_ffn(*cfg, weights, L, ws, x_perm, offsets, row_weight, x, y_perm, shared_out, st,
+                    nullptr, y_sc, sh_sc));
   } else {
     // the shared expert reads every token: quantise x once more, unpermuted
     uint8_t* xq = cfg->I_shared > 0 ? at<uint8_t*>(ws, L.xq) : nullptr;
@@ -814,8 +827,11 @@ moe_status_t moe_forward_ex(const moe_config_t* cfg, moe_weights_t weights, cons
                         y_perm, shared_out, st));
   }
   trace_mark(st, MOE_K_COMBINE);
-  MOE_CUDA(launch_combine(y_perm, inv_row, shared_out, out, cfg->T, cfg->k, cfg->H,
-                          cfg->T * cfg->k, err, st));
+  if (fp8)
+    MOE_CUDA(launch_combine(y_perm, inv_row, shared_out, out, cfg->T, cfg->k, cfg->H, R, err, st));
+  else
+    MOE_CUDA(launch_combine_half(y_perm, y_sc, inv_row, shared_out, sh_sc, out, cfg->T, cfg->k,
+                                 cfg->H, R, err, st));
   trace_mark(st, -1);
   return MOE_OK;
 }

@@ -2,8 +2,11 @@
 // expert results of each token gathered back to token order and summed in
 // fp32, slot order j = 0..k-1 then the shared expert, rounded once to bf16.
 // y_perm and shared_out are fp32 rows (the grouped down projection writes
-// them unrounded).  One block per token; each thread owns 8-column chunks and
+// them unrounded), or, in the layer forward, fp16 rows with a power-of-two
+// scale per 32 columns.  One block per token; each thread owns 8-column chunks and
 // issues the k row loads of a chunk back to back so they are in flight together.
+#include <cuda_fp16.h>
+
 #include "moe_internal.h"
 #include "ptx.cuh"
 
@@ -77,7 +80,76 @@ __global__ void __launch_bounds__(kThreads, 8)
   }
 }
 
+// acc[0..7] += 8 fp16 values (one uint4) times their power-of-two scale s.
+__device__ __forceinline__ void add8h(float (&acc)[8], const uint4& v, float s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    acc[2 * i] += f.x * s;
+    acc[2 * i + 1] += f.y * s;
+  }
+}
+
+// The same combine over fp16 rows with one power-of-two scale per 32 columns
+// ([rows][H/32]): each value is widened exactly, y = h * s, then summed in
+// fp32 in slot order, the shared row last.  One uint4 (8 columns) of every
+// row per chunk.
+__global__ void __launch_bounds__(kThreads, 8)
+    combine_half_kernel(const uint4* __restrict__ y, const float* __restrict__ ysc,
+                        const int32_t* __restrict__ inv_row, const uint4* __restrict__ sh,
+                        const float* __restrict__ shsc, uint4* __restrict__ out, int k, int H,
+                        int64_t R, uint32_t* err) {
+  __shared__ int64_t rows[kMaxK];
+  const int64_t t = blockIdx.x;
+  const int nch = H / 8;
+  const int nsc = H / 32;
+  if (threadIdx.x < k) {
+    const int32_t r = inv_row[t * k + threadIdx.x];
+    int64_t rr = r;
+    if (r < 0 || r >= R) {
+      atomicOr(err, kErrBounds);
+      rr = -1;
+    }
+    rows[threadIdx.x] = rr;
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < nch; c += kThreads) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int j0 = 0; j0 < k; j0 += 4) {
+      uint4 v[4];
+      float sc[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u;
+        if (j < k && rows[j] >= 0) {
+          v[u] = __ldcs(y + rows[j] * nch + c);
+          sc[u] = __ldg(ysc + rows[j] * nsc + (c >> 2));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u;
+        if (j < k && rows[j] >= 0) add8h(acc, v[u], sc[u]);
+      }
+    }
+    if (sh) add8h(acc, __ldcs(sh + t * nch + c), __ldg(shsc + t * nsc + (c >> 2)));
+    out[t * nch + c] = make_uint4(pack2(acc[0], acc[1]), pack2(acc[2], acc[3]),
+                                  pack2(acc[4], acc[5]), pack2(acc[6], acc[7]));
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_combine_half(const void* y, const float* y_scales, const int32_t* inv_row,
+                                const void* shared, const float* shared_scales, void* out,
+                                int64_t T, int k, int H, int64_t R, uint32_t* err,
+                                cudaStream_t stream) {
+  combine_half_kernel<<<static_cast<unsigned>(T), kThreads, 0, stream>>>(
+      static_cast<const uint4*>(y), y_scales, inv_row, static_cast<const uint4*>(shared),
+      shared_scales, static_cast<uint4*>(out), k, H, R, err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const void* y_perm, const int32_t* inv_row, const void* shared_out,
                            void* out, int64_t T, int k, int H, int64_t R, uint32_t* err,

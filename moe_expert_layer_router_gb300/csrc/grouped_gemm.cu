@@ -11,9 +11,11 @@
 // is one more group whose rows are the unpermuted tokens.
 //
 //   GEMM1 (kSwiGLU):  h = silu(A W_gate^T) * (A W_up^T)   bf16 out
-//   GEMM2:            y = row_weight * (A W_down^T)       fp32 out
-// (y stays fp32 so that the k expert rows of a token are rounded to bf16 only
-// once, after the combine has summed them.)
+//   GEMM2:            y = row_weight * (A W_down^T)       fp32 out, or fp16 with
+//                     a power-of-two scale per 32 columns (the layer forward)
+// (y is never rounded to bf16: the k expert rows of a token are rounded to bf16
+// only once, after the combine has summed them.  Scaled fp16 keeps 11
+// significant bits of every value at half the bytes of fp32.)
 //
 // Work unit: a 256-row x 256-column pair tile computed by the two CTAs of a
 // cluster with one 256x256x16 MMA per 16-wide K step.  Each CTA loads its own
@@ -37,6 +39,8 @@
 // TMEM holds two 256-column fp32 accumulators, so the epilogue of tile i
 // overlaps the MMAs of tile i+1.  Tiles come from a device-built schedule
 // (heaviest group first) and are dealt to the persistent pairs round robin.
+#include <cuda_fp16.h>
+
 #include "moe_internal.h"
 #include "ptx.cuh"
 
@@ -386,6 +390,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
           }
+        }
+      } else if (args.out_scales0 != nullptr) {
+        // fp16 y: each 32-column chunk of a row is scaled by a power of two
+        // s = 2^(floor(log2 amax) - 14), so that |y| / s < 2^15 fits fp16 with
+        // its full 11-bit precision; s goes to out_scales[row][column / 32].
+        // Staged and stored like h: 8 rows x 64 B per store instruction.
+        uint4* st16 = reinterpret_cast<uint4*>(out_stage + (warp - 2) * kStageOutBytes);
+        __half* base = routed ? static_cast<__half*>(args.out0) + int64_t(x.row0) * x.N
+                              : static_cast<__half*>(args.out1);
+        const int nsc = x.N / 32;
+        float* sbase = routed ? args.out_scales0 + int64_t(x.row0) * nsc : args.out_scales1;
+        const float w = (valid && routed && args.row_weight) ? args.row_weight[x.row0 + m] : 1.0f;
+        const int col0 = x.n_blk * kGemm2TileN + hs * 128;
+        const int ncb = (x.half ? 128 : kGemm2TileN) / 32;
+#pragma unroll 1
+        for (int cb = 0; cb < ncb; ++cb) {
+          if (col0 + cb * 32 >= x.N) break;  // warp-uniform
+          uint32_t yr[32];
+          ptx::tmem_ld32(taddr + cb * 32, yr);
+          ptx::tmem_ld_wait();
+          float amax = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(w * __uint_as_float(yr[j])));
+          // biased exponent of the scale, kept a normal float (amax = 0 gives the
+          // smallest normal; every value is then 0)
+          int sb = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 14;
+          sb = sb < 1 ? 1 : sb;
+          const float scale = __uint_as_float(static_cast<uint32_t>(sb) << 23);
+          const float inv = __uint_as_float(static_cast<uint32_t>(254 - sb) << 23);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t p[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i = v * 8 + e * 2;
+              const __half2 hh = __floats2half2_rn(w * __uint_as_float(yr[i]) * inv,
+                                                   w * __uint_as_float(yr[i + 1]) * inv);
+              p[e] = *reinterpret_cast<const uint32_t*>(&hh);
+            }
+            st16[lane * 4 + (v ^ ((lane >> 1) & 3))] = make_uint4(p[0], p[1], p[2], p[3]);
+          }
+          if (valid) sbase[int64_t(m) * nsc + (col0 >> 5) + cb] = scale;
+          __syncwarp();
+#pragma unroll
+          for (int it = 0; it < 4; ++it) {
+            const int i = it * 8 + (lane >> 2), vv = lane & 3;
+            const uint4 val = st16[i * 4 + (vv ^ ((i >> 1) & 3))];
+            if (m_base + i < x.rows)
+              *reinterpret_cast<uint4*>(base + int64_t(m_base + i) * x.N + col0 + cb * 32 +
+                                        vv * 8) = val;
+          }
+          __syncwarp();
         }
       } else {
         // full tile: 256 TMEM columns = output columns 256 n + [0,256);

@@ -43,8 +43,10 @@ struct GemmArgs {
   const CUtensorMap* b_maps;   // GEMM1: gate of group g at 2g, up at 2g+1; GEMM2: down at g
   const int32_t* offsets;      // [E+1] routed row offsets
   const int32_t* sched;        // tile schedule (see above)
-  void* out0;                  // routed output rows (GEMM1: bf16 h, GEMM2: fp32 y)
+  void* out0;                  // routed output rows (GEMM1: bf16 h, GEMM2: fp32 y or fp16 y)
   void* out1;                  // shared-expert output rows (same types)
+  float* out_scales0;          // GEMM2: null for fp32 y; else y is fp16 and these are its
+  float* out_scales1;          //   power-of-two scales, [rows][N/32] (routed / shared)
   const float* row_weight;     // GEMM2: per routed row scale, or null
   const int32_t* gather_rows;  // GEMM1: row -> token map; routed A rows are gathered from the
                                // unpermuted tokens (map_a0 has one-row boxes), or null
@@ -112,6 +114,13 @@ cudaError_t launch_grouped_gemm(bool swiglu, const CUtensorMap& map_a0, const CU
 cudaError_t launch_combine(const void* y_perm, const int32_t* inv_row, const void* shared_out,
                            void* out, int64_t T, int k, int H, int64_t R, uint32_t* err,
                            cudaStream_t stream);
+
+// Combine of fp16 expert rows with one power-of-two scale per 32 columns
+// ([rows][H/32] fp32), as written by the grouped GEMM2 with out_scales set.
+cudaError_t launch_combine_half(const void* y, const float* y_scales, const int32_t* inv_row,
+                                const void* shared, const float* shared_scales, void* out,
+                                int64_t T, int k, int H, int64_t R, uint32_t* err,
+                                cudaStream_t stream);
 
 cudaError_t launch_quant_weight_fp8(const float* w, int64_t N, int64_t K, uint8_t* q,
                                     float* scales, cudaStream_t stream);

@@ -91,3 +91,33 @@ def test_forward_full_size_sampled(lc, fused):
     assert torch.isfinite(out.float()).all()
     print(f"{lc.name}: T={lc.T} near-tie tokens {int(tie.sum())}, max/mean rows "
           f"{counts.max() / counts.mean():.2f}")
+
+
+@pytest.mark.parametrize("lc", SMALL[:3], ids=lambda c: c.name)
+def test_forward_matches_the_four_calls(lc):
+    """moe_forward keeps the expert outputs as fp16 with a power-of-two scale per
+    32 columns; the four public calls keep them fp32.  On the same routing the two
+    outputs differ by that rounding alone.  Each fp16 value is within 2^-12 of its
+    fp32 value (relative), so the two fp32 sums differ by at most 2^-12 of the
+    summed magnitudes; the two bf16 roundings of the sums then differ by at most
+    one bf16 ulp (<= 2^-7 of the output) more.  The test allows 2^-11."""
+    dev = torch.device("cuda")
+    L = Layer(lc, dev)
+    cfg = m.config_from(lc)
+    W = m.ExpertWeights(cfg, [w[0] for w in L.W], [w[1] for w in L.W], [w[2] for w in L.W],
+                        shared=L.S)
+    out, ids, w = m.moe_forward(cfg, W, L.x, L.wr, L.bias, return_routing=True)
+    ids2, w2, _ = m.moe_route(cfg, L.x, L.wr, L.bias)
+    assert torch.equal(ids, ids2) and torch.equal(w, w2)
+    p = m.moe_permute(cfg, ids2, w2, L.x)
+    y, s = m.moe_grouped_ffn(cfg, W, p["x_perm"], p["expert_offsets"], p["row_weight"],
+                             x_shared=L.x if L.S is not None else None)
+    out4 = m.moe_combine(cfg, y, p["inv_row"], s)
+    torch.cuda.synchronize()
+    a, b = out.float(), out4.float()
+    # magnitude of everything summed into each output element
+    mag = y.abs()[p["inv_row"].long()].sum(dim=1)
+    if s is not None:
+        mag = mag + s.abs()
+    bound = 2.0 ** -7 * b.abs() + 2.0 ** -11 * mag + 1e-30
+    assert ((a - b).abs() <= bound).all(), float(((a - b).abs() / bound).max())
