@@ -64,16 +64,39 @@ __global__ void __launch_bounds__(kScanThreads)
   __shared__ int tot[kMaxExperts];
   __shared__ int wsum[32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = warp; e < E; e += kScanThreads / 32) {
+  // Each warp scans its experts' columns in batches of 256 blocks: the batch's
+  // 8 loads per lane are issued together, and the next expert's first batch is
+  // loaded while the current one is scanned, so the warp waits on one memory
+  // latency per batch instead of one per 32 blocks.
+  constexpr int kB = 8;  // 32-block chunks per batch
+  auto load = [&](int e, int b0, int (&v)[kB]) {
     const int32_t* src = blk_counts + int64_t(e) * nblk;
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const int b = b0 + j * 32 + lane;
+      v[j] = b < nblk ? src[b] : 0;
+    }
+  };
+  int nxt[kB];
+  if (warp < E) load(warp, 0, nxt);
+  for (int e = warp; e < E; e += kScanThreads / 32) {
     int32_t* dst = blk_base + int64_t(e) * nblk;
     int carry = 0;
-    for (int b0 = 0; b0 < nblk; b0 += 32) {
-      const int b = b0 + lane;
-      const int v = b < nblk ? src[b] : 0;
-      const int inc = warp_incl_scan(v, lane);
-      if (b < nblk) dst[b] = carry + inc - v;
-      carry += __shfl_sync(0xffffffffu, inc, 31);
+    for (int b0 = 0; b0 < nblk; b0 += 32 * kB) {
+      int v[kB];
+#pragma unroll
+      for (int j = 0; j < kB; ++j) v[j] = nxt[j];
+      // prefetch: this expert's next batch, else the next expert's first
+      if (b0 + 32 * kB < nblk) load(e, b0 + 32 * kB, nxt);
+      else if (e + kScanThreads / 32 < E) load(e + kScanThreads / 32, 0, nxt);
+#pragma unroll
+      for (int j = 0; j < kB; ++j) {
+        if (b0 + j * 32 >= nblk) break;  // warp-uniform: chunks past the last block
+        const int b = b0 + j * 32 + lane;
+        const int inc = warp_incl_scan(v[j], lane);
+        if (b < nblk) dst[b] = carry + inc - v[j];
+        carry += __shfl_sync(0xffffffffu, inc, 31);
+      }
     }
     if (lane == 0) tot[e] = carry;
   }
