@@ -189,7 +189,7 @@ class Layer:
     fp8 layers: the fp32 weights are block-quantised by the library once, before
     any timing (W holds the fp32 originals, which the oracle baseline uses)."""
 
-    def __init__(self, lc, dev):
+    def __init__(self, lc, dev, keep_fp32=True):
         import moe_expert_layer_router_gb300 as m
         self.lc = lc
         self.x = wl.gen_x(lc, dev)
@@ -210,6 +210,9 @@ class Layer:
                 shared=tuple(t[0] for t in SQ) if SQ else None,
                 scales=([q[0][1] for q in Q], [q[1][1] for q in Q], [q[2][1] for q in Q]),
                 shared_scales=tuple(t[1] for t in SQ) if SQ else None)
+            if not keep_fp32:  # only the quantised weights are needed
+                self.W = self.S = None
+                torch.cuda.empty_cache()
         else:
             self.weights = m.ExpertWeights(self.cfg, [w[0] for w in self.W],
                                            [w[1] for w in self.W], [w[2] for w in self.W],
@@ -474,9 +477,64 @@ def run_ours(args, lc, rank, world, dev):
         "gpu_launches": launches,
         "clocks": clocks.summary(w0, w1) if clocks else None,
     }
+    if args.stack:
+        res["stack"] = stack_dispatch(args, lc, layer, dev)
     if world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(lc, layer, args.cpu_tokens)
     return res
+
+
+def stack_dispatch(args, lc, layer, dev):
+    """Layer-stack dispatch: L layers of the workload (seeds 0..L-1; layer 0 is the
+    benchmarked one) run in turn on the same input, (a) one moe_forward call per
+    layer, (b) one CUDA graph recorded once that, per layer, writes the layer index
+    on the device and runs moe_forward_stack.  The kernels are the same; (b) takes
+    the host out of the loop between layers."""
+    import moe_expert_layer_router_gb300 as m
+    L = args.stack
+    layers = [layer] + [Layer(lc.with_(seed=s), dev, keep_fp32=False) for s in range(1, L)]
+    cfg, x = layer.cfg, layer.x
+    stream = torch.cuda.current_stream(dev)
+    ws = m.Workspace(cfg, "forward", dev)
+    out = torch.empty(lc.T, lc.H, dtype=torch.bfloat16, device=dev)
+    biases = [Ly.bias for Ly in layers]
+    stack = m.LayerStack(cfg, [Ly.weights for Ly in layers], [Ly.wr for Ly in layers],
+                         biases if any(b is not None for b in biases) else None)
+    index = torch.arange(L, dtype=torch.int32, device=dev)
+    lid = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def direct():
+        for Ly in layers:
+            m.moe_forward(cfg, Ly.weights, x, Ly.wr, Ly.bias, out=out, ws=ws, stream=stream)
+
+    m.moe_forward_stack(cfg, stack, lid, x, out=out, ws=ws, stream=stream)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for l in range(L):
+            lid.copy_(index[l:l + 1])
+            m.moe_forward_stack(cfg, stack, lid, x, out=out, ws=ws,
+                                stream=torch.cuda.current_stream())
+
+    def timed(fn, reps):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / (reps * L)
+
+    reps = max(1, args.steps // L)
+    d_ms = timed(direct, reps)
+    g_ms = timed(graph.replay, reps)
+    m.moe_get_device_error(ws)
+    return {"layers": L, "direct_ms_per_layer": d_ms, "graph_ms_per_layer": g_ms,
+            "how": f"{reps} rounds over {L} seeded layers on one input: moe_forward per layer "
+                   f"vs one CUDA graph of moe_forward_stack (layer index written on the device)"}
 
 
 # ------------------------------------------------------------------ reference arm
@@ -537,6 +595,8 @@ def main(argv=None):
     ap.add_argument("--cpu-tokens", type=int, default=None)
     ap.add_argument("--ref-tokens", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stack", type=int, default=0,
+                    help="also time L layers dispatched directly vs one graph of a layer stack")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

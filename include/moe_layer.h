@@ -268,6 +268,45 @@ MOE_API moe_status_t moe_forward_ex(const moe_config_t* cfg, moe_weights_t weigh
                                     int32_t* topk_ids_out, float* topk_w_out, uint32_t flags,
                                     void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* ---- Layer stacks: one layer-oblivious descriptor table for L layers ----
+ * The layer-oblivious MoE kernel of "ASAP: A DiSaggregated and Asynchronous
+ * Inference System for MoE Prefill", section 3.4.2 (Bubble-Free Kernel
+ * Dispatching): the kernels can reach the weights of every layer, the
+ * per-layer addresses are precomputed in a device table, and the layer index
+ * is a device-side argument read when the kernels run.  A launch sequence
+ * recorded once (for instance a CUDA graph of moe_forward_stack) then serves
+ * any layer: the caller writes the index into device memory and replays, with
+ * no host work between layers.
+ *
+ * moe_stack_create
+ *   cfg         shape shared by every layer (T is the batch of later calls)
+ *   num_layers  L >= 1
+ *   layers      host array [L] of weight lists (as for moe_weights_create)
+ *   w_router    host array [L] of device pointers, bf16 [E, H] each
+ *   logit_bias  host array [L] of device pointers (fp32 [E] each, entries may be
+ *               NULL), or NULL for no bias in any layer
+ *   out         receives the handle; the library allocates one device table
+ *               (no weight copy).  The weights must outlive the handle.
+ * Errors: as moe_weights_create, for any layer. */
+typedef struct moe_stack* moe_stack_t;
+MOE_API moe_status_t moe_stack_create(const moe_config_t* cfg, int32_t num_layers,
+                                      const moe_weight_list_t* layers,
+                                      const void* const* w_router,
+                                      const float* const* logit_bias, moe_stack_t* out);
+/* Frees the stack's device table (synchronises the device first).  NULL is a no-op. */
+MOE_API void moe_stack_destroy(moe_stack_t stack);
+
+/* moe_forward on layer *layer of the stack.  layer: device pointer to one
+ * int32, read by the kernels when they run (not when this call returns), so it
+ * may be written between the replays of a recorded graph.  An index outside
+ * [0, L) sets MOE_ERR_BOUNDS in the status word and runs layer 0.  Other
+ * arguments as moe_forward (workspace op MOE_OP_FORWARD).  No host
+ * synchronisation, allocation or device->host copy: capturable in a CUDA graph. */
+MOE_API moe_status_t moe_forward_stack(const moe_config_t* cfg, moe_stack_t stack,
+                                       const int32_t* layer, const void* x, void* out,
+                                       int32_t* topk_ids_out, float* topk_w_out, void* ws,
+                                       size_t ws_bytes, moe_stream_t stream);
+
 /* fp8 weight preparation: 128x128 block quantisation of an fp32 [N, K] matrix
  * (N, K multiples of 128): scales[N/128, K/128] = amax/448 (1 for an all-zero
  * block), q = e4m3 rn_satfinite(w/s), computed in fp32.  Asynchronous. */

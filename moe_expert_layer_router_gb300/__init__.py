@@ -22,7 +22,7 @@ from ._native import MoeConfig, MoeError
 
 __all__ = ["MoeConfig", "MoeError", "make_config", "config_from", "Workspace", "ExpertWeights",
            "moe_route", "moe_permute", "moe_permute_noalloc", "moe_grouped_ffn", "moe_combine",
-           "moe_forward",
+           "moe_forward", "LayerStack", "moe_forward_stack",
            "moe_quantize_weight_fp8", "moe_quantize_act_fp8", "moe_get_device_error",
            "moe_workspace_size", "load"]
 
@@ -148,6 +148,7 @@ class ExpertWeights:
             wl.shared_gate_scales, wl.shared_up_scales, wl.shared_down_scales = (
                 s.data_ptr() for s in shared_scales)
         self.cfg = cfg
+        self._wl = wl
         h = C.c_void_p()
         N.check(N.lib().moe_weights_create(C.byref(cfg), C.byref(wl), C.byref(h)),
                 "moe_weights_create")
@@ -156,6 +157,45 @@ class ExpertWeights:
     def close(self):
         if getattr(self, "handle", None):
             N.lib().moe_weights_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class LayerStack:
+    """L layers of one shape behind one device descriptor table (moe_stack_create):
+    ``layers`` is a list of ExpertWeights (kept alive here), ``w_router`` a list of
+    bf16 [E, H] router matrices, ``bias`` None or a list of fp32 [E] tensors (or
+    None entries).  moe_forward_stack picks the layer from a device int32 tensor
+    when its kernels run, so one recorded CUDA graph serves every layer."""
+
+    def __init__(self, cfg: MoeConfig, layers, w_router, bias=None):
+        L = len(layers)
+        if L < 1 or len(w_router) != L or (bias is not None and len(bias) != L):
+            raise ValueError("layers, w_router (and bias) must list the same L >= 1 layers")
+        for l, w in enumerate(w_router):
+            _need(w, f"w_router[{l}]", torch.bfloat16, (cfg.E, cfg.H), None)
+        self._keep = [list(layers), list(w_router), bias]
+        wls = (N.MoeWeightList * L)(*[lw._wl for lw in layers])
+        routers = (C.c_void_p * L)(*[w.data_ptr() for w in w_router])
+        biases = None
+        if bias is not None:
+            biases = (C.c_void_p * L)(*[0 if b is None else b.data_ptr() for b in bias])
+        self._arrays = [wls, routers, biases]
+        self.cfg = cfg
+        self.num_layers = L
+        h = C.c_void_p()
+        N.check(N.lib().moe_stack_create(C.byref(cfg), L, wls, routers, biases, C.byref(h)),
+                "moe_stack_create")
+        self.handle = h.value
+
+    def close(self):
+        if getattr(self, "handle", None):
+            N.lib().moe_stack_destroy(self.handle)
             self.handle = None
 
     def __del__(self):
@@ -318,6 +358,30 @@ def moe_forward(cfg: MoeConfig, weights: ExpertWeights, x, w_router, bias=None, 
     N.check(N.lib().moe_forward_ex(C.byref(cfg), weights.handle, _ptr(x), _ptr(w_router),
                                    _ptr(bias), _ptr(out), _ptr(ids), _ptr(w), flags, ws.ptr,
                                    ws.nbytes, _stream(stream)), "moe_forward_ex")
+    return (out, ids, w) if return_routing else out
+
+
+def moe_forward_stack(cfg: MoeConfig, stack: LayerStack, layer, x, *, out=None,
+                      return_routing=False, ws=None, stream=None):
+    """moe_forward on layer ``layer`` (a device int32 tensor of one element, read
+    when the kernels run) of a LayerStack.  Returns out bf16 [T,H] (and (topk_ids,
+    topk_w) when return_routing)."""
+    dev = x.device
+    _need(x, "x", torch.bfloat16, (cfg.T, cfg.H), dev)
+    if layer.dtype != torch.int32 or layer.numel() != 1 or layer.device != dev:
+        raise ValueError("layer must be a one-element int32 tensor on the device of x")
+    if out is None:
+        out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
+    else:
+        _need(out, "out", torch.bfloat16, (cfg.T, cfg.H), dev)
+    ids = w = None
+    if return_routing:
+        ids = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=dev)
+        w = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=dev)
+    ws = _ws(ws, cfg, "forward", dev)
+    N.check(N.lib().moe_forward_stack(C.byref(cfg), stack.handle, _ptr(layer), _ptr(x),
+                                      _ptr(out), _ptr(ids), _ptr(w), ws.ptr, ws.nbytes,
+                                      _stream(stream)), "moe_forward_stack")
     return (out, ids, w) if return_routing else out
 
 

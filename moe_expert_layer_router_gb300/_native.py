@@ -55,6 +55,10 @@ _SIG = {
     "moe_get_device_error": (C.c_int, [_P, _P, C.POINTER(C.c_int32)]),
     "moe_weights_create": (C.c_int, [_CFG, C.POINTER(MoeWeightList), C.POINTER(_P)]),
     "moe_weights_destroy": (None, [_P]),
+    "moe_stack_create": (C.c_int, [_CFG, C.c_int32, C.POINTER(MoeWeightList), _P, _P,
+                                   C.POINTER(_P)]),
+    "moe_stack_destroy": (None, [_P]),
+    "moe_forward_stack": (C.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
     "moe_route": (C.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
     "moe_permute": (C.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
     "moe_grouped_ffn": (C.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),

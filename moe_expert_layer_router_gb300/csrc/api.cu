@@ -290,6 +290,40 @@ struct moe_weights {
   const float** scales2;  // fp8: down of group g at g
 };
 
+// Descriptor tables one call reads: a single layer's, or a layer stack's
+// (layer 0's entries plus a device layer index and the per-layer stride).
+struct moe_stack {
+  moe_config_t cfg;
+  int device;
+  int32_t num_layers;
+  int32_t G;
+  void* table;              // device: maps [L][3G] | router maps [L] | bias [L] | fp8 scales [L][3G]
+  CUtensorMap* maps;
+  CUtensorMap* router;
+  const float** bias;
+  const float** scales;
+};
+
+namespace moe {
+struct WeightView {
+  const CUtensorMap* maps1;
+  const CUtensorMap* maps2;
+  const float* const* scales1;
+  const float* const* scales2;
+  const int32_t* layer;
+  int32_t stride;
+  int32_t num_layers;
+};
+static WeightView view_of(const moe_weights* W) {
+  return WeightView{W->maps1, W->maps2, W->scales1, W->scales2, nullptr, 0, 1};
+}
+static WeightView view_of(const moe_stack* S, const int32_t* layer) {
+  const bool fp8 = S->cfg.wtype == MOE_DTYPE_FP8_E4M3;
+  return WeightView{S->maps, S->maps + 2 * S->G, fp8 ? S->scales : nullptr,
+                    fp8 ? S->scales + 2 * S->G : nullptr, layer, 3 * S->G, S->num_layers};
+}
+}  // namespace moe
+
 using namespace moe;
 
 extern "C" {
@@ -348,16 +382,12 @@ moe_status_t moe_get_device_error(void* ws, moe_stream_t stream, int32_t* device
   return MOE_OK;
 }
 
-moe_status_t moe_weights_create(const moe_config_t* cfg, const moe_weight_list_t* wl,
-                                moe_weights_t* out) {
-  MOE_TRY(check_config(cfg));
-  if (!wl || !out) return fail(MOE_ERR_INVALID_ARG, "weights or out is NULL");
-  *out = nullptr;
+// Validates one layer's weight list and encodes its 3G TMA descriptors
+// (GEMM1: gate / up of group g at 2g / 2g+1; GEMM2: down of group g at 2G+g)
+// and, for fp8, the matching scale pointers, into maps[3G] / scales[3G].
+static moe_status_t encode_layer(const moe_config_t* cfg, const moe_weight_list_t* wl,
+                                 CUtensorMap* maps, const float** scales, bool encode = true) {
   const bool fp8 = cfg->wtype == MOE_DTYPE_FP8_E4M3;
-  if (fp8 && (cfg->H / 128 > kFp8MaxKBlocks || cfg->I / 128 > kFp8MaxKBlocks ||
-              cfg->I_shared / 128 > kFp8MaxKBlocks))
-    return fail(MOE_ERR_UNSUPPORTED, "fp8 layers need H, I and I_shared <= %d",
-                128 * kFp8MaxKBlocks);
   if (!wl->gate || !wl->up || !wl->down)
     return fail(MOE_ERR_INVALID_ARG, "gate/up/down pointer arrays must not be NULL");
   if (fp8 && (!wl->gate_scales || !wl->up_scales || !wl->down_scales))
@@ -391,11 +421,10 @@ moe_status_t moe_weights_create(const moe_config_t* cfg, const moe_weight_list_t
       MOE_TRY(check_ptr4(wl->shared_down_scales, "shared_down_scales"));
     }
   }
+  if (!encode) return MOE_OK;  // checks only
   const int G = E + (shared ? 1 : 0);
-  std::vector<CUtensorMap> maps(3 * G);
-  std::vector<const float*> scales(fp8 ? 3 * G : 0);
-  CUtensorMap* m1 = maps.data();
-  CUtensorMap* m2 = maps.data() + 2 * G;
+  CUtensorMap* m1 = maps;
+  CUtensorMap* m2 = maps + 2 * G;
   const uint64_t H = cfg->H, I = cfg->I, Is = cfg->I_shared;
   for (int g = 0; g < G; ++g) {
     const bool sh = g == E;
@@ -418,6 +447,24 @@ moe_status_t moe_weights_create(const moe_config_t* cfg, const moe_weight_list_t
       scales[2 * G + g] = sh ? wl->shared_down_scales : wl->down_scales[g];
     }
   }
+
+  return MOE_OK;
+}
+
+moe_status_t moe_weights_create(const moe_config_t* cfg, const moe_weight_list_t* wl,
+                                moe_weights_t* out) {
+  MOE_TRY(check_config(cfg));
+  if (!wl || !out) return fail(MOE_ERR_INVALID_ARG, "weights or out is NULL");
+  *out = nullptr;
+  const bool fp8 = cfg->wtype == MOE_DTYPE_FP8_E4M3;
+  if (fp8 && (cfg->H / 128 > kFp8MaxKBlocks || cfg->I / 128 > kFp8MaxKBlocks ||
+              cfg->I_shared / 128 > kFp8MaxKBlocks))
+    return fail(MOE_ERR_UNSUPPORTED, "fp8 layers need H, I and I_shared <= %d",
+                128 * kFp8MaxKBlocks);
+  const int G = cfg->E + (cfg->I_shared > 0 ? 1 : 0);
+  std::vector<CUtensorMap> maps(3 * G);
+  std::vector<const float*> scales(fp8 ? 3 * G : 0);
+  MOE_TRY(encode_layer(cfg, wl, maps.data(), scales.data()));
   void* table = nullptr;
   const size_t map_bytes = maps.size() * sizeof(CUtensorMap);
   const size_t sc_bytes = scales.size() * sizeof(const float*);
@@ -443,6 +490,85 @@ moe_status_t moe_weights_create(const moe_config_t* cfg, const moe_weight_list_t
   return MOE_OK;
 }
 
+moe_status_t moe_stack_create(const moe_config_t* cfg, int32_t num_layers,
+                              const moe_weight_list_t* layers, const void* const* w_router,
+                              const float* const* logit_bias, moe_stack_t* out) {
+  MOE_TRY(check_config(cfg));
+  if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (num_layers < 1) return fail(MOE_ERR_INVALID_ARG, "num_layers = %d", num_layers);
+  if (!layers || !w_router) return fail(MOE_ERR_INVALID_ARG, "layers or w_router is NULL");
+  const bool fp8 = cfg->wtype == MOE_DTYPE_FP8_E4M3;
+  if (fp8 && (cfg->H / 128 > kFp8MaxKBlocks || cfg->I / 128 > kFp8MaxKBlocks ||
+              cfg->I_shared / 128 > kFp8MaxKBlocks))
+    return fail(MOE_ERR_UNSUPPORTED, "fp8 layers need H, I and I_shared <= %d",
+                128 * kFp8MaxKBlocks);
+  const int L = num_layers;
+  const int G = cfg->E + (cfg->I_shared > 0 ? 1 : 0);
+  const int E_pad = (cfg->E + 15) / 16 * 16;
+  std::vector<CUtensorMap> maps(size_t(L) * 3 * G), router(L);
+  std::vector<const float*> bias(L, nullptr);
+  std::vector<const float*> scales(fp8 ? size_t(L) * 3 * G : 0);
+  // every layer's arguments are checked before anything is encoded
+  for (int l = 0; l < L; ++l) {
+    MOE_TRY(encode_layer(cfg, &layers[l], nullptr, nullptr, false));
+    char nm[48];
+    snprintf(nm, sizeof nm, "w_router[%d]", l);
+    MOE_TRY(check_ptr(w_router[l], nm));
+    if (logit_bias && logit_bias[l]) {
+      snprintf(nm, sizeof nm, "logit_bias[%d]", l);
+      MOE_TRY(check_ptr4(logit_bias[l], nm));
+      bias[l] = logit_bias[l];
+    }
+  }
+  for (int l = 0; l < L; ++l) {
+    MOE_TRY(encode_layer(cfg, &layers[l], maps.data() + size_t(l) * 3 * G,
+                         fp8 ? scales.data() + size_t(l) * 3 * G : nullptr));
+    MOE_TRY(encode_2d(&router[l], true, w_router[l], cfg->H, cfg->E, kTileK, E_pad));
+  }
+  // device table: maps [L][3G] | router maps [L] | bias [L] | fp8 scales [L][3G]
+  const size_t maps_b = maps.size() * sizeof(CUtensorMap);
+  const size_t router_b = router.size() * sizeof(CUtensorMap);
+  const size_t bias_b = bias.size() * sizeof(const float*);
+  const size_t scales_b = scales.size() * sizeof(const float*);
+  void* table = nullptr;
+  MOE_CUDA(cudaMalloc(&table, maps_b + router_b + bias_b + scales_b));
+  uint8_t* tb = static_cast<uint8_t*>(table);
+  cudaError_t e = cudaMemcpy(tb, maps.data(), maps_b, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(tb + maps_b, router.data(), router_b, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(tb + maps_b + router_b, bias.data(), bias_b, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && scales_b)
+    e = cudaMemcpy(tb + maps_b + router_b + bias_b, scales.data(), scales_b, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(table);
+    return cuda_fail(e, "cudaMemcpy(stack table)");
+  }
+  moe_stack* st = new moe_stack;
+  st->cfg = *cfg;
+  st->device = current_device();
+  st->num_layers = L;
+  st->G = G;
+  st->table = table;
+  st->maps = reinterpret_cast<CUtensorMap*>(tb);
+  st->router = reinterpret_cast<CUtensorMap*>(tb + maps_b);
+  st->bias = reinterpret_cast<const float**>(tb + maps_b + router_b);
+  st->scales = fp8 ? reinterpret_cast<const float**>(tb + maps_b + router_b + bias_b) : nullptr;
+  *out = st;
+  return MOE_OK;
+}
+
+void moe_stack_destroy(moe_stack_t st) {
+  if (!st) return;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(st->device);
+  cudaDeviceSynchronize();
+  cudaFree(st->table);
+  cudaSetDevice(prev);
+  delete st;
+}
+
 void moe_weights_destroy(moe_weights_t w) {
   if (!w) return;
   int prev = 0;
@@ -461,14 +587,15 @@ namespace moe {
 
 static moe_status_t run_route(const moe_config_t& c, const void* x, const void* w_router,
                               const float* bias, int32_t* ids, float* w, float* logits,
-                              uint32_t* err, cudaStream_t st) {
+                              uint32_t* err, cudaStream_t st, const RouterTable* table = nullptr) {
   const int E_pad = (c.E + 15) / 16 * 16;
   CUtensorMap mx, mw;
   MOE_TRY(encode_2d(&mx, true, x, c.H, c.T, kTileK, kTileM));
-  MOE_TRY(encode_2d(&mw, true, w_router, c.H, c.E, kTileK, E_pad));
+  if (table) mw = mx;  // unused: the kernel reads the layer's descriptor from the table
+  else MOE_TRY(encode_2d(&mw, true, w_router, c.H, c.E, kTileK, E_pad));
   trace_mark(st, MOE_K_ROUTER);
   MOE_CUDA(launch_router(mx, mw, c.T, c.H, c.E, E_pad, c.k, c.score, c.renormalize, c.route_scale,
-                         bias, ids, w, logits, err, sm_count(), st));
+                         bias, ids, w, logits, err, sm_count(), st, table));
   return MOE_OK;
 }
 
@@ -495,7 +622,7 @@ static moe_status_t run_permute(const moe_config_t& c, const Layout& L, void* ws
 // bf16 grouped FFN.  GEMM1's routed rows come from x_perm (tile loads) or,
 // when gather_rows (row -> token) is given, straight from the unpermuted
 // tokens x_perm = x by TMA row gathers (the permuted copy is never written).
-static moe_status_t run_ffn(const moe_config_t& c, const moe_weights* W, const Layout& L, void* ws,
+static moe_status_t run_ffn(const moe_config_t& c, const WeightView& W, const Layout& L, void* ws,
                             const void* x_perm, const int32_t* offsets, const float* row_weight,
                             const void* x_shared, void* y_perm, void* shared_out,
                             cudaStream_t st, const int32_t* gather_rows = nullptr,
@@ -519,7 +646,10 @@ static moe_status_t run_ffn(const moe_config_t& c, const moe_weights* W, const L
   if (shared) MOE_TRY(encode_2d(&a1, true, x_shared, c.H, c.T, kTileK, kTileM));
   else a1 = a0;
   GemmArgs g1{};
-  g1.b_maps = W->maps1;
+  g1.b_maps = W.maps1;
+  g1.layer = W.layer;
+  g1.layer_stride = W.stride;
+  g1.num_layers = W.num_layers;
   g1.offsets = offsets;
   g1.sched = s1;
   g1.out0 = h;
@@ -545,7 +675,7 @@ static moe_status_t run_ffn(const moe_config_t& c, const moe_weights* W, const L
   else b1 = b0;
   GemmArgs g2 = g1;
   g2.gather_rows = nullptr;
-  g2.b_maps = W->maps2;
+  g2.b_maps = W.maps2;
   g2.sched = s2;
   g2.out0 = y_perm;
   g2.out1 = shared_out;
@@ -563,7 +693,7 @@ static moe_status_t run_ffn(const moe_config_t& c, const moe_weights* W, const L
 
 // fp8: e4m3 rows (x_perm, x_shared) with 1x128 scales -> GEMM1 (e4m3 h + scales
 // in the workspace) -> GEMM2 (fp32 y_perm / shared_out).
-static moe_status_t run_ffn_fp8(const moe_config_t& c, const moe_weights* W, const Layout& L,
+static moe_status_t run_ffn_fp8(const moe_config_t& c, const WeightView& W, const Layout& L,
                                 void* ws, const void* x_perm, const float* x_perm_scales,
                                 const int32_t* offsets, const float* row_weight,
                                 const void* x_shared, const float* x_shared_scales, void* y_perm,
@@ -588,8 +718,11 @@ static moe_status_t run_ffn_fp8(const moe_config_t& c, const moe_weights* W, con
   if (shared) MOE_TRY(encode_2d(&t1, false, x_shared, c.H, c.T, 128, 32));
   else t1 = t0;
   Fp8GemmArgs g1{};
-  g1.w_maps = W->maps1;
-  g1.w_scales = W->scales1;
+  g1.w_maps = W.maps1;
+  g1.w_scales = W.scales1;
+  g1.layer = W.layer;
+  g1.layer_stride = W.stride;
+  g1.num_layers = W.num_layers;
   g1.offsets = offsets;
   g1.sched = s1;
   g1.tok_scales0 = x_perm_scales;
@@ -615,8 +748,8 @@ static moe_status_t run_ffn_fp8(const moe_config_t& c, const moe_weights* W, con
   if (shared) MOE_TRY(encode_2d(&u1, false, hs, c.I_shared, c.T, 128, 32));
   else u1 = u0;
   Fp8GemmArgs g2 = g1;
-  g2.w_maps = W->maps2;
-  g2.w_scales = W->scales2;
+  g2.w_maps = W.maps2;
+  g2.w_scales = W.scales2;
   g2.sched = s2;
   g2.tok_scales0 = h_sc;
   g2.tok_scales1 = shared ? hs_sc : h_sc;
@@ -637,6 +770,71 @@ static moe_status_t run_ffn_fp8(const moe_config_t& c, const moe_weights* W, con
 static bool same_shape(const moe_config_t& a, const moe_config_t& b) {
   return a.H == b.H && a.E == b.E && a.I == b.I && a.I_shared == b.I_shared && a.wtype == b.wtype;
 }
+
+// The layer forward after validation: route (one router matrix, or a stack's
+// router table), permute, grouped FFN over the view's descriptors, combine.
+static moe_status_t forward_impl(const moe_config_t* cfg, const WeightView& W, const void* x,
+                                 const void* w_router, const float* logit_bias,
+                                 const RouterTable* rt, void* out, int32_t* topk_ids_out,
+                                 float* topk_w_out, uint32_t flags, void* ws,
+                                 moe_stream_t stream) {
+  const bool fp8 = cfg->wtype == MOE_DTYPE_FP8_E4M3;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const Layout L = layout(*cfg, MOE_OP_FORWARD);
+  uint32_t* err = err_word(ws);
+  int32_t* ids = topk_ids_out ? topk_ids_out : at<int32_t*>(ws, L.ids);
+  float* w = topk_w_out ? topk_w_out : at<float*>(ws, L.w);
+  int32_t* counts = at<int32_t*>(ws, L.counts);
+  int32_t* offsets = at<int32_t*>(ws, L.offsets);
+  int32_t* perm_token = at<int32_t*>(ws, L.perm_token);
+  int32_t* inv_row = at<int32_t*>(ws, L.inv_row);
+  float* row_weight = at<float*>(ws, L.row_weight);
+  const bool fused = (flags & MOE_FORWARD_FUSED_DISPATCH) && !fp8;
+  void* x_perm = at<void*>(ws, L.x_perm);
+  void* y_perm = at<void*>(ws, L.y_perm);
+  void* shared_out = cfg->I_shared > 0 ? at<void*>(ws, L.shared_out) : nullptr;
+
+  MOE_TRY(run_route(*cfg, x, w_router, logit_bias, ids, w, nullptr, err, st, rt));
+  float* x_perm_sc = fp8 ? at<float*>(ws, L.x_perm_sc) : nullptr;
+  MOE_TRY(run_permute(*cfg, L, ws, ids, w, x, counts, offsets, perm_token, inv_row, row_weight,
+                      fused ? nullptr : x_perm, x_perm_sc, st));
+  // bf16 layers keep y and the shared output as fp16 with a power-of-two
+  // scale per 32 columns, inside the fp32-sized workspace regions: the
+  // scales follow the fp16 rows
+  const int64_t R = cfg->T * cfg->k;
+  float* y_sc = fp8 ? nullptr : reinterpret_cast<float*>(static_cast<uint8_t*>(y_perm) +
+                                                         size_t(R) * cfg->H * 2);
+  float* sh_sc = (fp8 || !shared_out) ? nullptr
+                                      : reinterpret_cast<float*>(static_cast<uint8_t*>(shared_out) +
+                                                                 size_t(cfg->T) * cfg->H * 2);
+  if (fused) {
+    // fused dispatch: GEMM1 gathers each expert's rows from x by token index
+    MOE_TRY(run_ffn(*cfg, W, L, ws, x, offsets, row_weight, x, y_perm, shared_out, st,
+                    perm_token, y_sc, sh_sc));
+  } else if (!fp8) {
+    MOE_TRY(run_ffn(*cfg, W, L, ws, x_perm, offsets, row_weight, x, y_perm, shared_out, st,
+                    nullptr, y_sc, sh_sc));
+  } else {
+    // the shared expert reads every token: quantise x once more, unpermuted
+    uint8_t* xq = cfg->I_shared > 0 ? at<uint8_t*>(ws, L.xq) : nullptr;
+    float* xq_sc = cfg->I_shared > 0 ? at<float*>(ws, L.xq_sc) : nullptr;
+    if (xq) {
+      trace_mark(st, MOE_K_QUANT);
+      MOE_CUDA(launch_quant_act_fp8(x, cfg->T, cfg->H, xq, xq_sc, st));
+    }
+    MOE_TRY(run_ffn_fp8(*cfg, W, L, ws, x_perm, x_perm_sc, offsets, row_weight, xq, xq_sc,
+                        y_perm, shared_out, st));
+  }
+  trace_mark(st, MOE_K_COMBINE);
+  if (fp8)
+    MOE_CUDA(launch_combine(y_perm, inv_row, shared_out, out, cfg->T, cfg->k, cfg->H, R, err, st));
+  else
+    MOE_CUDA(launch_combine_half(y_perm, y_sc, inv_row, shared_out, sh_sc, out, cfg->T, cfg->k,
+                                 cfg->H, R, err, st));
+  trace_mark(st, -1);
+  return MOE_OK;
+}
+
 
 }  // namespace moe
 
@@ -726,9 +924,9 @@ moe_status_t moe_grouped_ffn(const moe_config_t* cfg, moe_weights_t weights, con
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const void* xs = cfg->I_shared > 0 ? x_shared : nullptr;
   const moe_status_t s =
-      fp8 ? run_ffn_fp8(*cfg, weights, L, ws, x_perm, x_perm_scales, expert_offsets, row_weight,
+      fp8 ? run_ffn_fp8(*cfg, view_of(weights), L, ws, x_perm, x_perm_scales, expert_offsets, row_weight,
                         xs, x_shared_scales, y_perm, shared_out, st)
-          : run_ffn(*cfg, weights, L, ws, x_perm, expert_offsets, row_weight, xs, y_perm,
+          : run_ffn(*cfg, view_of(weights), L, ws, x_perm, expert_offsets, row_weight, xs, y_perm,
                     shared_out, st);
   trace_mark(st, -1);
   return s;
@@ -772,7 +970,6 @@ moe_status_t moe_forward_ex(const moe_config_t* cfg, moe_weights_t weights, cons
   if (!weights) return fail(MOE_ERR_INVALID_ARG, "weights is NULL");
   if (!same_shape(weights->cfg, *cfg))
     return fail(MOE_ERR_INVALID_ARG, "weights were created for a different layer shape");
-  const bool fp8 = cfg->wtype == MOE_DTYPE_FP8_E4M3;
   if (cfg->T == 0) return MOE_OK;
   MOE_TRY(check_ptr(x, "x"));
   MOE_TRY(check_ptr(w_router, "w_router"));
@@ -780,60 +977,27 @@ moe_status_t moe_forward_ex(const moe_config_t* cfg, moe_weights_t weights, cons
   if (logit_bias) MOE_TRY(check_ptr4(logit_bias, "logit_bias"));
   if (topk_ids_out) MOE_TRY(check_ptr4(topk_ids_out, "topk_ids_out"));
   if (topk_w_out) MOE_TRY(check_ptr4(topk_w_out, "topk_w_out"));
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const Layout L = layout(*cfg, MOE_OP_FORWARD);
-  uint32_t* err = err_word(ws);
-  int32_t* ids = topk_ids_out ? topk_ids_out : at<int32_t*>(ws, L.ids);
-  float* w = topk_w_out ? topk_w_out : at<float*>(ws, L.w);
-  int32_t* counts = at<int32_t*>(ws, L.counts);
-  int32_t* offsets = at<int32_t*>(ws, L.offsets);
-  int32_t* perm_token = at<int32_t*>(ws, L.perm_token);
-  int32_t* inv_row = at<int32_t*>(ws, L.inv_row);
-  float* row_weight = at<float*>(ws, L.row_weight);
-  const bool fused = (flags & MOE_FORWARD_FUSED_DISPATCH) && !fp8;
-  void* x_perm = at<void*>(ws, L.x_perm);
-  void* y_perm = at<void*>(ws, L.y_perm);
-  void* shared_out = cfg->I_shared > 0 ? at<void*>(ws, L.shared_out) : nullptr;
+  return forward_impl(cfg, view_of(weights), x, w_router, logit_bias, nullptr, out, topk_ids_out,
+                      topk_w_out, flags, ws, stream);
+}
 
-  MOE_TRY(run_route(*cfg, x, w_router, logit_bias, ids, w, nullptr, err, st));
-  float* x_perm_sc = fp8 ? at<float*>(ws, L.x_perm_sc) : nullptr;
-  MOE_TRY(run_permute(*cfg, L, ws, ids, w, x, counts, offsets, perm_token, inv_row, row_weight,
-                      fused ? nullptr : x_perm, x_perm_sc, st));
-  // bf16 layers keep y and the shared output as fp16 with a power-of-two
-  // scale per 32 columns, inside the fp32-sized workspace regions: the
-  // scales follow the fp16 rows
-  const int64_t R = cfg->T * cfg->k;
-  float* y_sc = fp8 ? nullptr : reinterpret_cast<float*>(static_cast<uint8_t*>(y_perm) +
-                                                         size_t(R) * cfg->H * 2);
-  float* sh_sc = (fp8 || !shared_out) ? nullptr
-                                      : reinterpret_cast<float*>(static_cast<uint8_t*>(shared_out) +
-                                                                 size_t(cfg->T) * cfg->H * 2);
-  if (fused) {
-    // fused dispatch: GEMM1 gathers each expert's rows from x by token index
-    MOE_TRY(run_ffn(*cfg, weights, L, ws, x, offsets, row_weight, x, y_perm, shared_out, st,
-                    perm_token, y_sc, sh_sc));
-  } else if (!fp8) {
-    MOE_TRY(run_ffn(*cfg, weights, L, ws, x_perm, offsets, row_weight, x, y_perm, shared_out, st,
-                    nullptr, y_sc, sh_sc));
-  } else {
-    // the shared expert reads every token: quantise x once more, unpermuted
-    uint8_t* xq = cfg->I_shared > 0 ? at<uint8_t*>(ws, L.xq) : nullptr;
-    float* xq_sc = cfg->I_shared > 0 ? at<float*>(ws, L.xq_sc) : nullptr;
-    if (xq) {
-      trace_mark(st, MOE_K_QUANT);
-      MOE_CUDA(launch_quant_act_fp8(x, cfg->T, cfg->H, xq, xq_sc, st));
-    }
-    MOE_TRY(run_ffn_fp8(*cfg, weights, L, ws, x_perm, x_perm_sc, offsets, row_weight, xq, xq_sc,
-                        y_perm, shared_out, st));
-  }
-  trace_mark(st, MOE_K_COMBINE);
-  if (fp8)
-    MOE_CUDA(launch_combine(y_perm, inv_row, shared_out, out, cfg->T, cfg->k, cfg->H, R, err, st));
-  else
-    MOE_CUDA(launch_combine_half(y_perm, y_sc, inv_row, shared_out, sh_sc, out, cfg->T, cfg->k,
-                                 cfg->H, R, err, st));
-  trace_mark(st, -1);
-  return MOE_OK;
+moe_status_t moe_forward_stack(const moe_config_t* cfg, moe_stack_t stack, const int32_t* layer,
+                               const void* x, void* out, int32_t* topk_ids_out, float* topk_w_out,
+                               void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  MOE_TRY(check_ws(*cfg, MOE_OP_FORWARD, ws, ws_bytes));
+  if (!stack) return fail(MOE_ERR_INVALID_ARG, "stack is NULL");
+  if (!same_shape(stack->cfg, *cfg))
+    return fail(MOE_ERR_INVALID_ARG, "the stack was created for a different layer shape");
+  MOE_TRY(check_ptr4(layer, "layer"));
+  if (cfg->T == 0) return MOE_OK;
+  MOE_TRY(check_ptr(x, "x"));
+  MOE_TRY(check_ptr(out, "out"));
+  if (topk_ids_out) MOE_TRY(check_ptr4(topk_ids_out, "topk_ids_out"));
+  if (topk_w_out) MOE_TRY(check_ptr4(topk_w_out, "topk_w_out"));
+  const RouterTable rt{stack->router, stack->bias, layer, stack->num_layers};
+  return forward_impl(cfg, view_of(stack, layer), x, nullptr, nullptr, &rt, out, topk_ids_out,
+                      topk_w_out, 0u, ws, stream);
 }
 
 moe_status_t moe_quantize_weight_fp8(const float* w, int64_t N, int64_t K, uint8_t* q,

@@ -129,13 +129,13 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint3
 // B operand of this CTA for a tile: GEMM1 -- gate and up rows [128 n + 64 r,
 // +64) (two boxes); GEMM2 -- W_down rows [256 n + 128 r, +128).
 template <bool kSwiGLU>
-__device__ __forceinline__ void b_operand(const Tile& x, uint32_t rank, const GemmArgs& args,
+__device__ __forceinline__ void b_operand(const Tile& x, uint32_t rank, const CUtensorMap* bmaps,
                                           const CUtensorMap*& mb, int& b_row) {
   if (kSwiGLU) {
-    mb = args.b_maps + 2 * x.g;
+    mb = bmaps + 2 * x.g;
     b_row = x.n_blk * kGemm1TileN + int(rank) * (kGemmBRows / 2);
   } else {
-    mb = args.b_maps + x.g;
+    mb = bmaps + x.g;
     b_row = x.n_blk * kGemm2TileN + int(rank) * kGemmBRows;
   }
 }
@@ -170,6 +170,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int pair = blockIdx.x >> 1;
   const int num_pairs = gridDim.x >> 1;
   const int G = args.E + args.has_shared;
+  // weight descriptors of this call's layer (layer stacks index their table)
+  const CUtensorMap* bmaps =
+      args.b_maps + resolve_layer(args.layer, args.num_layers, args.err) * args.layer_stride;
 
   for (int i = threadIdx.x; i < sched_ints(G); i += kThreads) c.sched[i] = args.sched[i];
   for (int i = threadIdx.x; i <= args.E; i += kThreads) c.offsets[i] = args.offsets[i];
@@ -215,7 +218,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                            : static_cast<const void*>(&map_a1);
           const CUtensorMap* mb;
           int b_row;
-          b_operand<kSwiGLU>(x, rank, args, mb, b_row);
+          b_operand<kSwiGLU>(x, rank, bmaps, mb, b_row);
           // A rows of this CTA: 128 (full tile) or 64 (half tile; the box still
           // brings 128 rows, the MMA reads the first 64)
           const int a_row = x.row0 + x.m_blk * kPairRows +
@@ -247,7 +250,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                    : static_cast<const void*>(&map_a1);
         const CUtensorMap* mb;
         int b_row;
-        b_operand<kSwiGLU>(x, rank, args, mb, b_row);
+        b_operand<kSwiGLU>(x, rank, bmaps, mb, b_row);
         const int a_row = x.row0 + x.m_blk * kPairRows + int(rank) * cta_rows;
         // gathers bring exactly the rows used; tile loads (shared expert) 128
         const uint32_t a_bytes = routed ? uint32_t(cta_rows) * 128u : uint32_t(kABytes);

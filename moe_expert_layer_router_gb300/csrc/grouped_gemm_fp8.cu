@@ -146,6 +146,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = args.E + args.has_shared;
+  // weight descriptors and scales of this call's layer (layer stacks)
+  const int layer = resolve_layer(args.layer, args.num_layers, args.err);
+  const CUtensorMap* wmaps = args.w_maps + layer * args.layer_stride;
+  const float* const* wscales = args.w_scales + layer * args.layer_stride;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -184,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n_tok = left < C::kTok ? left : C::kTok;
         const int n_box = (n_tok + kTokBox - 1) / kTokBox;
         const int tok_row = x.row0 + x.tok_blk * C::kTok;
-        const CUtensorMap* mw = kGateUp ? args.w_maps + 2 * x.g : args.w_maps + x.g;
+        const CUtensorMap* mw = kGateUp ? wmaps + 2 * x.g : wmaps + x.g;
         const int w_row = x.w_blk * kWRows;
         const uint32_t bytes = (kGateUp ? 2 : 1) * kWBytes + n_box * kTokBox * kKB;
         const int kb_n = x.K / kKB;
@@ -268,8 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         c.tok_scale[j * kMaxKB + kb] = __ldg(ts + int64_t(tok_row + j) * kb_n + kb);
       }
       epi_sync();
-      const float* ws0 = args.w_scales[kGateUp ? 2 * x.g : x.g] + int64_t(x.w_blk) * kb_n;
-      const float* ws1 = kGateUp ? args.w_scales[2 * x.g + 1] + int64_t(x.w_blk) * kb_n : ws0;
+      const float* ws0 = wscales[kGateUp ? 2 * x.g : x.g] + int64_t(x.w_blk) * kb_n;
+      const float* ws1 = kGateUp ? wscales[2 * x.g + 1] + int64_t(x.w_blk) * kb_n : ws0;
       float acc0[C::kTok], acc1[kGateUp ? C::kTok : 1];
 #pragma unroll
       for (int j = 0; j < C::kTok; ++j) acc0[j] = 0.0f;

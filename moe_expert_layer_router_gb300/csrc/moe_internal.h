@@ -39,8 +39,24 @@ constexpr int kFp8MaxKBlocks = 64; // fp8: at most 64 K blocks of 128 (H, I <= 8
 //   [G+2 .. 2G+1]  group processed in each slot (heaviest first)
 __host__ __device__ inline int sched_ints(int G) { return 2 * G + 2; }
 
+// Layer of a layer-stack call: *layer when given (read at kernel time; an
+// index outside [0, n) sets kErrBounds and selects layer 0), else 0.
+__device__ __forceinline__ int resolve_layer(const int32_t* layer, int n, uint32_t* err) {
+  if (layer == nullptr) return 0;
+  const int l = *reinterpret_cast<const volatile int32_t*>(layer);
+  if (l < 0 || l >= n) {
+    if (threadIdx.x == 0) atomicOr(err, kErrBounds);
+    return 0;
+  }
+  return l;
+}
+
 struct GemmArgs {
   const CUtensorMap* b_maps;   // GEMM1: gate of group g at 2g, up at 2g+1; GEMM2: down at g
+                               // (layer 0's, in a layer stack)
+  const int32_t* layer;        // layer stack: device layer index, else null
+  int32_t layer_stride;        // descriptors per layer in the stack table
+  int32_t num_layers;
   const int32_t* offsets;      // [E+1] routed row offsets
   const int32_t* sched;        // tile schedule (see above)
   void* out0;                  // routed output rows (GEMM1: bf16 h, GEMM2: fp32 y or fp16 y)
@@ -63,6 +79,9 @@ struct GemmArgs {
 struct Fp8GemmArgs {
   const CUtensorMap* w_maps;      // GEMM1: gate of group g at 2g, up at 2g+1; GEMM2: down at g
   const float* const* w_scales;   // same indexing; each [rows/128, K/128] fp32
+  const int32_t* layer;           // layer stack: device layer index (both tables advance
+  int32_t layer_stride;           //   by layer_stride entries per layer), else null
+  int32_t num_layers;
   const int32_t* offsets;         // [E+1] routed row offsets
   const int32_t* sched;           // tile schedule (64-token tiles)
   const float* tok_scales0;       // routed token scales [T*k, K/128]
@@ -79,10 +98,19 @@ struct Fp8GemmArgs {
 };
 
 // --------------------------------------------------------------- launchers
+// Router of one layer, or (w_table non-null) of layer *layer of a stack whose
+// router descriptors and bias pointers are device tables [num_layers].
+struct RouterTable {
+  const CUtensorMap* w_table;
+  const float* const* bias_table;
+  const int32_t* layer;
+  int32_t num_layers;
+};
 cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_w, int64_t T, int H,
                           int E, int E_pad, int k, int score, int renormalize, float route_scale,
                           const float* bias, int32_t* topk_ids, float* topk_w, float* logits_out,
-                          uint32_t* err, int sm_count, cudaStream_t stream);
+                          uint32_t* err, int sm_count, cudaStream_t stream,
+                          const RouterTable* table = nullptr);
 
 cudaError_t launch_hist(const int32_t* ids, int64_t T, int k, int E, int32_t* blk_counts,
                         uint32_t* err, cudaStream_t stream);

@@ -63,6 +63,7 @@ struct RouterArgs {
   float* logits_out;
   uint32_t* err;
   uint32_t tmem_cols;
+  RouterTable table;  // layer stacks: per-layer router descriptors and biases
 };
 
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
@@ -191,8 +192,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int S = static_cast<int>(ptx::cluster_nctarank());   // K split of this token tile
   const uint32_t crank = ptx::cluster_ctarank();
   const int64_t m0 = int64_t(blockIdx.x / S) * kTileM;
+  // this call's router matrix and bias (a layer stack indexes its tables)
+  const float* bias = a.bias;
+  const void* map_w_ptr = &map_w;
+  if (a.table.w_table) {
+    const int l = resolve_layer(a.table.layer, a.table.num_layers, a.err);
+    map_w_ptr = a.table.w_table + l;
+    bias = a.table.bias_table[l];
+  }
 
-  for (int i = threadIdx.x; i < a.E; i += kThreads) c.bias[i] = a.bias ? a.bias[i] : 0.0f;
+  for (int i = threadIdx.x; i < a.E; i += kThreads) c.bias[i] = bias ? bias[i] : 0.0f;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&c.full[s], 1);
@@ -227,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ptx::mbar_wait(&c.empty[s], ph ^ 1, abort, a.err)) break;
         ptx::mbar_arrive_expect_tx(&c.full[s], stage_bytes);
         ptx::tma_load_2d(a_tiles + s * kABytes, &map_x, &c.full[s], kb * kTileK, int32_t(m0));
-        ptx::tma_load_2d(b_tiles + s * kMaxBBytes, &map_w, &c.full[s], kb * kTileK, 0);
+        ptx::tma_load_2d(b_tiles + s * kMaxBBytes, map_w_ptr, &c.full[s], kb * kTileK, 0);
       }
       if (*abort) {
         const uint32_t first = it > kStages ? it - kStages : 0;
@@ -486,7 +495,8 @@ cudaError_t launch_k(const CUtensorMap& mx, const CUtensorMap& mw, const RouterA
 cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_w, int64_t T, int H,
                           int E, int E_pad, int k, int score, int renormalize, float route_scale,
                           const float* bias, int32_t* topk_ids, float* topk_w, float* logits_out,
-                          uint32_t* err, int sm_count, cudaStream_t stream) {
+                          uint32_t* err, int sm_count, cudaStream_t stream,
+                          const RouterTable* table) {
   RouterArgs a;
   a.T = T;
   a.H = H;
@@ -501,6 +511,7 @@ cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_w, in
   a.topk_w = topk_w;
   a.logits_out = logits_out;
   a.err = err;
+  a.table = table ? *table : RouterTable{nullptr, nullptr, nullptr, 0};
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>(E_pad)) cols <<= 1;
   a.tmem_cols = cols;

@@ -138,3 +138,30 @@ def test_forward_ex_rejects_unknown_flags(L):
     assert L.moe_workspace_size(C.byref(c), N.MOE_OP_FORWARD, C.byref(nb)) == 0
     rc = L.moe_forward_ex(C.byref(c), None, 16, 16, None, 16, None, None, 0x8, ws, nb.value, None)
     assert rc == N.MOE_ERR_INVALID_ARG and b"flags" in L.moe_last_error_message()
+
+
+def test_stack_create_validates(L):
+    """moe_stack_create checks every layer's list before touching the device."""
+    c = cfg()
+    h = C.c_void_p()
+    good = (C.c_void_p * 8)(*([0x1000] * 8))
+    bad = (C.c_void_p * 8)(*([0x1000] * 5 + [0x1001] + [0x1000] * 2))
+    wls = (N.MoeWeightList * 2)()
+    for wl, arr in zip(wls, (good, bad)):
+        wl.gate = wl.up = wl.down = C.cast(arr, C.POINTER(C.c_void_p))
+    routers = (C.c_void_p * 2)(0x2000, 0x2000)
+    assert L.moe_stack_create(C.byref(c), 0, wls, routers, None, C.byref(h)) == N.MOE_ERR_INVALID_ARG
+    assert L.moe_stack_create(C.byref(c), 2, None, routers, None, C.byref(h)) == N.MOE_ERR_INVALID_ARG
+    assert L.moe_stack_create(C.byref(c), 2, wls, routers, None, C.byref(h)) == N.MOE_ERR_INVALID_ARG
+    assert b"gate[5]" in L.moe_last_error_message()      # layer 1's bad pointer
+    assert h.value is None
+
+
+def test_forward_stack_validates(L):
+    c = cfg()
+    nb = C.c_size_t()
+    assert L.moe_workspace_size(C.byref(c), N.MOE_OP_FORWARD, C.byref(nb)) == 0
+    ws = 0x10000
+    assert L.moe_forward_stack(C.byref(c), None, 16, 16, 16, None, None, ws, nb.value,
+                               None) == N.MOE_ERR_INVALID_ARG
+    assert b"stack" in L.moe_last_error_message()
