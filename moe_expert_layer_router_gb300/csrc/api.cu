@@ -707,7 +707,9 @@ static moe_status_t run_ffn_fp8(const moe_config_t& c, const WeightView& W, cons
   uint8_t* hs = at<uint8_t*>(ws, L.hs);
   float* h_sc = at<float*>(ws, L.h_sc);
   float* hs_sc = at<float*>(ws, L.hs_sc);
-  const int n1r = c.I / kFp8WRows, n1s = c.I_shared / kFp8WRows, n2 = c.H / kFp8WRows;
+  // GEMM1 tiles: 128 intermediate columns (gate + up); GEMM2 tiles: 256 output columns
+  const int n1r = c.I / kFp8WRows, n1s = c.I_shared / kFp8WRows;
+  const int n2 = (c.H + 2 * kFp8WRows - 1) / (2 * kFp8WRows);
   trace_mark(st, MOE_K_PLAN);
   MOE_CUDA(launch_plan(offsets, c.E, shared ? 1 : 0, c.T, n1r, n1s, n2, n2, s1, s2,
                        kFp8Tile1Tokens, kFp8Tile2Tokens, st));

@@ -45,18 +45,21 @@ constexpr int kTokBox = 32;                 // token rows per TMA box
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxKB = kFp8MaxKBlocks;      // K blocks per row (H or I up to 8192)
 
-// GEMM1: 64-token tiles (two boxes), 5 stages of 40 KB.  GEMM2: 32-token
-// tiles (one box), 10 stages of 20 KB, so 160 KB of weights are in flight per
-// SM against HBM latency.
+// Every tile holds two 128-row weight blocks: GEMM1 the gate and the up rows
+// of 128 intermediate columns, GEMM2 two consecutive 128-row blocks of W_down
+// (256 output columns).  A stage is both blocks' 128-byte K slice plus the
+// tokens'.  GEMM1: 64-token tiles, 5 stages of 40 KB.  GEMM2: 32-token tiles,
+// 6 stages of 36 KB (192 KB of weights in flight per SM against HBM latency).
 template <bool kGateUp>
 struct Cfg {
   static constexpr int kTok = kGateUp ? kFp8Tile1Tokens : kFp8Tile2Tokens;  // tokens per tile
   static constexpr int kTokBytes = kTok * kKB;                               // token region per stage
-  static constexpr int kStages = kGateUp ? 5 : 10;
-  static constexpr int kStageBytes = (kGateUp ? 2 : 1) * kWBytes + kTokBytes;
-  static constexpr int kBufCols = (kGateUp ? 2 : 1) * 64;   // TMEM columns per partial
-  static constexpr int kBufs = kTmemCols / kBufCols;        // 4 or 8
+  static constexpr int kStages = kGateUp ? 5 : 6;
+  static constexpr int kStageBytes = 2 * kWBytes + kTokBytes;
+  static constexpr int kBufCols = 128;                      // TMEM columns per partial
+  static constexpr int kBufs = kTmemCols / kBufCols;        // 4
 };
+constexpr int kBlk1Col = 64;  // TMEM column of the second block's partial
 
 template <bool kGateUp>
 struct __align__(8) SmemCtl {
@@ -141,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   SmemCtl<kGateUp>& c = *reinterpret_cast<SmemCtl<kGateUp>*>(smem + C::kStages * C::kStageBytes);
   auto stage_w = [&](int s, int which) { return smem + s * C::kStageBytes + which * kWBytes; };
-  auto stage_t = [&](int s) { return smem + s * C::kStageBytes + (kGateUp ? 2 : 1) * kWBytes; };
+  auto stage_t = [&](int s) { return smem + s * C::kStageBytes + 2 * kWBytes; };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -188,9 +191,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n_tok = left < C::kTok ? left : C::kTok;
         const int n_box = (n_tok + kTokBox - 1) / kTokBox;
         const int tok_row = x.row0 + x.tok_blk * C::kTok;
-        const CUtensorMap* mw = kGateUp ? wmaps + 2 * x.g : wmaps + x.g;
-        const int w_row = x.w_blk * kWRows;
-        const uint32_t bytes = (kGateUp ? 2 : 1) * kWBytes + n_box * kTokBox * kKB;
+        // the two weight blocks: gate and up rows of the same 128 columns
+        // (GEMM1), or W_down rows [256 w, +128) and [256 w + 128, +128) (GEMM2;
+        // past H the second box is zero-filled)
+        const CUtensorMap* mw0 = kGateUp ? wmaps + 2 * x.g : wmaps + x.g;
+        const CUtensorMap* mw1 = kGateUp ? mw0 + 1 : mw0;
+        const int w_row0 = x.w_blk * (kGateUp ? kWRows : 2 * kWRows);
+        const int w_row1 = kGateUp ? w_row0 : w_row0 + kWRows;
+        const uint32_t bytes = 2 * kWBytes + n_box * kTokBox * kKB;
         const int kb_n = x.K / kKB;
         bool ok = true;
         const int rot = t % kb_n;
@@ -200,8 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kbe = kb + rot < kb_n ? kb + rot : kb + rot - kb_n;
           if (!ptx::mbar_wait(&c.empty[s], ph ^ 1, abort, args.err)) { ok = false; break; }
           ptx::mbar_arrive_expect_tx(&c.full[s], bytes);
-          ptx::tma_load_2d(stage_w(s, 0), mw, &c.full[s], kbe * kKB, w_row);
-          if (kGateUp) ptx::tma_load_2d(stage_w(s, 1), mw + 1, &c.full[s], kbe * kKB, w_row);
+          ptx::tma_load_2d(stage_w(s, 0), mw0, &c.full[s], kbe * kKB, w_row0);
+          ptx::tma_load_2d(stage_w(s, 1), mw1, &c.full[s], kbe * kKB, w_row1);
           for (int bx = 0; bx < n_box; ++bx)
             ptx::tma_load_2d(stage_t(s) + bx * kTokBox * kKB, map_t, &c.full[s], kbe * kKB,
                              tok_row + bx * kTokBox);
@@ -237,11 +245,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t dt = ptx::sw128_desc(ptx::smem_u32(stage_t(s)));
           const uint32_t d0 = tmem_base + b * C::kBufCols;
 #pragma unroll
-          for (int w = 0; w < (kGateUp ? 2 : 1); ++w) {
+          for (int w = 0; w < 2; ++w) {
             const uint64_t dw = ptx::sw128_desc(ptx::smem_u32(stage_w(s, w)));
 #pragma unroll
             for (int k = 0; k < kKB / 32; ++k)
-              ptx::mma_f8(d0 + w * 64, dw + 2 * k, dt + 2 * k, idesc, k != 0);  // up partial at +64
+              ptx::mma_f8(d0 + w * kBlk1Col, dw + 2 * k, dt + 2 * k, idesc, k != 0);
           }
           ptx::mma_commit(&c.empty[s]);
           ptx::mma_commit(&c.pfull[b]);
@@ -272,13 +280,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         c.tok_scale[j * kMaxKB + kb] = __ldg(ts + int64_t(tok_row + j) * kb_n + kb);
       }
       epi_sync();
-      const float* ws0 = wscales[kGateUp ? 2 * x.g : x.g] + int64_t(x.w_blk) * kb_n;
-      const float* ws1 = kGateUp ? wscales[2 * x.g + 1] + int64_t(x.w_blk) * kb_n : ws0;
-      float acc0[C::kTok], acc1[kGateUp ? C::kTok : 1];
+      // block scales of the tile's two weight blocks (GEMM2: row blocks 2w and
+      // 2w+1 of W_down; the second exists only while 256 w + 128 < H)
+      const bool blk1 = kGateUp || (2 * x.w_blk + 1) * kWRows < args.N_routed;
+      const float* ws0 = wscales[kGateUp ? 2 * x.g : x.g] +
+                         int64_t(kGateUp ? x.w_blk : 2 * x.w_blk) * kb_n;
+      const float* ws1 = kGateUp ? wscales[2 * x.g + 1] + int64_t(x.w_blk) * kb_n
+                                 : (blk1 ? ws0 + kb_n : ws0);
+      float acc0[C::kTok], acc1[C::kTok];
 #pragma unroll
-      for (int j = 0; j < C::kTok; ++j) acc0[j] = 0.0f;
-#pragma unroll
-      for (int j = 0; j < (kGateUp ? C::kTok : 1); ++j) acc1[j] = 0.0f;
+      for (int j = 0; j < C::kTok; ++j) {
+        acc0[j] = 0.0f;
+        acc1[j] = 0.0f;
+      }
       bool ok = true;
       const int rot = t % kb_n;
       for (int kb = 0; kb < kb_n; ++kb, ++pb) {
@@ -288,30 +302,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ptx::mbar_wait(&c.pfull[b], bph, abort, args.err)) { ok = false; break; }
         ptx::tc_fence_after();
         const float sw0 = __ldg(ws0 + kbe);
-        const float sw1 = kGateUp ? __ldg(ws1 + kbe) : 0.0f;
+        const float sw1 = __ldg(ws1 + kbe);
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * C::kBufCols;
 #pragma unroll
         for (int half = 0; half < C::kTok / 32; ++half) {
           if (half * 32 < n_tok) {  // warp-uniform
-            uint32_t p0[32];
+            uint32_t p0[32], p1[32];
             ptx::tmem_ld32(taddr + half * 32, p0);
-            if constexpr (kGateUp) {
-              uint32_t p1[32];
-              ptx::tmem_ld32(taddr + 64 + half * 32, p1);
-              ptx::tmem_ld_wait();
+            ptx::tmem_ld32(taddr + kBlk1Col + half * 32, p1);
+            ptx::tmem_ld_wait();
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const float sx = c.tok_scale[(half * 32 + j) * kMaxKB + kbe];
-                acc0[half * 32 + j] += __uint_as_float(p0[j]) * (sw0 * sx);
-                acc1[half * 32 + j] += __uint_as_float(p1[j]) * (sw1 * sx);
-              }
-            } else {
-              ptx::tmem_ld_wait();
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const float sx = c.tok_scale[(half * 32 + j) * kMaxKB + kbe];
-                acc0[half * 32 + j] += __uint_as_float(p0[j]) * (sw0 * sx);
-              }
+            for (int j = 0; j < 32; ++j) {
+              const float sx = c.tok_scale[(half * 32 + j) * kMaxKB + kbe];
+              acc0[half * 32 + j] += __uint_as_float(p0[j]) * (sw0 * sx);
+              acc1[half * 32 + j] += __uint_as_float(p1[j]) * (sw1 * sx);
             }
           }
         }
@@ -350,13 +354,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         float* y = static_cast<float*>(routed ? args.out0 : args.out1);
         const int n_o = args.N_routed;  // H for both groups
-        const int col = x.w_blk * kWRows + r;
+        const int col = x.w_blk * 2 * kWRows + r;  // block 0; block 1 is 128 columns on
 #pragma unroll
         for (int j = 0; j < C::kTok; ++j) {
           if (j < n_tok) {
             const int64_t row = tok_row + j;
             const float w = (routed && args.row_weight) ? __ldg(args.row_weight + row) : 1.0f;
             y[row * n_o + col] = w * acc0[j];
+            if (blk1) y[row * n_o + col + kWRows] = w * acc1[j];
           }
         }
       }

@@ -63,7 +63,8 @@ def test_forward_empty_batch_is_a_noop():
     assert m.moe_get_device_error(ws) == 0
 
 
-FULL = [(wl.QWEN3, False), (wl.DSV3, False), (wl.DSV3_SKEW, False), (wl.DSV3, True)]
+FULL = [(wl.QWEN3, False), (wl.DSV3, False), (wl.DSV3_SKEW, False), (wl.DSV3, True),
+        (wl.DSV3_T512, False)]
 
 
 @pytest.mark.parametrize("lc,fused", FULL,

@@ -71,6 +71,8 @@ class Fp8Layer:
     wl.DSV3_FP8.with_(name="fp8_small", T=96, H=512, E=8, k=2, I=384, I_shared=256),
     wl.DSV3_FP8.with_(name="fp8_ragged", T=150, H=1024, E=4, k=2, I=256, I_shared=0,
                       score="softmax", route_scale=1.0),
+    # H = 3 x 128: GEMM2's last 256-column tile has only its first weight block
+    wl.DSV3_FP8.with_(name="fp8_h384", T=80, H=384, E=4, k=2, I=256, I_shared=128),
 ], ids=lambda c: c.name)
 def test_fp8_grouped_ffn_matches_oracle(lc):
     dev = torch.device("cuda")

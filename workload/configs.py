@@ -80,13 +80,18 @@ DSV3 = LayerConfig("dsv3", T=16384, H=7168, E=256, k=8, I=2048, I_shared=2048,
 DSV3_SKEW = DSV3.with_(name="dsv3_skewed", T=sum(skewed_lengths(0)), zipf_bias=True)
 DSV3_FP8 = DSV3.with_(name="dsv3_fp8", T=512, wtype="fp8_e4m3")
 
+# DeepSeek-V3 layer in bf16 at a small batch (16 rows per expert): the
+# memory-bound regime of the grouped GEMMs, a parity and bench case.
+DSV3_T512 = DSV3.with_(name="dsv3_bf16_t512", T=512)
+
 # Profiling slice: DeepSeek-V3 expert shapes and rows per expert (T*k/E = 512), a
 # quarter of the experts and tokens, so that one ncu capture holds a few GB.
 DSV3_SLICE = DSV3.with_(name="dsv3_slice", T=4096, E=64)
 # fp8 profiling slice: 16 tokens per expert as in the 512-token fp8 batch, 1/4 of the experts
 DSV3_FP8_SLICE = DSV3_FP8.with_(name="dsv3_fp8_slice", T=128, E=64)
 
-CONFIGS = {c.name: c for c in (TINY, QWEN3, DSV3, DSV3_SKEW, DSV3_FP8, DSV3_SLICE, DSV3_FP8_SLICE)}
+CONFIGS = {c.name: c for c in (TINY, QWEN3, DSV3, DSV3_SKEW, DSV3_FP8, DSV3_T512, DSV3_SLICE,
+                                DSV3_FP8_SLICE)}
 
 
 # ---------------------------------------------------------------- tensors
