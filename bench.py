@@ -321,7 +321,7 @@ def run_ours(args, lc, rank, world, dev):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize(dev)
-    N.check(N.lib().moe_set_trace(N.C.byref(trace)), "moe_set_trace")
+    # the timed steps run with no trace hook: the value is the plain calls
     w0 = time.time()
     start.record(stream)
     for _ in range(args.steps):
@@ -329,9 +329,16 @@ def run_ours(args, lc, rank, world, dev):
     end.record(stream)
     torch.cuda.synchronize(dev)
     w1 = time.time()
-    N.lib().moe_set_trace(None)
     barrier()
     ms_local = start.elapsed_time(end) / args.steps
+    m.moe_get_device_error(ws)
+    # the same steps again with the trace hook: per-kernel durations and the
+    # number of kernels each step launches
+    N.check(N.lib().moe_set_trace(N.C.byref(trace)), "moe_set_trace")
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize(dev)
+    N.lib().moe_set_trace(None)
     m.moe_get_device_error(ws)
 
     # per-kernel durations from the trace
