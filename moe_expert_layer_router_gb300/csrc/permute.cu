@@ -192,10 +192,12 @@ __global__ void __launch_bounds__(kScatterThreads)
     for (int tl = warp; tl < nt; tl += nwarps) {
       const uint4* s4 = reinterpret_cast<const uint4*>(x + (t0 + tl) * int64_t(H));
       const int32_t* rr = rows_s + tl * k;
-      for (int c0 = c_lo; c0 < c_hi; c0 += 32 * 4) {
-        uint4 v[4];
+      // 8 x 16 bytes per lane in flight: enough outstanding reads per SM to
+      // cover HBM latency with the 8 KB-per-warp write burst behind them
+      for (int c0 = c_lo; c0 < c_hi; c0 += 32 * 8) {
+        uint4 v[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 8; ++u) {
           const int cc = c0 + u * 32 + lane;
           if (cc < c_hi) v[u] = __ldcs(s4 + cc);
         }
@@ -204,7 +206,7 @@ __global__ void __launch_bounds__(kScatterThreads)
           if (row < 0) continue;
           uint4* d4 = dst + int64_t(row) * nch;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
+          for (int u = 0; u < 8; ++u) {
             const int cc = c0 + u * 32 + lane;
             if (cc < c_hi) d4[cc] = v[u];
           }
