@@ -32,6 +32,7 @@ SMALL = [
     wl.DSV3.with_(name="dsv3_shape_T64", T=64, E=32, k=4, I=256, I_shared=256),
     wl.TINY.with_(name="skewish", T=700, E=16, k=3, H=384, I=128, zipf_bias=False),
     wl.TINY.with_(name="one_token_k1", T=1, k=1),
+    wl.TINY.with_(name="e40_k5", T=300, E=40, k=5, H=512, I=256, I_shared=128),
 ]
 
 

@@ -22,6 +22,7 @@ CASES = [
     wl.TINY.with_(name="k1", E=32, k=1, T=130, score="sigmoid", renormalize=False),
     wl.TINY.with_(name="softmax_full", E=64, k=6, T=200, renormalize=False),
     wl.TINY.with_(name="k16", E=48, k=16, T=140, H=256),
+    wl.TINY.with_(name="e40", E=40, k=5, T=300, H=512),                   # E_pad = 48: 8 padded columns
 ]
 
 
