@@ -8,7 +8,9 @@ kernels, helpers, tables or constants.  Only the seeded input generators in
 
 Plain, slow and single-threaded in spirit: numpy float64, one step per
 function, in the order the layer is defined.  See ``moe.py`` for the bf16
-layer and ``fp8.py`` for the e4m3 codec and block quantisation.
+layer, ``fp8.py`` for the e4m3 codec and block quantisation, and
+``nvfp4.py`` for the E2M1 codec, NVFP4 two-level block quantisation and the
+NVFP4 layer.
 
 Sources (page title, section):
   * ASAP: A DiSaggregated and Asynchronous Inference System for MoE Prefill,
@@ -24,15 +26,17 @@ Sources (page title, section):
     Analysis and Performance Validation, section 3, "Data-Flow Closed Loop"
     step 3 (FFN side: gated routing + expert computation).
 The pages do not fix the scoring rule, SwiGLU, the routed scale, tie-breaks,
-the permutation order or the fp8 scale convention; those readings are stated
-where they are used.
+the permutation order, the fp8 scale convention or how NVFP4 activations
+are scaled; those readings are stated where they are used.
 
 Parity status: every function here is pinned by the CPU tests in
 ``tests/test_oracle_*.py`` (closed forms, invariants, brute force, hand-worked
 fixtures under ``tests/golden/`` and library routines).  The fp8 scale
-convention (amax/448 in fp32) is the one reading that nothing on the pages
-pins: "parity unpinned" beyond self-consistency and the OCP e4m3 codec.
+convention (amax/448 in fp32) and the NVFP4 tensor scales (amax/2688 for
+weights, static per-layer scales for activations) are the readings that
+nothing on the pages pins: "parity unpinned" beyond self-consistency and the
+published codecs (OCP e4m3, OCP MX E2M1).
 """
-from . import fp8, moe
+from . import fp8, moe, nvfp4
 
-__all__ = ["moe", "fp8"]
+__all__ = ["moe", "fp8", "nvfp4"]
