@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define MOE_API __attribute__((visibility("default")))
@@ -78,8 +78,13 @@ typedef enum moe_score {
 
 typedef enum moe_dtype {
   MOE_DTYPE_BF16 = 0,         /* bf16 weights, bf16 x_perm / h, fp32 accumulation */
-  MOE_DTYPE_FP8_E4M3 = 1      /* e4m3 weights with 128x128 fp32 block scales;
+  MOE_DTYPE_FP8_E4M3 = 1,     /* e4m3 weights with 128x128 fp32 block scales;
                                  e4m3 activations with 1x128 fp32 group scales */
+  MOE_DTYPE_NVFP4 = 2         /* NVFP4 weights and activations: E2M1 values, one
+                                 e4m3 scale per 16 elements along K, an fp32 tensor
+                                 scale per matrix (weights) or per layer (static
+                                 activation scales); block-scaled fp4 tensor cores.
+                                 Runs through moe_forward / moe_forward_stack only. */
 } moe_dtype_t;
 
 typedef enum moe_op {
@@ -92,11 +97,12 @@ typedef enum moe_op {
 
 /* Layer shape and routing rule.
  *   T          tokens (>= 0; 0 makes every call a no-op); T*k < 2^31
- *   H          hidden size, multiple of 128, >= 128
+ *   H          hidden size, multiple of 128 (of 256 for NVFP4), >= 128
  *   E          routed experts, 1..256
  *   k          experts per token, 1..min(E, 16)
- *   I          routed expert intermediate size, multiple of 128
+ *   I          routed expert intermediate size, multiple of 128 (256 for NVFP4)
  *   I_shared   shared expert intermediate size, 0 (none) or multiple of 128
+ *              (256 for NVFP4)
  *   score      moe_score_t
  *   renormalize 1: normalise the k selected weights to sum 1; 0: softmax over
  *              all E (softmax) or the raw sigmoid (sigmoid)
@@ -123,7 +129,22 @@ typedef struct moe_config {
  *   *_scales[e]     fp8 only: fp32 block scales, gate/up [I/128, H/128],
  *                   down [H/128, I/128]; NULL arrays for bf16
  *   shared_*        the shared expert ([I_shared, H] / [H, I_shared]) and its
- *                   scales; NULL when I_shared == 0 */
+ *                   scales; NULL when I_shared == 0
+ * NVFP4 (MOE_DTYPE_NVFP4), as written by moe_quantize_weight_nvfp4:
+ *   gate[e]         the expert's stacked gate/up matrix, E2M1 codes [2I, H/2]
+ *                   bytes (two values per byte, the even element in the low
+ *                   nibble), rows interleaved in 64-row blocks [gate 64 | up 64];
+ *                   up[] and the *_scales arrays are unused (may be NULL)
+ *   down[e]         E2M1 codes [H, I/2]
+ *   gate_sf[e], down_sf[e]   their e4m3 block scales in the MMA scale layout
+ *                   (see moe_quantize_weight_nvfp4), 16-byte aligned
+ *   gate_tscale[e], down_tscale[e]   device pointers to the fp32 tensor scales
+ *   shared_gate / shared_down / shared_gate_sf / shared_down_sf /
+ *   shared_gate_tscale / shared_down_tscale   the shared expert's, alike
+ *   input_scale     static fp32 tensor scale g_x of the expert inputs, > 0
+ *   hidden_scale    static fp32 tensor scale g_h of the intermediate h, > 0
+ *   (NVFP4 checkpoints carry such static activation scales; every activation
+ *   block scale is computed at run time from them.) */
 typedef struct moe_weight_list {
   const void* const* gate;
   const void* const* up;
@@ -137,6 +158,16 @@ typedef struct moe_weight_list {
   const float* shared_gate_scales;
   const float* shared_up_scales;
   const float* shared_down_scales;
+  const void* const* gate_sf;
+  const void* const* down_sf;
+  const float* const* gate_tscale;
+  const float* const* down_tscale;
+  const void* shared_gate_sf;
+  const void* shared_down_sf;
+  const float* shared_gate_tscale;
+  const float* shared_down_tscale;
+  float input_scale;
+  float hidden_scale;
 } moe_weight_list_t;
 
 typedef struct moe_weights* moe_weights_t;
@@ -317,6 +348,33 @@ MOE_API moe_status_t moe_quantize_weight_fp8(const float* w, int64_t N, int64_t 
  * 1x128 groups: scales[M, K/128], codes q[M, K], same rule as above. */
 MOE_API moe_status_t moe_quantize_act_fp8(const void* x, int64_t M, int64_t K, uint8_t* q, float* scales,
                                   moe_stream_t stream);
+
+/* NVFP4 weight preparation (MoE weights in NVFP4: "DWDP: Distributed Weight
+ * Data Parallelism for High-Performance LLM Inference on NVL72", section A4,
+ * experimental setup).  w: bf16 [N, K]; w2: NULL, or a second bf16 [N, K]
+ * matrix stacked with w (an expert's up projection next to its gate), in
+ * which case the output has 2N rows interleaved in 64-row blocks
+ * [w rows 64b..64b+63 | w2 rows 64b..64b+63].  Computed in fp32:
+ *   g = amax / (6 * 448) over the whole (stacked) matrix (1 if all zero),
+ *   per 16 consecutive elements of a row: s = e4m3_rn_satfinite(amax_b / (6 g)),
+ *   q = E2M1 round-to-nearest-even, saturating at 6, of x / (s g)  (q = 0 if s g = 0).
+ *   codes       [rows, K/2] bytes, element 2i in the low nibble of byte i
+ *   sf          rows * K/16 bytes: the e4m3 codes of s in the MMA scale layout:
+ *               512-byte atoms of 128 rows x 4 blocks; the scale of (row r,
+ *               block b) is byte ((r/128) * (K/64) + b/4) * 512 + (r%32) * 16
+ *               + ((r%128)/32) * 4 + b%4
+ *   tensor_scale  device fp32, receives g
+ * N a multiple of 128 (of 64 with w2), K of 64.  Asynchronous; tensor_scale is
+ * used as scratch until the call's last kernel has run. */
+MOE_API moe_status_t moe_quantize_weight_nvfp4(const void* w, const void* w2, int64_t N, int64_t K,
+                                               uint8_t* codes, uint8_t* sf, float* tensor_scale,
+                                               moe_stream_t stream);
+
+/* NVFP4 activation quantisation with a static tensor scale g (> 0) of a bf16
+ * [M, K] matrix (K a multiple of 16), the same block rule: codes [M, K/2],
+ * sf [M, K/16] e4m3 scale codes, row-major. */
+MOE_API moe_status_t moe_quantize_act_nvfp4(const void* x, int64_t M, int64_t K, float g,
+                                            uint8_t* codes, uint8_t* sf, moe_stream_t stream);
 
 /* Waits for `stream`, reads the workspace's sticky device status word, clears
  * it and maps it to MOE_OK / MOE_ERR_BOUNDS / MOE_ERR_DEVICE_TIMEOUT.

@@ -24,7 +24,8 @@ __all__ = ["MoeConfig", "MoeError", "make_config", "config_from", "Workspace", "
            "moe_route", "moe_permute", "moe_permute_noalloc", "moe_grouped_ffn", "moe_combine",
            "moe_forward", "LayerStack", "moe_forward_stack",
            "moe_quantize_weight_fp8", "moe_quantize_act_fp8", "moe_get_device_error",
-           "moe_workspace_size", "load"]
+           "moe_workspace_size", "load", "Nvfp4ExpertWeights", "moe_quantize_weight_nvfp4",
+           "moe_quantize_act_nvfp4", "quantize_experts_nvfp4"]
 
 _OPS = {"route": N.MOE_OP_ROUTE, "permute": N.MOE_OP_PERMUTE, "grouped_ffn": N.MOE_OP_GROUPED_FFN,
         "combine": N.MOE_OP_COMBINE, "forward": N.MOE_OP_FORWARD}
@@ -40,7 +41,8 @@ def make_config(T, H, E, k, I, I_shared=0, score="softmax", renormalize=True, ro
     return MoeConfig(int(T), int(H), int(E), int(k), int(I), int(I_shared),
                      {"softmax": N.MOE_SCORE_SOFTMAX, "sigmoid": N.MOE_SCORE_SIGMOID}[score],
                      1 if renormalize else 0, float(route_scale),
-                     {"bf16": N.MOE_DTYPE_BF16, "fp8_e4m3": N.MOE_DTYPE_FP8_E4M3}[wtype])
+                     {"bf16": N.MOE_DTYPE_BF16, "fp8_e4m3": N.MOE_DTYPE_FP8_E4M3,
+                      "nvfp4": N.MOE_DTYPE_NVFP4}[wtype])
 
 
 def config_from(layer, T: int | None = None) -> MoeConfig:
@@ -148,6 +150,75 @@ class ExpertWeights:
             wl.shared_gate_scales, wl.shared_up_scales, wl.shared_down_scales = (
                 s.data_ptr() for s in shared_scales)
         self.cfg = cfg
+        self._wl = wl
+        h = C.c_void_p()
+        N.check(N.lib().moe_weights_create(C.byref(cfg), C.byref(wl), C.byref(h)),
+                "moe_weights_create")
+        self.handle = h.value
+
+    def close(self):
+        if getattr(self, "handle", None):
+            N.lib().moe_weights_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Nvfp4ExpertWeights:
+    """NVFP4 expert weights (MOE_DTYPE_NVFP4) -> device descriptor table.
+
+    Per expert e: ``gate_up[e]`` uint8 [2I, H/2] (stacked gate/up E2M1 codes,
+    rows interleaved in 64-row blocks), ``down[e]`` uint8 [H, I/2], their
+    MMA-layout block scales ``gate_up_sf[e]`` / ``down_sf[e]`` (uint8, rows*K/16
+    bytes) and fp32 tensor scales ``gate_up_ts`` / ``down_ts`` (device float32
+    tensors [E]: entry e is expert e's).  ``shared`` = (gate_up, down,
+    gate_up_sf, down_sf, tensor scales [2]) or None.  ``input_scale`` and
+    ``hidden_scale`` are the static activation tensor scales g_x, g_h.  The
+    tensors are referenced, not copied; this object keeps them alive."""
+
+    def __init__(self, cfg: MoeConfig, gate_up, down, gate_up_sf, down_sf, gate_up_ts, down_ts,
+                 input_scale, hidden_scale, shared=None):
+        E, H, I = cfg.E, cfg.H, cfg.I
+        if not (len(gate_up) == len(down) == len(gate_up_sf) == len(down_sf) == E):
+            raise ValueError("gate_up/down and their scales must each list E tensors")
+        for e in range(E):
+            _need(gate_up[e], f"gate_up[{e}]", torch.uint8, (2 * I, H // 2), None)
+            _need(down[e], f"down[{e}]", torch.uint8, (H, I // 2), None)
+            _need(gate_up_sf[e], f"gate_up_sf[{e}]", torch.uint8, (2 * I * H // 16,), None)
+            _need(down_sf[e], f"down_sf[{e}]", torch.uint8, (H * I // 16,), None)
+        _need(gate_up_ts, "gate_up_ts", torch.float32, (E,), None)
+        _need(down_ts, "down_ts", torch.float32, (E,), None)
+        self._keep = [list(gate_up), list(down), list(gate_up_sf), list(down_sf), gate_up_ts,
+                      down_ts, shared]
+        ts = lambda t: (C.c_void_p * E)(*[t.data_ptr() + 4 * e for e in range(E)])
+        self._arrays = [_ptr_array(gate_up), _ptr_array(down), _ptr_array(gate_up_sf),
+                        _ptr_array(down_sf), ts(gate_up_ts), ts(down_ts)]
+        wl = N.MoeWeightList()
+        P = C.POINTER(C.c_void_p)
+        wl.gate = C.cast(self._arrays[0], P)
+        wl.down = C.cast(self._arrays[1], P)
+        wl.gate_sf = C.cast(self._arrays[2], P)
+        wl.down_sf = C.cast(self._arrays[3], P)
+        wl.gate_tscale = C.cast(self._arrays[4], P)
+        wl.down_tscale = C.cast(self._arrays[5], P)
+        wl.input_scale = float(input_scale)
+        wl.hidden_scale = float(hidden_scale)
+        if shared is not None:
+            sgu, sd, sgu_sf, sd_sf, sts = shared
+            Is = cfg.I_shared
+            _need(sgu, "shared gate_up", torch.uint8, (2 * Is, H // 2), None)
+            _need(sd, "shared down", torch.uint8, (H, Is // 2), None)
+            _need(sts, "shared tensor scales", torch.float32, (2,), None)
+            wl.shared_gate, wl.shared_down = sgu.data_ptr(), sd.data_ptr()
+            wl.shared_gate_sf, wl.shared_down_sf = sgu_sf.data_ptr(), sd_sf.data_ptr()
+            wl.shared_gate_tscale, wl.shared_down_tscale = sts.data_ptr(), sts.data_ptr() + 4
+        self.cfg = cfg
+        self.input_scale = float(input_scale)
+        self.hidden_scale = float(hidden_scale)
         self._wl = wl
         h = C.c_void_p()
         N.check(N.lib().moe_weights_create(C.byref(cfg), C.byref(wl), C.byref(h)),
@@ -405,3 +476,64 @@ def moe_quantize_act_fp8(x, stream=None):
     N.check(N.lib().moe_quantize_act_fp8(_ptr(x), M, K, _ptr(q), _ptr(s), _stream(stream)),
             "moe_quantize_act_fp8")
     return q, s
+
+
+def moe_quantize_weight_nvfp4(w, w2=None, tensor_scale=None, stream=None):
+    """NVFP4 weights (moe_quantize_weight_nvfp4): bf16 [N, K] (w2: a second
+    [N, K] matrix stacked with w, rows interleaved in 64-row blocks) ->
+    (codes uint8 [rows, K/2], MMA-layout scales uint8 [rows*K/16], tensor scale
+    float32 [1], or written into ``tensor_scale`` (a float32 view of one element))."""
+    Nr, K = w.shape
+    _need(w, "w", torch.bfloat16, (Nr, K), None)
+    if w2 is not None:
+        _need(w2, "w2", torch.bfloat16, (Nr, K), w.device)
+    rows = 2 * Nr if w2 is not None else Nr
+    codes = torch.empty(rows, K // 2, dtype=torch.uint8, device=w.device)
+    sf = torch.empty(rows * K // 16, dtype=torch.uint8, device=w.device)
+    ts = tensor_scale if tensor_scale is not None else torch.empty(1, dtype=torch.float32,
+                                                                    device=w.device)
+    N.check(N.lib().moe_quantize_weight_nvfp4(w.data_ptr(), _ptr(w2), Nr, K, codes.data_ptr(),
+                                              sf.data_ptr(), ts.data_ptr(), _stream(stream)),
+            "moe_quantize_weight_nvfp4")
+    return codes, sf, ts
+
+
+def moe_quantize_act_nvfp4(x, g, stream=None):
+    """bf16 [M, K] -> (codes uint8 [M, K/2], e4m3 scale codes uint8 [M, K/16]) with
+    the static tensor scale g."""
+    M, K = x.shape
+    _need(x, "x", torch.bfloat16, (M, K), None)
+    codes = torch.empty(M, K // 2, dtype=torch.uint8, device=x.device)
+    sf = torch.empty(M, K // 16, dtype=torch.uint8, device=x.device)
+    N.check(N.lib().moe_quantize_act_nvfp4(x.data_ptr(), M, K, float(g), codes.data_ptr(),
+                                           sf.data_ptr(), _stream(stream)),
+            "moe_quantize_act_nvfp4")
+    return codes, sf
+
+
+def quantize_experts_nvfp4(cfg: MoeConfig, gate, up, down, shared=None, *, input_scale,
+                           hidden_scale, stream=None) -> Nvfp4ExpertWeights:
+    """Quantise bf16 expert weights (lists of [I, H] gate/up and [H, I] down
+    tensors, and the shared expert's triple) to NVFP4 on the GPU and build the
+    layer's weight table.  The quantised tensors are owned by the result."""
+    E = cfg.E
+    dev = gate[0].device
+    gu_ts = torch.empty(E, dtype=torch.float32, device=dev)
+    d_ts = torch.empty(E, dtype=torch.float32, device=dev)
+    gu, dn, gu_sf, dn_sf = [], [], [], []
+    for e in range(E):
+        c, s, _ = moe_quantize_weight_nvfp4(gate[e], up[e], gu_ts[e:e + 1], stream)
+        gu.append(c)
+        gu_sf.append(s)
+        c, s, _ = moe_quantize_weight_nvfp4(down[e], None, d_ts[e:e + 1], stream)
+        dn.append(c)
+        dn_sf.append(s)
+    sh = None
+    if shared is not None:
+        sg, su, sd = shared
+        sts = torch.empty(2, dtype=torch.float32, device=dev)
+        c1, s1, _ = moe_quantize_weight_nvfp4(sg, su, sts[0:1], stream)
+        c2, s2, _ = moe_quantize_weight_nvfp4(sd, None, sts[1:2], stream)
+        sh = (c1, c2, s1, s2, sts)
+    return Nvfp4ExpertWeights(cfg, gu, dn, gu_sf, dn_sf, gu_ts, d_ts, input_scale, hidden_scale,
+                              shared=sh)

@@ -16,7 +16,7 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "moe_layer.h")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, \
     MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_BOUNDS = range(7)
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
-MOE_DTYPE_BF16, MOE_DTYPE_FP8_E4M3 = 0, 1
+MOE_DTYPE_BF16, MOE_DTYPE_FP8_E4M3, MOE_DTYPE_NVFP4 = 0, 1, 2
 MOE_OP_ROUTE, MOE_OP_PERMUTE, MOE_OP_GROUPED_FFN, MOE_OP_COMBINE, MOE_OP_FORWARD = range(5)
 MOE_FORWARD_FUSED_DISPATCH = 0x1
 
@@ -33,7 +33,12 @@ class MoeWeightList(C.Structure):
                 ("up_scales", C.POINTER(C.c_void_p)), ("down_scales", C.POINTER(C.c_void_p)),
                 ("shared_gate", C.c_void_p), ("shared_up", C.c_void_p),
                 ("shared_down", C.c_void_p), ("shared_gate_scales", C.c_void_p),
-                ("shared_up_scales", C.c_void_p), ("shared_down_scales", C.c_void_p)]
+                ("shared_up_scales", C.c_void_p), ("shared_down_scales", C.c_void_p),
+                ("gate_sf", C.POINTER(C.c_void_p)), ("down_sf", C.POINTER(C.c_void_p)),
+                ("gate_tscale", C.POINTER(C.c_void_p)), ("down_tscale", C.POINTER(C.c_void_p)),
+                ("shared_gate_sf", C.c_void_p), ("shared_down_sf", C.c_void_p),
+                ("shared_gate_tscale", C.c_void_p), ("shared_down_tscale", C.c_void_p),
+                ("input_scale", C.c_float), ("hidden_scale", C.c_float)]
 
 
 class MoeTrace(C.Structure):
@@ -67,6 +72,8 @@ _SIG = {
     "moe_forward_ex": (C.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, C.c_uint32, _P, C.c_size_t, _P]),
     "moe_quantize_weight_fp8": (C.c_int, [_P, C.c_int64, C.c_int64, _P, _P, _P]),
     "moe_quantize_act_fp8": (C.c_int, [_P, C.c_int64, C.c_int64, _P, _P, _P]),
+    "moe_quantize_weight_nvfp4": (C.c_int, [_P, _P, C.c_int64, C.c_int64, _P, _P, _P, _P]),
+    "moe_quantize_act_nvfp4": (C.c_int, [_P, C.c_int64, C.c_int64, C.c_float, _P, _P, _P]),
     "moe_set_trace": (C.c_int, [C.POINTER(MoeTrace)]),
     "moe_permute_noalloc": (C.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }

@@ -22,7 +22,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libmoe_gb300.so")
 
 SOURCES = ["api.cu", "router.cu", "permute.cu", "grouped_gemm.cu", "combine.cu", "quant.cu",
-           "permute_noalloc.cu", "grouped_gemm_fp8.cu"]
+           "permute_noalloc.cu", "grouped_gemm_fp8.cu", "grouped_gemm_nvfp4.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler",
          "-fvisibility=hidden", "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

@@ -169,8 +169,10 @@ static moe_status_t check_config(const moe_config_t* c) {
     return fail(MOE_ERR_INVALID_ARG, "renormalize = %d is not 0 or 1", c->renormalize);
   if (!std::isfinite(c->route_scale) || c->route_scale <= 0.0f)
     return fail(MOE_ERR_INVALID_ARG, "route_scale must be finite and > 0");
-  if (c->wtype != MOE_DTYPE_BF16 && c->wtype != MOE_DTYPE_FP8_E4M3)
+  if (c->wtype != MOE_DTYPE_BF16 && c->wtype != MOE_DTYPE_FP8_E4M3 && c->wtype != MOE_DTYPE_NVFP4)
     return fail(MOE_ERR_INVALID_ARG, "wtype = %d is not a moe_dtype_t", c->wtype);
+  if (c->wtype == MOE_DTYPE_NVFP4 && (c->H % 256 || c->I % 256 || c->I_shared % 256))
+    return fail(MOE_ERR_UNSUPPORTED, "NVFP4 layers need H, I and I_shared multiples of 256");
   if (c->T * int64_t(c->k) >= (int64_t(1) << 31))
     return fail(MOE_ERR_UNSUPPORTED, "T*k = %lld does not fit int32 row indices",
                 (long long)(c->T * c->k));
@@ -207,8 +209,18 @@ struct Layout {
   size_t ids = 0, w = 0, counts = 0, offsets = 0, perm_token = 0, inv_row = 0, row_weight = 0,
          x_perm = 0, y_perm = 0, shared_out = 0;  // forward
   size_t x_perm_sc = 0, xq = 0, xq_sc = 0;    // forward, fp8: x_perm scales, quantised x
+  size_t pad_offsets = 0;                     // NVFP4: offsets of the 128-row-padded segments
   size_t total = 0;
 };
+
+// NVFP4 keeps every expert's rows in whole 128-row blocks: at most R + 127 E rows.
+static int64_t nvfp4_rows(const moe_config_t& c) {
+  const int64_t r = c.T * c.k + int64_t(c.E) * (kNvfp4Rows - 1);
+  return (r + kNvfp4Rows - 1) / kNvfp4Rows * kNvfp4Rows;
+}
+static int64_t nvfp4_tokens(const moe_config_t& c) {
+  return (c.T + kNvfp4Rows - 1) / kNvfp4Rows * kNvfp4Rows;
+}
 
 static Layout layout(const moe_config_t& c, int op) {
   Layout L;
@@ -228,7 +240,39 @@ static Layout layout(const moe_config_t& c, int op) {
     L.blk_base = take(size_t(nblk) * c.E * 4);
   }
   const bool fp8 = c.wtype == MOE_DTYPE_FP8_E4M3;
+  const bool fp4 = c.wtype == MOE_DTYPE_NVFP4;
   const size_t esz = fp8 ? 1 : 2;  // bytes per element of x_perm and h
+  if (fp4) {
+    // codes (half a byte per element) and MMA-layout scales (1/16 byte) over
+    // the padded rows; the expert outputs as fp16 + scales in fp32-sized regions
+    const size_t Rp = size_t(nvfp4_rows(c)), Tp = size_t(nvfp4_tokens(c));
+    if (ffn) {
+      L.sched1 = take(size_t(sched_ints(G)) * 4);
+      L.sched2 = take(size_t(sched_ints(G)) * 4);
+      L.h = take(Rp * c.I / 2);
+      L.hs = take(Tp * c.I_shared / 2);
+      L.h_sc = take(Rp * c.I / 16);
+      L.hs_sc = take(Tp * c.I_shared / 16);
+    }
+    if (op == MOE_OP_FORWARD) {
+      L.ids = take(size_t(R) * 4);
+      L.w = take(size_t(R) * 4);
+      L.counts = take(size_t(c.E) * 4);
+      L.offsets = take(size_t(c.E + 1) * 4);
+      L.pad_offsets = take(size_t(c.E + 1) * 4);
+      L.perm_token = take(size_t(R) * 4);
+      L.inv_row = take(size_t(R) * 4);
+      L.row_weight = take(size_t(R) * 4);
+      L.x_perm = take(Rp * c.H / 2);
+      L.x_perm_sc = take(Rp * c.H / 16);
+      L.xq = take(Tp * c.H / 2);
+      L.xq_sc = take(Tp * c.H / 16);
+      L.y_perm = take(size_t(R) * c.H * 4);
+      L.shared_out = take(size_t(T) * c.H * 4);
+    }
+    L.total = at;
+    return L;
+  }
   if (ffn) {
     L.sched1 = take(size_t(sched_ints(G)) * 4);
     L.sched2 = take(size_t(sched_ints(G)) * 4);
@@ -286,8 +330,11 @@ struct moe_weights {
   void* table;          // device: CUtensorMap maps1[2G], maps2[G] (+ fp8: scale pointers)
   CUtensorMap* maps1;
   CUtensorMap* maps2;
-  const float** scales1;  // fp8: gate of group g at 2g, up at 2g+1
+  const float** scales1;  // fp8: gate of group g at 2g, up at 2g+1 (NVFP4: scale bytes)
   const float** scales2;  // fp8: down of group g at g
+  const float** gs1;      // NVFP4: tensor-scale pointers, indexed like scales1
+  const float** gs2;
+  float* act;             // NVFP4: device [2] = g_x, g_h
 };
 
 // Descriptor tables one call reads: a single layer's, or a layer stack's
@@ -298,10 +345,13 @@ struct moe_stack {
   int32_t num_layers;
   int32_t G;
   void* table;              // device: maps [L][3G] | router maps [L] | bias [L] | fp8 scales [L][3G]
+                            //   | NVFP4: tensor scales [L][3G] | activation scales [L][2]
   CUtensorMap* maps;
   CUtensorMap* router;
   const float** bias;
   const float** scales;
+  const float** gs;
+  float* act;
 };
 
 namespace moe {
@@ -313,14 +363,27 @@ struct WeightView {
   const int32_t* layer;
   int32_t stride;
   int32_t num_layers;
+  const float* const* gs1 = nullptr;  // NVFP4 tensor scales
+  const float* const* gs2 = nullptr;
+  const float* act = nullptr;         // NVFP4 [num_layers][2]
 };
 static WeightView view_of(const moe_weights* W) {
-  return WeightView{W->maps1, W->maps2, W->scales1, W->scales2, nullptr, 0, 1};
+  WeightView v{W->maps1, W->maps2, W->scales1, W->scales2, nullptr, 0, 1};
+  v.gs1 = W->gs1;
+  v.gs2 = W->gs2;
+  v.act = W->act;
+  return v;
 }
 static WeightView view_of(const moe_stack* S, const int32_t* layer) {
-  const bool fp8 = S->cfg.wtype == MOE_DTYPE_FP8_E4M3;
-  return WeightView{S->maps, S->maps + 2 * S->G, fp8 ? S->scales : nullptr,
-                    fp8 ? S->scales + 2 * S->G : nullptr, layer, 3 * S->G, S->num_layers};
+  const bool scaled = S->cfg.wtype != MOE_DTYPE_BF16;
+  WeightView v{S->maps, S->maps + 2 * S->G, scaled ? S->scales : nullptr,
+               scaled ? S->scales + 2 * S->G : nullptr, layer, 3 * S->G, S->num_layers};
+  if (S->cfg.wtype == MOE_DTYPE_NVFP4) {
+    v.gs1 = S->gs;
+    v.gs2 = S->gs + 2 * S->G;
+    v.act = S->act;
+  }
+  return v;
 }
 }  // namespace moe
 
@@ -385,8 +448,14 @@ moe_status_t moe_get_device_error(void* ws, moe_stream_t stream, int32_t* device
 // Validates one layer's weight list and encodes its 3G TMA descriptors
 // (GEMM1: gate / up of group g at 2g / 2g+1; GEMM2: down of group g at 2G+g)
 // and, for fp8, the matching scale pointers, into maps[3G] / scales[3G].
+static moe_status_t encode_layer_nvfp4(const moe_config_t* cfg, const moe_weight_list_t* wl,
+                                       CUtensorMap* maps, const float** scales, const float** gs,
+                                       float* act, bool encode);
+
 static moe_status_t encode_layer(const moe_config_t* cfg, const moe_weight_list_t* wl,
-                                 CUtensorMap* maps, const float** scales, bool encode = true) {
+                                 CUtensorMap* maps, const float** scales, bool encode = true,
+                                 const float** gs = nullptr, float* act = nullptr) {
+  if (cfg->wtype == MOE_DTYPE_NVFP4) return encode_layer_nvfp4(cfg, wl, maps, scales, gs, act, encode);
   const bool fp8 = cfg->wtype == MOE_DTYPE_FP8_E4M3;
   if (!wl->gate || !wl->up || !wl->down)
     return fail(MOE_ERR_INVALID_ARG, "gate/up/down pointer arrays must not be NULL");
@@ -451,6 +520,70 @@ static moe_status_t encode_layer(const moe_config_t* cfg, const moe_weight_list_
   return MOE_OK;
 }
 
+// NVFP4: GEMM1 descriptor of group g at 2g (the stacked gate/up codes, 2I x H/2
+// bytes; 2g+1 repeats it), GEMM2 at 2G+g (down codes, H x I/2 bytes); boxes of
+// 128 rows x 128 bytes.  scales[] hold the MMA-layout scale bytes, gs[] the
+// tensor-scale pointers (same indexing); act[0..1] = g_x, g_h.
+static moe_status_t encode_layer_nvfp4(const moe_config_t* cfg, const moe_weight_list_t* wl,
+                                       CUtensorMap* maps, const float** scales, const float** gs,
+                                       float* act, bool encode) {
+  if (!wl->gate || !wl->down || !wl->gate_sf || !wl->down_sf || !wl->gate_tscale ||
+      !wl->down_tscale)
+    return fail(MOE_ERR_INVALID_ARG,
+                "NVFP4 weights need gate, down, gate_sf, down_sf, gate_tscale and down_tscale arrays");
+  if (!std::isfinite(wl->input_scale) || wl->input_scale <= 0.0f ||
+      !std::isfinite(wl->hidden_scale) || wl->hidden_scale <= 0.0f)
+    return fail(MOE_ERR_INVALID_ARG, "NVFP4 input_scale and hidden_scale must be finite and > 0");
+  const int E = cfg->E;
+  char nm[64];
+  for (int e = 0; e < E; ++e) {
+    snprintf(nm, sizeof nm, "gate[%d]", e);
+    MOE_TRY(check_ptr(wl->gate[e], nm));
+    snprintf(nm, sizeof nm, "down[%d]", e);
+    MOE_TRY(check_ptr(wl->down[e], nm));
+    snprintf(nm, sizeof nm, "gate_sf[%d]", e);
+    MOE_TRY(check_ptr(wl->gate_sf[e], nm));
+    snprintf(nm, sizeof nm, "down_sf[%d]", e);
+    MOE_TRY(check_ptr(wl->down_sf[e], nm));
+    snprintf(nm, sizeof nm, "gate_tscale[%d]", e);
+    MOE_TRY(check_ptr4(wl->gate_tscale[e], nm));
+    snprintf(nm, sizeof nm, "down_tscale[%d]", e);
+    MOE_TRY(check_ptr4(wl->down_tscale[e], nm));
+  }
+  const bool shared = cfg->I_shared > 0;
+  if (shared) {
+    MOE_TRY(check_ptr(wl->shared_gate, "shared_gate"));
+    MOE_TRY(check_ptr(wl->shared_down, "shared_down"));
+    MOE_TRY(check_ptr(wl->shared_gate_sf, "shared_gate_sf"));
+    MOE_TRY(check_ptr(wl->shared_down_sf, "shared_down_sf"));
+    MOE_TRY(check_ptr4(wl->shared_gate_tscale, "shared_gate_tscale"));
+    MOE_TRY(check_ptr4(wl->shared_down_tscale, "shared_down_tscale"));
+  }
+  if (!encode) return MOE_OK;
+  const int G = E + (shared ? 1 : 0);
+  CUtensorMap* m1 = maps;
+  CUtensorMap* m2 = maps + 2 * G;
+  const uint64_t H = cfg->H, I = cfg->I, Is = cfg->I_shared;
+  for (int g = 0; g < G; ++g) {
+    const bool sh = g == E;
+    const uint64_t inter = sh ? Is : I;
+    const void* wgu = sh ? wl->shared_gate : wl->gate[g];
+    const void* wd = sh ? wl->shared_down : wl->down[g];
+    MOE_TRY(encode_2d(&m1[2 * g], false, wgu, H / 2, 2 * inter, 128, kNvfp4Rows));
+    m1[2 * g + 1] = m1[2 * g];
+    MOE_TRY(encode_2d(&m2[g], false, wd, inter / 2, H, 128, kNvfp4Rows));
+    scales[2 * g] = static_cast<const float*>(sh ? wl->shared_gate_sf : wl->gate_sf[g]);
+    scales[2 * g + 1] = scales[2 * g];
+    scales[2 * G + g] = static_cast<const float*>(sh ? wl->shared_down_sf : wl->down_sf[g]);
+    gs[2 * g] = sh ? wl->shared_gate_tscale : wl->gate_tscale[g];
+    gs[2 * g + 1] = gs[2 * g];
+    gs[2 * G + g] = sh ? wl->shared_down_tscale : wl->down_tscale[g];
+  }
+  act[0] = wl->input_scale;
+  act[1] = wl->hidden_scale;
+  return MOE_OK;
+}
+
 moe_status_t moe_weights_create(const moe_config_t* cfg, const moe_weight_list_t* wl,
                                 moe_weights_t* out) {
   MOE_TRY(check_config(cfg));
@@ -461,18 +594,28 @@ moe_status_t moe_weights_create(const moe_config_t* cfg, const moe_weight_list_t
               cfg->I_shared / 128 > kFp8MaxKBlocks))
     return fail(MOE_ERR_UNSUPPORTED, "fp8 layers need H, I and I_shared <= %d",
                 128 * kFp8MaxKBlocks);
+  const bool fp4 = cfg->wtype == MOE_DTYPE_NVFP4;
   const int G = cfg->E + (cfg->I_shared > 0 ? 1 : 0);
   std::vector<CUtensorMap> maps(3 * G);
-  std::vector<const float*> scales(fp8 ? 3 * G : 0);
-  MOE_TRY(encode_layer(cfg, wl, maps.data(), scales.data()));
+  std::vector<const float*> scales((fp8 || fp4) ? 3 * G : 0);
+  std::vector<const float*> gs(fp4 ? 3 * G : 0);
+  float act[2] = {0.0f, 0.0f};
+  MOE_TRY(encode_layer(cfg, wl, maps.data(), scales.data(), true, gs.data(), act));
+  // device table: maps [3G] | scale pointers [3G] | NVFP4: tensor-scale pointers [3G] | g_x, g_h
   void* table = nullptr;
   const size_t map_bytes = maps.size() * sizeof(CUtensorMap);
   const size_t sc_bytes = scales.size() * sizeof(const float*);
-  MOE_CUDA(cudaMalloc(&table, map_bytes + sc_bytes));
-  cudaError_t e = cudaMemcpy(table, maps.data(), map_bytes, cudaMemcpyHostToDevice);
+  const size_t gs_bytes = gs.size() * sizeof(const float*);
+  const size_t act_bytes = fp4 ? sizeof(act) : 0;
+  MOE_CUDA(cudaMalloc(&table, map_bytes + sc_bytes + gs_bytes + act_bytes));
+  uint8_t* tb = static_cast<uint8_t*>(table);
+  cudaError_t e = cudaMemcpy(tb, maps.data(), map_bytes, cudaMemcpyHostToDevice);
   if (e == cudaSuccess && sc_bytes)
-    e = cudaMemcpy(static_cast<uint8_t*>(table) + map_bytes, scales.data(), sc_bytes,
-                   cudaMemcpyHostToDevice);
+    e = cudaMemcpy(tb + map_bytes, scales.data(), sc_bytes, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && gs_bytes)
+    e = cudaMemcpy(tb + map_bytes + sc_bytes, gs.data(), gs_bytes, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && act_bytes)
+    e = cudaMemcpy(tb + map_bytes + sc_bytes + gs_bytes, act, act_bytes, cudaMemcpyHostToDevice);
   if (e != cudaSuccess) {
     cudaFree(table);
     return cuda_fail(e, "cudaMemcpy(weight table)");
@@ -483,9 +626,13 @@ moe_status_t moe_weights_create(const moe_config_t* cfg, const moe_weight_list_t
   w->table = table;
   w->maps1 = static_cast<CUtensorMap*>(table);
   w->maps2 = static_cast<CUtensorMap*>(table) + 2 * G;
-  const float** sp = reinterpret_cast<const float**>(static_cast<uint8_t*>(table) + map_bytes);
-  w->scales1 = fp8 ? sp : nullptr;
-  w->scales2 = fp8 ? sp + 2 * G : nullptr;
+  const float** sp = reinterpret_cast<const float**>(tb + map_bytes);
+  w->scales1 = (fp8 || fp4) ? sp : nullptr;
+  w->scales2 = (fp8 || fp4) ? sp + 2 * G : nullptr;
+  const float** gp = reinterpret_cast<const float**>(tb + map_bytes + sc_bytes);
+  w->gs1 = fp4 ? gp : nullptr;
+  w->gs2 = fp4 ? gp + 2 * G : nullptr;
+  w->act = fp4 ? reinterpret_cast<float*>(tb + map_bytes + sc_bytes + gs_bytes) : nullptr;
   *out = w;
   return MOE_OK;
 }
@@ -508,7 +655,10 @@ moe_status_t moe_stack_create(const moe_config_t* cfg, int32_t num_layers,
   const int E_pad = (cfg->E + 15) / 16 * 16;
   std::vector<CUtensorMap> maps(size_t(L) * 3 * G), router(L);
   std::vector<const float*> bias(L, nullptr);
-  std::vector<const float*> scales(fp8 ? size_t(L) * 3 * G : 0);
+  const bool fp4 = cfg->wtype == MOE_DTYPE_NVFP4;
+  std::vector<const float*> scales((fp8 || fp4) ? size_t(L) * 3 * G : 0);
+  std::vector<const float*> gs(fp4 ? size_t(L) * 3 * G : 0);
+  std::vector<float> act(fp4 ? size_t(L) * 2 : 0);
   // every layer's arguments are checked before anything is encoded
   for (int l = 0; l < L; ++l) {
     MOE_TRY(encode_layer(cfg, &layers[l], nullptr, nullptr, false));
@@ -523,7 +673,9 @@ moe_status_t moe_stack_create(const moe_config_t* cfg, int32_t num_layers,
   }
   for (int l = 0; l < L; ++l) {
     MOE_TRY(encode_layer(cfg, &layers[l], maps.data() + size_t(l) * 3 * G,
-                         fp8 ? scales.data() + size_t(l) * 3 * G : nullptr));
+                         (fp8 || fp4) ? scales.data() + size_t(l) * 3 * G : nullptr, true,
+                         fp4 ? gs.data() + size_t(l) * 3 * G : nullptr,
+                         fp4 ? act.data() + size_t(l) * 2 : nullptr));
     MOE_TRY(encode_2d(&router[l], true, w_router[l], cfg->H, cfg->E, kTileK, E_pad));
   }
   // device table: maps [L][3G] | router maps [L] | bias [L] | fp8 scales [L][3G]
@@ -531,8 +683,10 @@ moe_status_t moe_stack_create(const moe_config_t* cfg, int32_t num_layers,
   const size_t router_b = router.size() * sizeof(CUtensorMap);
   const size_t bias_b = bias.size() * sizeof(const float*);
   const size_t scales_b = scales.size() * sizeof(const float*);
+  const size_t gs_b = gs.size() * sizeof(const float*);
+  const size_t act_b = act.size() * sizeof(float);
   void* table = nullptr;
-  MOE_CUDA(cudaMalloc(&table, maps_b + router_b + bias_b + scales_b));
+  MOE_CUDA(cudaMalloc(&table, maps_b + router_b + bias_b + scales_b + gs_b + act_b));
   uint8_t* tb = static_cast<uint8_t*>(table);
   cudaError_t e = cudaMemcpy(tb, maps.data(), maps_b, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(tb + maps_b, router.data(), router_b, cudaMemcpyHostToDevice);
@@ -540,6 +694,12 @@ moe_status_t moe_stack_create(const moe_config_t* cfg, int32_t num_layers,
     e = cudaMemcpy(tb + maps_b + router_b, bias.data(), bias_b, cudaMemcpyHostToDevice);
   if (e == cudaSuccess && scales_b)
     e = cudaMemcpy(tb + maps_b + router_b + bias_b, scales.data(), scales_b, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && gs_b)
+    e = cudaMemcpy(tb + maps_b + router_b + bias_b + scales_b, gs.data(), gs_b,
+                   cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && act_b)
+    e = cudaMemcpy(tb + maps_b + router_b + bias_b + scales_b + gs_b, act.data(), act_b,
+                   cudaMemcpyHostToDevice);
   if (e != cudaSuccess) {
     cudaFree(table);
     return cuda_fail(e, "cudaMemcpy(stack table)");
@@ -553,7 +713,12 @@ moe_status_t moe_stack_create(const moe_config_t* cfg, int32_t num_layers,
   st->maps = reinterpret_cast<CUtensorMap*>(tb);
   st->router = reinterpret_cast<CUtensorMap*>(tb + maps_b);
   st->bias = reinterpret_cast<const float**>(tb + maps_b + router_b);
-  st->scales = fp8 ? reinterpret_cast<const float**>(tb + maps_b + router_b + bias_b) : nullptr;
+  st->scales = (fp8 || fp4) ? reinterpret_cast<const float**>(tb + maps_b + router_b + bias_b)
+                            : nullptr;
+  st->gs = fp4 ? reinterpret_cast<const float**>(tb + maps_b + router_b + bias_b + scales_b)
+               : nullptr;
+  st->act = fp4 ? reinterpret_cast<float*>(tb + maps_b + router_b + bias_b + scales_b + gs_b)
+                : nullptr;
   *out = st;
   return MOE_OK;
 }
@@ -769,6 +934,116 @@ static moe_status_t run_ffn_fp8(const moe_config_t& c, const WeightView& W, cons
   return MOE_OK;
 }
 
+// NVFP4: histogram, scan (with the 128-row padded offsets) and the quantising
+// scatter; then the tile plan, GEMM1 (NVFP4 h + scales) and GEMM2 (fp16 y with
+// power-of-two scales per 32 columns, unpadded rows).
+static moe_status_t run_nvfp4(const moe_config_t& c, const WeightView& W, const Layout& L, void* ws,
+                              const void* x, const int32_t* ids, const float* topk_w,
+                              int32_t* counts, int32_t* offsets, int32_t* perm_token,
+                              int32_t* inv_row, float* row_weight, void* y, float* y_sc,
+                              void* shared_out, float* sh_sc, cudaStream_t st) {
+  uint32_t* err = err_word(ws);
+  const bool shared = c.I_shared > 0;
+  const int64_t R = c.T * c.k;
+  const int64_t Rp = nvfp4_rows(c), Tp = nvfp4_tokens(c);
+  const int nblk = static_cast<int>((c.T + kPermTok - 1) / kPermTok);
+  int32_t* blk_counts = at<int32_t*>(ws, L.blk_counts);
+  int32_t* blk_base = at<int32_t*>(ws, L.blk_base);
+  int32_t* pad_offsets = at<int32_t*>(ws, L.pad_offsets);
+  uint8_t* xq = at<uint8_t*>(ws, L.x_perm);
+  uint8_t* xq_sf = at<uint8_t*>(ws, L.x_perm_sc);
+  uint8_t* xs = shared ? at<uint8_t*>(ws, L.xq) : nullptr;
+  uint8_t* xs_sf = shared ? at<uint8_t*>(ws, L.xq_sc) : nullptr;
+  trace_mark(st, MOE_K_HIST);
+  MOE_CUDA(launch_hist(ids, c.T, c.k, c.E, blk_counts, err, st));
+  trace_mark(st, MOE_K_SCAN);
+  MOE_CUDA(launch_scan(blk_counts, nblk, c.E, blk_base, counts, offsets, st, pad_offsets));
+  Nvfp4Scatter q{};
+  q.pad_offsets = pad_offsets;
+  q.act_scales = W.act;
+  q.layer = W.layer;
+  q.num_layers = W.num_layers;
+  q.rows_pad = Rp;
+  q.x_codes = xq;
+  q.x_sf = xq_sf;
+  q.xs_codes = xs;
+  q.xs_sf = xs_sf;
+  trace_mark(st, MOE_K_SCATTER);
+  MOE_CUDA(launch_scatter_nvfp4(ids, topk_w, x, c.T, c.k, c.E, c.H, blk_base, offsets, perm_token,
+                                inv_row, row_weight, q, err, st));
+
+  int32_t* s1 = at<int32_t*>(ws, L.sched1);
+  int32_t* s2 = at<int32_t*>(ws, L.sched2);
+  uint8_t* h = at<uint8_t*>(ws, L.h);
+  uint8_t* hs = at<uint8_t*>(ws, L.hs);
+  uint8_t* h_sf = at<uint8_t*>(ws, L.h_sc);
+  uint8_t* hs_sf = at<uint8_t*>(ws, L.hs_sc);
+  // GEMM1 tiles: 64 h columns (128 stacked gate/up rows); GEMM2 tiles: 128 y columns
+  const int n1r = c.I / 64, n1s = c.I_shared / 64, n2 = c.H / kNvfp4Rows;
+  trace_mark(st, MOE_K_PLAN);
+  MOE_CUDA(launch_plan(offsets, c.E, shared ? 1 : 0, c.T, n1r, n1s, n2, n2, s1, s2, kNvfp4Rows,
+                       kNvfp4Rows, st));
+  const int grid = sm_count();
+  CUtensorMap a0, a1;
+  MOE_TRY(encode_2d(&a0, false, xq, c.H / 2, Rp, 128, kNvfp4Rows));
+  if (shared) MOE_TRY(encode_2d(&a1, false, xs, c.H / 2, Tp, 128, kNvfp4Rows));
+  else a1 = a0;
+  Nvfp4GemmArgs g1{};
+  g1.w_maps = W.maps1;
+  g1.w_sf = reinterpret_cast<const uint8_t* const*>(W.scales1);
+  g1.w_gs = W.gs1;
+  g1.act_scales = W.act;
+  g1.layer = W.layer;
+  g1.layer_stride = W.stride;
+  g1.num_layers = W.num_layers;
+  g1.offsets = offsets;
+  g1.pad_offsets = pad_offsets;
+  g1.sched = s1;
+  g1.a_sf0 = xq_sf;
+  g1.a_sf1 = shared ? xs_sf : xq_sf;
+  g1.out0 = h;
+  g1.out1 = hs;
+  g1.out_sf0 = h_sf;
+  g1.out_sf1 = hs_sf;
+  g1.err = err;
+  g1.E = c.E;
+  g1.has_shared = shared ? 1 : 0;
+  g1.T = static_cast<int32_t>(c.T);
+  g1.K_routed = c.H;
+  g1.K_shared = c.H;
+  g1.N_routed = c.I;
+  g1.N_shared = c.I_shared;
+  trace_mark(st, MOE_K_GEMM1);
+  MOE_CUDA(launch_grouped_gemm_nvfp4(true, a0, a1, g1, grid, st));
+
+  CUtensorMap b0, b1;
+  MOE_TRY(encode_2d(&b0, false, h, c.I / 2, Rp, 128, kNvfp4Rows));
+  if (shared) MOE_TRY(encode_2d(&b1, false, hs, c.I_shared / 2, Tp, 128, kNvfp4Rows));
+  else b1 = b0;
+  Nvfp4GemmArgs g2 = g1;
+  g2.w_maps = W.maps2;
+  g2.w_sf = reinterpret_cast<const uint8_t* const*>(W.scales2);
+  g2.w_gs = W.gs2;
+  g2.sched = s2;
+  g2.a_sf0 = h_sf;
+  g2.a_sf1 = shared ? hs_sf : h_sf;
+  g2.out0 = y;
+  g2.out1 = shared_out;
+  g2.out_sf0 = nullptr;
+  g2.out_sf1 = nullptr;
+  g2.out_scales0 = y_sc;
+  g2.out_scales1 = sh_sc;
+  g2.row_weight = row_weight;
+  g2.K_routed = c.I;
+  g2.K_shared = c.I_shared;
+  g2.N_routed = c.H;
+  g2.N_shared = c.H;
+  trace_mark(st, MOE_K_GEMM2);
+  MOE_CUDA(launch_grouped_gemm_nvfp4(false, b0, b1, g2, grid, st));
+  (void)R;
+  return MOE_OK;
+}
+
 static bool same_shape(const moe_config_t& a, const moe_config_t& b) {
   return a.H == b.H && a.E == b.E && a.I == b.I && a.I_shared == b.I_shared && a.wtype == b.wtype;
 }
@@ -797,13 +1072,27 @@ static moe_status_t forward_impl(const moe_config_t* cfg, const WeightView& W, c
   void* shared_out = cfg->I_shared > 0 ? at<void*>(ws, L.shared_out) : nullptr;
 
   MOE_TRY(run_route(*cfg, x, w_router, logit_bias, ids, w, nullptr, err, st, rt));
+  const int64_t R = cfg->T * cfg->k;
+  if (cfg->wtype == MOE_DTYPE_NVFP4) {
+    // expert and shared outputs as fp16 + power-of-two scales, as for bf16 layers
+    float* y_sc = reinterpret_cast<float*>(static_cast<uint8_t*>(y_perm) + size_t(R) * cfg->H * 2);
+    float* sh_sc = shared_out ? reinterpret_cast<float*>(static_cast<uint8_t*>(shared_out) +
+                                                         size_t(cfg->T) * cfg->H * 2)
+                              : nullptr;
+    MOE_TRY(run_nvfp4(*cfg, W, L, ws, x, ids, w, counts, offsets, perm_token, inv_row, row_weight,
+                      y_perm, y_sc, shared_out, sh_sc, st));
+    trace_mark(st, MOE_K_COMBINE);
+    MOE_CUDA(launch_combine_half(y_perm, y_sc, inv_row, shared_out, sh_sc, out, cfg->T, cfg->k,
+                                 cfg->H, R, err, st));
+    trace_mark(st, -1);
+    return MOE_OK;
+  }
   float* x_perm_sc = fp8 ? at<float*>(ws, L.x_perm_sc) : nullptr;
   MOE_TRY(run_permute(*cfg, L, ws, ids, w, x, counts, offsets, perm_token, inv_row, row_weight,
                       fused ? nullptr : x_perm, x_perm_sc, st));
   // bf16 layers keep y and the shared output as fp16 with a power-of-two
   // scale per 32 columns, inside the fp32-sized workspace regions: the
   // scales follow the fp16 rows
-  const int64_t R = cfg->T * cfg->k;
   float* y_sc = fp8 ? nullptr : reinterpret_cast<float*>(static_cast<uint8_t*>(y_perm) +
                                                          size_t(R) * cfg->H * 2);
   float* sh_sc = (fp8 || !shared_out) ? nullptr
@@ -868,6 +1157,8 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, const
                          int32_t* perm_token, int32_t* inv_row, float* row_weight, void* x_perm,
                          float* x_perm_scales, void* ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(check_config(cfg));
+  if (cfg->wtype == MOE_DTYPE_NVFP4)
+    return fail(MOE_ERR_UNSUPPORTED, "NVFP4 layers run through moe_forward / moe_forward_stack");
   MOE_TRY(check_ws(*cfg, MOE_OP_PERMUTE, ws, ws_bytes));
   MOE_TRY(check_ptr4(expert_counts, "expert_counts"));
   MOE_TRY(check_ptr4(expert_offsets, "expert_offsets"));
@@ -904,6 +1195,8 @@ moe_status_t moe_grouped_ffn(const moe_config_t* cfg, moe_weights_t weights, con
                              const float* x_shared_scales, void* y_perm, void* shared_out,
                              void* ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(check_config(cfg));
+  if (cfg->wtype == MOE_DTYPE_NVFP4)
+    return fail(MOE_ERR_UNSUPPORTED, "NVFP4 layers run through moe_forward / moe_forward_stack");
   MOE_TRY(check_ws(*cfg, MOE_OP_GROUPED_FFN, ws, ws_bytes));
   if (!weights) return fail(MOE_ERR_INVALID_ARG, "weights is NULL");
   if (!same_shape(weights->cfg, *cfg))
@@ -1031,6 +1324,43 @@ moe_status_t moe_quantize_act_fp8(const void* x, int64_t M, int64_t K, uint8_t* 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   trace_mark(st, MOE_K_QUANT);
   MOE_CUDA(launch_quant_act_fp8(x, M, K, q, scales, st));
+  trace_mark(st, -1);
+  return MOE_OK;
+}
+
+moe_status_t moe_quantize_weight_nvfp4(const void* w, const void* w2, int64_t N, int64_t K,
+                                       uint8_t* codes, uint8_t* sf, float* tensor_scale,
+                                       moe_stream_t stream) {
+  if (N <= 0 || K <= 0 || K % 64 || (w2 ? N % 64 : N % 128))
+    return fail(MOE_ERR_INVALID_ARG,
+                "NVFP4 weights need K a positive multiple of 64 and N of 128 (of 64 with w2)");
+  MOE_TRY(check_ptr(w, "w"));
+  if (w2) MOE_TRY(check_ptr(w2, "w2"));
+  MOE_TRY(check_ptr(codes, "codes"));
+  MOE_TRY(check_ptr(sf, "sf"));
+  MOE_TRY(check_ptr4(tensor_scale, "tensor_scale"));
+  if ((w2 ? 2 * N : N) * (K / 16) >= (int64_t(1) << 39)) return fail(MOE_ERR_UNSUPPORTED, "matrix too large");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  trace_mark(st, MOE_K_QUANT);
+  MOE_CUDA(launch_quant_weight_nvfp4(w, w2, N, K, codes, sf, tensor_scale, st));
+  trace_mark(st, -1);
+  return MOE_OK;
+}
+
+moe_status_t moe_quantize_act_nvfp4(const void* x, int64_t M, int64_t K, float g, uint8_t* codes,
+                                    uint8_t* sf, moe_stream_t stream) {
+  if (M < 0 || K <= 0 || K % 16)
+    return fail(MOE_ERR_INVALID_ARG, "M >= 0 and K a positive multiple of 16 required");
+  if (!std::isfinite(g) || g <= 0.0f) return fail(MOE_ERR_INVALID_ARG, "g must be finite and > 0");
+  if (M == 0) return MOE_OK;
+  MOE_TRY(check_ptr(x, "x"));
+  if (!codes || (reinterpret_cast<uintptr_t>(codes) & 7))
+    return fail(MOE_ERR_INVALID_ARG, "codes is NULL or not 8-byte aligned");
+  if (!sf) return fail(MOE_ERR_INVALID_ARG, "sf is NULL");
+  if (M * (K / 16) >= (int64_t(1) << 39)) return fail(MOE_ERR_UNSUPPORTED, "matrix too large");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  trace_mark(st, MOE_K_QUANT);
+  MOE_CUDA(launch_quant_act_nvfp4(x, M, K, g, codes, sf, st));
   trace_mark(st, -1);
   return MOE_OK;
 }

@@ -1,0 +1,355 @@
+// NVFP4 grouped GEMMs: E2M1 tokens x E2M1 expert weights, one UE4M3 scale per
+// 16 elements along K on both sides, on the tcgen05 block-scaled tensor cores
+// (kind::mxf4nvf4, scale_vec::4X).  MoE weights in NVFP4 as in the DWDP
+// write-up's experimental setup (section A4); grouped matrix multiplication
+// over per-expert weight buffers as in "ASAP: A DiSaggregated and Asynchronous
+// Inference System for MoE Prefill", section 3.4.2, and "DWDP: Distributed
+// Weight Data Parallelism for High-Performance LLM Inference on NVL72",
+// section 4.2.
+//
+// Tile: 128 token rows (UMMA M) x 128 weight rows (UMMA N), K in stages of 256
+// elements (128 bytes per row).  Each expert's rows are padded to a multiple
+// of 128 in the permuted buffers, so a tile is one aligned row block and its
+// scales are whole 512-byte atoms (see nvfp4.cuh, sf_offset).
+//   stage = A 16 KB | B 16 KB | A scales 2 KB | B scales 2 KB  (6 stages)
+// A and B arrive by TMA (128-byte swizzle), the scale atoms by 1-D bulk copies.
+// The MMA lane copies the 8 atoms of a stage into that stage's TMEM scale slot
+// (tcgen05.cp, ordered before the MMAs that read them) and issues 4 MMAs of
+// K = 64.  A slot is rewritten only after the stage's smem was released, i.e.
+// after the MMAs that read the slot completed.
+// TMEM: accumulators 2 x 128 columns (the epilogue of tile i overlaps the MMAs
+// of tile i+1), scale slots at 256 + 32 s (A: +4m, B: +16+4m).
+//
+//   GEMM1 (kGemm1): B = 128 rows of the expert's stacked gate/up matrix, whose
+//     rows are interleaved in 64-row blocks [gate 64 | up 64]: tile n holds the
+//     gate and up rows of h columns [64 n, 64 n + 64).  h = silu(g) * u with
+//     g, u = accumulator * g_x * g_w, quantised to NVFP4 with the static scale
+//     g_h: packed codes and MMA-layout scales of every row of the row block.
+//   GEMM2: B = 128 rows of W_down; y = accumulator * g_h * g_w * row weight,
+//     written as fp16 with a power-of-two scale per 32 columns (only the
+//     block's real rows, at their unpadded row index).
+// Warp roles: warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer, warps
+// 2..5 epilogue (one row per thread).  Persistent CTAs over the device-built
+// tile schedule (heaviest experts first, tiles of one weight block adjacent).
+#include <cuda_fp16.h>
+
+#include "moe_internal.h"
+#include "nvfp4.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kRows = 128;                  // token rows per tile
+constexpr int kCols = 128;                  // weight rows per tile
+constexpr int kRowBytes = 128;              // K bytes per stage and row (256 elements)
+constexpr int kABytes = kRows * kRowBytes;  // 16 KB
+constexpr int kBBytes = kCols * kRowBytes;  // 16 KB
+constexpr int kSfBytes = 2048;              // 4 atoms of 512 bytes (4 MMAs of K = 64)
+constexpr int kStageBytes = kABytes + kBBytes + 2 * kSfBytes;
+constexpr int kStages = 6;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kAccCols = 128;
+constexpr int kSfCol = 256;                 // first scale slot
+constexpr uint32_t kIdesc = ptx::idesc_nvf4(kRows, kCols);
+static_assert(kSfCol + 32 * kStages <= int(kTmemCols), "TMEM budget");
+
+struct __align__(8) SmemCtl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t afull[2];
+  uint64_t aempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + sizeof(SmemCtl);
+
+struct Tile {
+  int g, rb, nb, rows, K;
+};
+
+__device__ __forceinline__ Tile decode_tile(int t, const Nvfp4GemmArgs& a, int G) {
+  const int32_t* ts = a.sched + 1;
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(ts + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  Tile x;
+  x.g = __ldg(a.sched + G + 2 + lo);
+  const int local = t - __ldg(ts + lo);
+  const bool routed = x.g < a.E;
+  x.rows = routed ? __ldg(a.offsets + x.g + 1) - __ldg(a.offsets + x.g) : a.T;
+  x.K = routed ? a.K_routed : a.K_shared;
+  const int mt = (x.rows + kRows - 1) / kRows;
+  x.nb = local / mt;
+  x.rb = local - x.nb * mt;
+  return x;
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
+  const uint64_t t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer() - t0 > kWaitTimeoutNs) {
+      atomicOr(err, kErrTimeout);
+      return;
+    }
+  }
+}
+
+// Barrier over the 4 epilogue warps that also ORs `v` over them, so that a
+// decision to stop is taken by all of them together.
+__device__ __forceinline__ bool epi_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+template <bool kGemm1>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap map_a0,
+                              const __grid_constant__ CUtensorMap map_a1,
+                              const Nvfp4GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  SmemCtl& c = *reinterpret_cast<SmemCtl*>(smem + kStages * kStageBytes);
+  auto stage_a = [&](int s) { return smem + s * kStageBytes; };
+  auto stage_b = [&](int s) { return smem + s * kStageBytes + kABytes; };
+  auto stage_sfa = [&](int s) { return smem + s * kStageBytes + kABytes + kBBytes; };
+  auto stage_sfb = [&](int s) { return smem + s * kStageBytes + kABytes + kBBytes + kSfBytes; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = args.E + args.has_shared;
+  const int layer = resolve_layer(args.layer, args.num_layers, args.err);
+  const int tab = layer * args.layer_stride;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&c.full[s], 1);
+      ptx::mbar_init(&c.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&c.afull[b], 1);
+      ptx::mbar_init(&c.aempty[b], 4);
+    }
+    ptx::mbar_init(&c.drain, 1);
+    c.abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&c.tmem_base, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = c.tmem_base;
+  const int num_tiles = __ldg(args.sched);
+  volatile int* abort = &c.abort;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------- TMA producer
+      uint32_t it = 0;
+      for (int t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
+        const Tile x = decode_tile(t, args, G);
+        const bool routed = x.g < args.E;
+        const int prow0 = (routed ? __ldg(args.pad_offsets + x.g) : 0) + x.rb * kRows;
+        const void* map_a = routed ? static_cast<const void*>(&map_a0)
+                                   : static_cast<const void*>(&map_a1);
+        const int widx = kGemm1 ? 2 * x.g : x.g;
+        const CUtensorMap* map_b = args.w_maps + tab + widx;
+        const int atoms = x.K / 64;  // scale atoms per 128-row block
+        const uint8_t* asf = (routed ? args.a_sf0 : args.a_sf1) + int64_t(prow0 / kRows) * atoms * 512;
+        const uint8_t* bsf = args.w_sf[tab + widx] + int64_t(x.nb) * atoms * 512;
+        const int ks_n = x.K / 256;
+        bool ok = true;
+        for (int ks = 0; ks < ks_n; ++ks, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1;
+          if (!ptx::mbar_wait(&c.empty[s], ph ^ 1, abort, args.err)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(&c.full[s], kStageBytes);
+          ptx::tma_load_2d(stage_a(s), map_a, &c.full[s], ks * kRowBytes, prow0);
+          ptx::tma_load_2d(stage_b(s), map_b, &c.full[s], ks * kRowBytes, x.nb * kCols);
+          ptx::bulk_load(stage_sfa(s), asf + ks * kSfBytes, kSfBytes, &c.full[s]);
+          ptx::bulk_load(stage_sfb(s), bsf + ks * kSfBytes, kSfBytes, &c.full[s]);
+        }
+        if (!ok) break;
+      }
+      if (*abort) {
+        const uint32_t first = it > uint32_t(kStages) ? it - kStages : 0;
+        for (uint32_t j = first; j < it; ++j)
+          drain_wait(&c.full[j % kStages], (j / kStages) & 1, args.err);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------- MMA issuer
+      uint32_t it = 0, tc = 0;
+      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tc) {
+        const Tile x = decode_tile(t, args, G);
+        const int buf = tc & 1;
+        const uint32_t bph = (tc >> 1) & 1;
+        if (!ptx::mbar_wait(&c.aempty[buf], bph ^ 1, abort, args.err)) break;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + buf * kAccCols;
+        const int ks_n = x.K / 256;
+        bool ok = true;
+        for (int ks = 0; ks < ks_n; ++ks, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1;
+          if (!ptx::mbar_wait(&c.full[s], ph, abort, args.err)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t slot = tmem_base + kSfCol + 32 * s;
+          const uint32_t sa = ptx::smem_u32(stage_sfa(s)), sb = ptx::smem_u32(stage_sfb(s));
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            ptx::tmem_cp_sf(slot + 4 * m, ptx::sf_atom_desc(sa + 512 * m));
+            ptx::tmem_cp_sf(slot + 16 + 4 * m, ptx::sf_atom_desc(sb + 512 * m));
+          }
+          const uint64_t da = ptx::sw128_desc(ptx::smem_u32(stage_a(s)));
+          const uint64_t db = ptx::sw128_desc(ptx::smem_u32(stage_b(s)));
+#pragma unroll
+          for (int m = 0; m < 4; ++m)
+            ptx::mma_nvf4(d, da + 2 * m, db + 2 * m, kIdesc, slot + 4 * m, slot + 16 + 4 * m,
+                          (ks | m) != 0);
+          ptx::mma_commit(&c.empty[s]);
+        }
+        if (!ok) break;
+        ptx::mma_commit(&c.afull[buf]);
+      }
+      ptx::mma_commit(&c.drain);
+      drain_wait(&c.drain, 0, args.err);
+    }
+  } else {
+    // ------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;
+    const int r = q * 32 + lane;  // row of the tile (TMEM lane)
+    const float gx = __ldg(args.act_scales + 2 * layer);
+    const float gh = __ldg(args.act_scales + 2 * layer + 1);
+    uint32_t tc = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tc) {
+      const Tile x = decode_tile(t, args, G);
+      const bool routed = x.g < args.E;
+      const int buf = tc & 1;
+      const uint32_t bph = (tc >> 1) & 1;
+      const bool ok = ptx::mbar_wait(&c.afull[buf], bph, abort, args.err);
+      if (epi_any(!ok || *abort)) break;  // uniform over the epilogue warps
+      ptx::tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kAccCols;
+      uint32_t acc[4][32];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) ptx::tmem_ld32(taddr + 32 * j, acc[j]);
+      ptx::tmem_ld_wait();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&c.aempty[buf]);  // accumulator free for tile i+2
+
+      const int widx = kGemm1 ? 2 * x.g : x.g;
+      const float gw = *args.w_gs[tab + widx];
+      if constexpr (kGemm1) {
+        // columns [0,64) gate, [64,128) up of h columns [64 nb, 64 nb + 64)
+        const float alpha = __fmul_rn(gx, gw);
+        const int n_h = routed ? args.N_routed : args.N_shared;  // I or I_shared
+        const int64_t p = (routed ? __ldg(args.pad_offsets + x.g) : 0) + int64_t(x.rb) * kRows + r;
+        uint8_t* codes = static_cast<uint8_t*>(routed ? args.out0 : args.out1) + p * (n_h / 2) + x.nb * 32;
+        uint8_t* sf = routed ? args.out_sf0 : args.out_sf1;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float h[2][16];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float gv = __uint_as_float(acc[hh][i]) * alpha;
+            const float uv = __uint_as_float(acc[2 + hh][i]) * alpha;
+            h[i >> 4][i & 15] = silu_f(gv) * uv;
+          }
+          uint2 q0, q1;
+          const uint32_t s0 = nvfp4::quantize16(h[0], gh, q0);
+          const uint32_t s1 = nvfp4::quantize16(h[1], gh, q1);
+          *reinterpret_cast<uint4*>(codes + hh * 16) = make_uint4(q0.x, q0.y, q1.x, q1.y);
+          *reinterpret_cast<uint16_t*>(sf + nvfp4::sf_offset(p, 4 * x.nb + 2 * hh, n_h)) =
+              static_cast<uint16_t>(s0 | (s1 << 8));
+        }
+      } else {
+        const float alpha = __fmul_rn(gh, gw);
+        const int n_out = args.N_routed;  // H
+        const int valid_rows = x.rows - x.rb * kRows;
+        if (r < valid_rows) {
+          const int64_t row = (routed ? int64_t(__ldg(args.offsets + x.g)) : 0) +
+                              int64_t(x.rb) * kRows + r;
+          const float w = (routed && args.row_weight) ? args.row_weight[row] : 1.0f;
+          const float wa = w * alpha;
+          __half* y = static_cast<__half*>(routed ? args.out0 : args.out1) + row * n_out + x.nb * kCols;
+          float* ys = (routed ? args.out_scales0 : args.out_scales1) + row * (n_out / 32) + x.nb * 4;
+#pragma unroll
+          for (int cb = 0; cb < 4; ++cb) {
+            float amax = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(wa * __uint_as_float(acc[cb][j])));
+            // fp16 with a power-of-two scale s = 2^(floor(log2 amax) - 14): |y| / s < 2^15
+            int sb = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 14;
+            sb = sb < 1 ? 1 : sb;
+            const float scale = __uint_as_float(static_cast<uint32_t>(sb) << 23);
+            const float inv = __uint_as_float(static_cast<uint32_t>(254 - sb) << 23);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t pk[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int i = v * 8 + e * 2;
+                const __half2 hh = __floats2half2_rn(wa * __uint_as_float(acc[cb][i]) * inv,
+                                                     wa * __uint_as_float(acc[cb][i + 1]) * inv);
+                pk[e] = *reinterpret_cast<const uint32_t*>(&hh);
+              }
+              *reinterpret_cast<uint4*>(y + cb * 32 + v * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            ys[cb] = scale;
+          }
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <bool kGemm1>
+cudaError_t launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const Nvfp4GemmArgs& args,
+                        int grid, cudaStream_t stream) {
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(grouped_gemm_nvfp4_kernel<kGemm1>),
+                                   static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  grouped_gemm_nvfp4_kernel<kGemm1><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_nvfp4(bool gemm1, const CUtensorMap& map_a0,
+                                      const CUtensorMap& map_a1, const Nvfp4GemmArgs& args,
+                                      int grid, cudaStream_t stream) {
+  return gemm1 ? launch_impl<true>(map_a0, map_a1, args, grid, stream)
+               : launch_impl<false>(map_a0, map_a1, args, grid, stream);
+}
+
+}  // namespace moe

@@ -97,6 +97,35 @@ struct Fp8GemmArgs {
   int32_t N_routed, N_shared;     // output columns (GEMM1: I, I_s; GEMM2: H, H)
 };
 
+// NVFP4 grouped GEMM (tokens on the MMA's M side, 128-row blocks of each
+// expert's rows padded to a multiple of 128).
+constexpr int kNvfp4Rows = 128;     // token rows per tile = padding granule of the permuted rows
+struct Nvfp4GemmArgs {
+  const CUtensorMap* w_maps;      // GEMM1: stacked gate/up of group g at 2g; GEMM2: down at g
+  const uint8_t* const* w_sf;     // same indexing: the matrix's scales in the MMA layout
+  const float* const* w_gs;       // same indexing: the matrix's fp32 tensor scale (device)
+  const float* act_scales;        // [num_layers][2] static tensor scales g_x, g_h (device)
+  const int32_t* layer;           // layer stack: device layer index (tables advance by
+  int32_t layer_stride;           //   layer_stride entries per layer), else null
+  int32_t num_layers;
+  const int32_t* offsets;         // [E+1] routed row offsets
+  const int32_t* pad_offsets;     // [E+1] offsets of each expert's 128-row-padded segment
+  const int32_t* sched;           // tile schedule (128-row tiles)
+  const uint8_t* a_sf0;           // routed A scales (MMA layout over the padded rows)
+  const uint8_t* a_sf1;           // shared-expert A scales (MMA layout over token rows)
+  void* out0;                     // GEMM1: h codes [padded rows, I/2]; GEMM2: fp16 y [T*k, H]
+  void* out1;                     // GEMM1: shared h codes [T pad, I_s/2]; GEMM2: fp16 [T, H]
+  uint8_t* out_sf0;               // GEMM1: h scales (MMA layout)
+  uint8_t* out_sf1;               // GEMM1: shared h scales (MMA layout)
+  float* out_scales0;             // GEMM2: y power-of-two scales [T*k, H/32]
+  float* out_scales1;             // GEMM2: shared [T, H/32]
+  const float* row_weight;        // GEMM2: per routed row (unpadded order), or null
+  uint32_t* err;
+  int32_t E, has_shared, T;
+  int32_t K_routed, K_shared;     // reduction sizes (multiples of 256)
+  int32_t N_routed, N_shared;     // GEMM1: I, I_shared (h columns); GEMM2: H, H
+};
+
 // --------------------------------------------------------------- launchers
 // Router of one layer, or (w_table non-null) of layer *layer of a stack whose
 // router descriptors and bias pointers are device tables [num_layers].
@@ -115,14 +144,39 @@ cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_w, in
 cudaError_t launch_hist(const int32_t* ids, int64_t T, int k, int E, int32_t* blk_counts,
                         uint32_t* err, cudaStream_t stream);
 
+// pad_offsets (optional, [E+1]): exclusive scan of the counts rounded up to
+// multiples of 128 (the NVFP4 layout of the permuted rows).
 cudaError_t launch_scan(const int32_t* blk_counts, int nblk, int E, int32_t* blk_base,
-                        int32_t* counts, int32_t* offsets, cudaStream_t stream);
+                        int32_t* counts, int32_t* offsets, cudaStream_t stream,
+                        int32_t* pad_offsets = nullptr);
 
 cudaError_t launch_scatter(const int32_t* ids, const float* topk_w, const void* x, int64_t T,
                            int k, int E, int H, int fp8, const int32_t* blk_base,
                            const int32_t* offsets, int32_t* perm_token, int32_t* inv_row,
                            float* row_weight, void* x_perm, float* x_perm_scales, uint32_t* err,
                            cudaStream_t stream);
+
+// NVFP4 scatter: the maps as launch_scatter; each token quantised once with the
+// static tensor scale *g_x (g_x = act_scales + 2 * layer), its codes written to
+// its k padded rows (pad_offsets) with MMA-layout scales, and (xs_codes non-null)
+// to its own row of the token-order copy for the shared expert.  The scales of
+// every padding row are set to zero.
+struct Nvfp4Scatter {
+  const int32_t* pad_offsets;
+  const float* act_scales;
+  const int32_t* layer;
+  int32_t num_layers;
+  int64_t rows_pad;     // rows of x_perm (bounds check)
+  uint8_t* x_codes;     // [rows_pad, H/2]
+  uint8_t* x_sf;        // MMA layout over rows_pad rows
+  uint8_t* xs_codes;    // [T pad, H/2] or null
+  uint8_t* xs_sf;
+};
+cudaError_t launch_scatter_nvfp4(const int32_t* ids, const float* topk_w, const void* x,
+                                 int64_t T, int k, int E, int H, const int32_t* blk_base,
+                                 const int32_t* offsets, int32_t* perm_token, int32_t* inv_row,
+                                 float* row_weight, const Nvfp4Scatter& q, uint32_t* err,
+                                 cudaStream_t stream);
 
 // Grid (a multiple of 2) of the grouped GEMMs: as many CTA pairs as the
 // device can hold at once.
@@ -135,6 +189,10 @@ cudaError_t launch_plan(const int32_t* offsets, int E, int has_shared, int64_t T
 cudaError_t launch_grouped_gemm_fp8(bool gate_up, const CUtensorMap& tok_map0,
                                     const CUtensorMap& tok_map1, const Fp8GemmArgs& args, int grid,
                                     cudaStream_t stream);
+
+cudaError_t launch_grouped_gemm_nvfp4(bool gemm1, const CUtensorMap& map_a0,
+                                      const CUtensorMap& map_a1, const Nvfp4GemmArgs& args,
+                                      int grid, cudaStream_t stream);
 
 cudaError_t launch_grouped_gemm(bool swiglu, const CUtensorMap& map_a0, const CUtensorMap& map_a1,
                                 const GemmArgs& args, int grid, cudaStream_t stream);
@@ -155,6 +213,18 @@ cudaError_t launch_quant_weight_fp8(const float* w, int64_t N, int64_t K, uint8_
 
 cudaError_t launch_quant_act_fp8(const void* x, int64_t M, int64_t K, uint8_t* q, float* scales,
                                  cudaStream_t stream);
+
+// NVFP4 weights: bf16 [N, K] (w2 null) or the stacked gate/up pair (w, w2 both
+// [N, K]; output rows interleaved in 64-row blocks [w 64 | w2 64]); codes
+// [rows, K/2], MMA-layout scales, tensor scale amax / 2688 into *tensor_scale.
+cudaError_t launch_quant_weight_nvfp4(const void* w, const void* w2, int64_t N, int64_t K,
+                                      uint8_t* codes, uint8_t* sf, float* tensor_scale,
+                                      cudaStream_t stream);
+
+// NVFP4 activations with a static tensor scale: codes [M, K/2], row-major
+// scales [M, K/16] (e4m3 codes).
+cudaError_t launch_quant_act_nvfp4(const void* x, int64_t M, int64_t K, float g, uint8_t* codes,
+                                   uint8_t* sf, cudaStream_t stream);
 
 }  // namespace moe
 

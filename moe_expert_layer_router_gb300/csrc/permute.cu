@@ -20,6 +20,7 @@
 #include <cuda_fp8.h>
 
 #include "moe_internal.h"
+#include "nvfp4.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -60,9 +61,10 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
 __global__ void __launch_bounds__(kScanThreads)
     scan_kernel(const int32_t* __restrict__ blk_counts, int nblk, int E,
                 int32_t* __restrict__ blk_base, int32_t* __restrict__ counts,
-                int32_t* __restrict__ offsets) {
+                int32_t* __restrict__ offsets, int32_t* __restrict__ pad_offsets) {
   __shared__ int tot[kMaxExperts];
   __shared__ int wsum[32];
+  __shared__ int psum[32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Each warp scans its experts' columns in batches of 256 blocks: the batch's
   // 8 loads per lane are issued together, and the next expert's first batch is
@@ -116,6 +118,22 @@ __global__ void __launch_bounds__(kScanThreads)
     counts[threadIdx.x] = v;
     offsets[threadIdx.x] = wsum[warp] + inc - v;
     if (threadIdx.x == E - 1) offsets[E] = wsum[warp] + inc;
+  }
+  if (pad_offsets == nullptr) return;
+  // the same scan over the counts rounded up to whole 128-row blocks
+  const int pv = (v + kNvfp4Rows - 1) / kNvfp4Rows * kNvfp4Rows;
+  const int pinc = warp_incl_scan(pv, lane);
+  if (lane == 31) psum[warp] = pinc;
+  __syncthreads();
+  if (warp == 0) {
+    const int s = psum[lane];
+    const int si = warp_incl_scan(s, lane);
+    psum[lane] = si - s;
+  }
+  __syncthreads();
+  if (threadIdx.x < E) {
+    pad_offsets[threadIdx.x] = psum[warp] + pinc - pv;
+    if (threadIdx.x == E - 1) pad_offsets[E] = psum[warp] + pinc;
   }
 }
 
@@ -247,6 +265,146 @@ __global__ void __launch_bounds__(kScatterThreads)
   }
 }
 
+// NVFP4 scatter: the ranks and maps as scatter_kernel; each lane quantises one
+// 16-element block of a token (nvfp4.cuh) and writes its 8 code bytes to the
+// token's k rows at their positions in the 128-row-padded layout
+// (pad_offsets[e] + the row's index inside expert e), the scales of 4 adjacent
+// blocks as one 32-bit word of the MMA scale layout.  Afterwards every block
+// zeroes part of the padding rows' scales, so that padding contributes 0.
+__global__ void __launch_bounds__(kScatterThreads)
+    scatter_nvfp4_kernel(const int32_t* __restrict__ ids, const float* __restrict__ topk_w,
+                         const __nv_bfloat16* __restrict__ x, int64_t T, int k, int E, int H,
+                         int nblk, const int32_t* __restrict__ blk_base,
+                         const int32_t* __restrict__ offsets, int32_t* __restrict__ perm_token,
+                         int32_t* __restrict__ inv_row, float* __restrict__ row_weight,
+                         const Nvfp4Scatter qa, uint32_t* err) {
+  __shared__ uint32_t mask[kMaxExperts][kPermTok / 32];
+  __shared__ int64_t pos_s[kPermTok * kMaxK];
+  for (int i = threadIdx.x; i < E * (kPermTok / 32); i += kScatterThreads)
+    (&mask[0][0])[i] = 0u;
+  __syncthreads();
+  const int64_t t0 = int64_t(blockIdx.x) * kPermTok;
+  const int nt = static_cast<int>(T - t0 < kPermTok ? T - t0 : kPermTok);
+  const int n = nt * k;
+  const int32_t* src = ids + t0 * k;
+  for (int i = threadIdx.x; i < n; i += kScatterThreads) {
+    const int tl = i / k;
+    const int e = src[i];
+    if (static_cast<unsigned>(e) < static_cast<unsigned>(E))
+      atomicOr(&mask[e][tl >> 5], 1u << (tl & 31));
+  }
+  __syncthreads();
+  const int64_t R = T * k;
+  const bool write_maps = blockIdx.y == 0;
+  for (int i = threadIdx.x; i < n; i += kScatterThreads) {
+    const int tl = i / k;
+    const int e = src[i];
+    int32_t row = -1;
+    int64_t pos = -1;
+    if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) {
+      const int wd = tl >> 5;
+      int rank = __popc(mask[e][wd] & ((1u << (tl & 31)) - 1u));
+      for (int w = 0; w < wd; ++w) rank += __popc(mask[e][w]);
+      const int64_t local = int64_t(blk_base[int64_t(e) * nblk + blockIdx.x]) + rank;
+      const int64_t r = int64_t(offsets[e]) + local;
+      const int64_t p = int64_t(qa.pad_offsets[e]) + local;
+      if (r >= 0 && r < R && p >= 0 && p < qa.rows_pad) {
+        row = static_cast<int32_t>(r);
+        pos = p;
+      } else if (write_maps) {
+        atomicOr(err, kErrBounds);
+      }
+    } else if (write_maps) {
+      atomicOr(err, kErrBounds);
+    }
+    pos_s[i] = pos;
+    if (write_maps) {
+      inv_row[t0 * k + i] = row;
+      if (row >= 0) {
+        perm_token[row] = static_cast<int32_t>(t0 + tl);
+        if (row_weight) row_weight[row] = topk_w[t0 * k + i];
+      }
+    }
+  }
+  __syncthreads();
+
+  const int layer = resolve_layer(qa.layer, qa.num_layers, err);
+  const float g = __ldg(qa.act_scales + 2 * layer);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = kScatterThreads / 32;
+  // this block's column slice, in whole 128-column groups (8 blocks each)
+  const int groups = H / 128;
+  const int b_lo = static_cast<int>(int64_t(groups) * blockIdx.y / gridDim.y) * 8;
+  const int b_hi = static_cast<int>(int64_t(groups) * (blockIdx.y + 1) / gridDim.y) * 8;
+  for (int tl = warp; tl < nt; tl += nwarps) {
+    const __nv_bfloat16* xr = x + (t0 + tl) * int64_t(H);
+    const int64_t* pp = pos_s + tl * k;
+    for (int b0 = b_lo; b0 < b_hi; b0 += 32) {
+      const int b = b0 + lane;
+      const bool on = b < b_hi;  // groups of 4 lanes are all on or all off
+      float f[16];
+      if (on) {
+        const uint4 u0 = __ldcs(reinterpret_cast<const uint4*>(xr + b * 16));
+        const uint4 u1 = __ldcs(reinterpret_cast<const uint4*>(xr + b * 16 + 8));
+        const uint32_t w8[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          f[2 * j] = __uint_as_float(w8[j] << 16);
+          f[2 * j + 1] = __uint_as_float(w8[j] & 0xffff0000u);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) f[j] = 0.0f;
+      }
+      uint2 q;
+      const uint32_t sc = nvfp4::quantize16(f, g, q);
+      uint32_t w4 = sc << (8 * (lane & 3));
+      w4 |= __shfl_xor_sync(0xffffffffu, w4, 1);
+      w4 |= __shfl_xor_sync(0xffffffffu, w4, 2);
+      if (!on) continue;
+      for (int j = 0; j < k; ++j) {
+        const int64_t p = pp[j];
+        if (p < 0) continue;
+        *reinterpret_cast<uint2*>(qa.x_codes + p * (H / 2) + b * 8) = q;
+        if ((lane & 3) == 0)
+          *reinterpret_cast<uint32_t*>(qa.x_sf + nvfp4::sf_offset(p, b, H)) = w4;
+      }
+      if (qa.xs_codes) {
+        const int64_t t = t0 + tl;
+        *reinterpret_cast<uint2*>(qa.xs_codes + t * (H / 2) + b * 8) = q;
+        if ((lane & 3) == 0)
+          *reinterpret_cast<uint32_t*>(qa.xs_sf + nvfp4::sf_offset(t, b, H)) = w4;
+      }
+    }
+  }
+
+  // padding rows: zero scale words (4 blocks each), spread over the whole grid
+  const int wpr = H / 64;
+  const int64_t gthreads = int64_t(gridDim.x) * gridDim.y * blockDim.x;
+  const int64_t gtid =
+      (int64_t(blockIdx.y) * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t routed_words = int64_t(E) * (kNvfp4Rows - 1) * wpr;
+  const int64_t t_pad = (T + kNvfp4Rows - 1) / kNvfp4Rows * kNvfp4Rows;
+  const int64_t shared_words = qa.xs_sf ? (t_pad - T) * wpr : 0;
+  for (int64_t i = gtid; i < routed_words + shared_words; i += gthreads) {
+    if (i < routed_words) {
+      const int e = static_cast<int>(i / ((kNvfp4Rows - 1) * wpr));
+      const int64_t rem = i - int64_t(e) * (kNvfp4Rows - 1) * wpr;
+      const int rr = static_cast<int>(rem / wpr), w = static_cast<int>(rem - int64_t(rr) * wpr);
+      const int cnt = offsets[e + 1] - offsets[e];
+      const int pad = qa.pad_offsets[e + 1] - qa.pad_offsets[e] - cnt;
+      if (rr >= pad) continue;
+      const int64_t p = int64_t(qa.pad_offsets[e]) + cnt + rr;
+      if (p < qa.rows_pad) *reinterpret_cast<uint32_t*>(qa.x_sf + nvfp4::sf_offset(p, 4 * w, H)) = 0u;
+    } else {
+      const int64_t j = i - routed_words;
+      const int64_t t = T + j / wpr;
+      const int w = static_cast<int>(j % wpr);
+      *reinterpret_cast<uint32_t*>(qa.xs_sf + nvfp4::sf_offset(t, 4 * w, H)) = 0u;
+    }
+  }
+}
+
 // Tile schedules of GEMM1 and GEMM2 from the row offsets: per group
 // ceil(rows/tile_rows) x n_tiles tiles; groups ordered by descending tile count
 // (ties: lower group first) so the heaviest experts start first.
@@ -308,8 +466,10 @@ cudaError_t launch_hist(const int32_t* ids, int64_t T, int k, int E, int32_t* bl
 }
 
 cudaError_t launch_scan(const int32_t* blk_counts, int nblk, int E, int32_t* blk_base,
-                        int32_t* counts, int32_t* offsets, cudaStream_t stream) {
-  scan_kernel<<<1, kScanThreads, 0, stream>>>(blk_counts, nblk, E, blk_base, counts, offsets);
+                        int32_t* counts, int32_t* offsets, cudaStream_t stream,
+                        int32_t* pad_offsets) {
+  scan_kernel<<<1, kScanThreads, 0, stream>>>(blk_counts, nblk, E, blk_base, counts, offsets,
+                                              pad_offsets);
   return cudaGetLastError();
 }
 
@@ -329,6 +489,24 @@ cudaError_t launch_scatter(const int32_t* ids, const float* topk_w, const void* 
   scatter_kernel<<<dim3(nblk, ysplit), kScatterThreads, 0, stream>>>(
       ids, topk_w, static_cast<const __nv_bfloat16*>(x), T, k, E, H, nblk, fp8, blk_base, offsets,
       perm_token, inv_row, row_weight, x_perm, x_perm_scales, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter_nvfp4(const int32_t* ids, const float* topk_w, const void* x,
+                                 int64_t T, int k, int E, int H, const int32_t* blk_base,
+                                 const int32_t* offsets, int32_t* perm_token, int32_t* inv_row,
+                                 float* row_weight, const Nvfp4Scatter& q, uint32_t* err,
+                                 cudaStream_t stream) {
+  const int nblk = static_cast<int>((T + kPermTok - 1) / kPermTok);
+  int sm = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev);
+  int ysplit = (2 * sm + nblk - 1) / nblk;
+  if (ysplit > H / 128) ysplit = H / 128;
+  if (ysplit < 1) ysplit = 1;
+  scatter_nvfp4_kernel<<<dim3(nblk, ysplit), kScatterThreads, 0, stream>>>(
+      ids, topk_w, static_cast<const __nv_bfloat16*>(x), T, k, E, H, nblk, blk_base, offsets,
+      perm_token, inv_row, row_weight, q, err);
   return cudaGetLastError();
 }
 

@@ -210,6 +210,59 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
   return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// ---------------------------------------------------------------- NVFP4 (block-scaled fp4)
+// 1-D bulk copy global -> shared, completing on `bar` (both addresses 16-byte
+// aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Descriptor of a 512-byte scale-factor atom in shared memory for tcgen05.cp:
+// 32 rows of 16 bytes, no swizzle (four 8-row core matrices, 128 bytes apart).
+__device__ __forceinline__ uint64_t sf_atom_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);  // start address
+  d |= static_cast<uint64_t>(128 >> 4) << 16;                // leading byte offset
+  d |= static_cast<uint64_t>(128 >> 4) << 32;                // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                       // descriptor version (tcgen05)
+  return d;
+}
+
+// Copies one scale-factor atom (row j's 16 bytes hold the four K-block scales
+// of rows j, 32+j, 64+j, 96+j) into TMEM columns taddr..taddr+3 of lanes 0..31,
+// replicated into all four lane quarters: the layout the block-scaled MMA reads
+// for 128 rows (row 32i+j at lane j, column i; byte b = K block b).
+__device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// D (+)= (A x SFA) (B x SFB)^T, A/B packed E2M1 (K = 64 per instruction), one
+// UE4M3 scale per 16 elements along K (scale_vec::4X).  sfa/sfb: TMEM addresses
+// of the 4-column scale groups (4-column aligned).
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor: dense, A/B = E2M1 (format 1), UE4M3 scales (bit 23
+// clear), scale IDs 0, both K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

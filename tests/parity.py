@@ -11,6 +11,14 @@ import workload as wl
 BF16_MAX_OVER_RMS = 2e-2
 BF16_MEAN_REL = 5e-3
 FP8_MAX_OVER_RMS = 6e-2
+# NVFP4 (no bound on the pages): the GPU and the oracle quantise the same values
+# with the same float32 steps, so they differ by fp32 accumulation, the fp16 /
+# bf16 output roundings, and the rare E2M1 or e4m3 decision on h that fp32 and
+# fp64 take on different sides of a rounding threshold; one such decision moves
+# a row by a few percent of RMS at the test sizes, hence the quantised-path bound
+# of the fp8 layer, with the bf16 mean bound.
+NVFP4_MAX_OVER_RMS = 6e-2
+NVFP4_MEAN_REL = 5e-3
 
 
 def f64(t) -> np.ndarray:

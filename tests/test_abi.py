@@ -31,7 +31,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_abi_version_and_strings(L):
-    assert L.moe_abi_version() == 1
+    assert L.moe_abi_version() == 2
     for s in range(7):
         assert L.moe_status_string(s)
 
@@ -165,3 +165,59 @@ def test_forward_stack_validates(L):
     assert L.moe_forward_stack(C.byref(c), None, 16, 16, 16, None, None, ws, nb.value,
                                None) == N.MOE_ERR_INVALID_ARG
     assert b"stack" in L.moe_last_error_message()
+
+
+def test_nvfp4_config_and_entry_points(L):
+    """NVFP4 layers need H, I, I_shared multiples of 256, and run only through
+    moe_forward / moe_forward_stack."""
+    n = C.c_size_t(0)
+    for kw in (dict(H=384), dict(I=384), dict(I_shared=128)):
+        c = cfg(wtype="nvfp4", **kw)
+        assert L.moe_workspace_size(C.byref(c), N.MOE_OP_FORWARD, C.byref(n)) == N.MOE_ERR_UNSUPPORTED
+    c = cfg(wtype="nvfp4", I_shared=256)
+    assert L.moe_workspace_size(C.byref(c), N.MOE_OP_FORWARD, C.byref(n)) == N.MOE_OK
+    # the padded NVFP4 rows: at most T*k + 127 E, in 128-row blocks, times H/2 + H/16 bytes
+    Rp = (256 * 2 + 127 * 8 + 127) // 128 * 128
+    assert n.value >= Rp * (512 // 2 + 512 // 16)
+    ws = 0x100000
+    assert L.moe_permute(C.byref(c), 16, None, None, 16, 16, 16, 16, None, None, None, ws,
+                         n.value, None) == N.MOE_ERR_UNSUPPORTED
+    assert L.moe_grouped_ffn(C.byref(c), 16, 16, None, 16, None, None, None, 16, None, ws,
+                             n.value, None) == N.MOE_ERR_UNSUPPORTED
+
+
+def test_nvfp4_weight_list_layout():
+    assert N.MoeWeightList.gate_sf.offset == 12 * 8
+    assert N.MoeWeightList.input_scale.offset == 20 * 8
+    assert C.sizeof(N.MoeWeightList) == 20 * 8 + 8
+
+
+def test_nvfp4_weights_create_validates(L):
+    c = cfg(wtype="nvfp4", I=512)
+    h = C.c_void_p()
+    wl = N.MoeWeightList()
+    good = (C.c_void_p * 8)(*([0x1000] * 8))
+    P = C.POINTER(C.c_void_p)
+    wl.gate = wl.down = C.cast(good, P)
+    # scale and tensor-scale arrays missing
+    assert L.moe_weights_create(C.byref(c), C.byref(wl), C.byref(h)) == N.MOE_ERR_INVALID_ARG
+    assert b"gate_sf" in L.moe_last_error_message()
+    bad_sf = (C.c_void_p * 8)(*([0x1000] * 3 + [0x1008] + [0x1000] * 4))
+    wl.gate_sf = C.cast(bad_sf, P)
+    wl.down_sf = wl.gate_tscale = wl.down_tscale = C.cast(good, P)
+    wl.input_scale, wl.hidden_scale = 1.0, 0.0
+    assert L.moe_weights_create(C.byref(c), C.byref(wl), C.byref(h)) == N.MOE_ERR_INVALID_ARG
+    assert b"hidden_scale" in L.moe_last_error_message()
+    wl.hidden_scale = 0.0625
+    assert L.moe_weights_create(C.byref(c), C.byref(wl), C.byref(h)) == N.MOE_ERR_INVALID_ARG
+    assert b"gate_sf[3]" in L.moe_last_error_message()
+    assert h.value is None
+
+
+def test_nvfp4_quantize_validation(L):
+    assert L.moe_quantize_weight_nvfp4(16, None, 100, 128, 16, 16, 16, None) == N.MOE_ERR_INVALID_ARG
+    assert L.moe_quantize_weight_nvfp4(16, 16, 96, 128, 16, 16, 16, None) == N.MOE_ERR_INVALID_ARG
+    assert L.moe_quantize_weight_nvfp4(16, None, 128, 96, 16, 16, 16, None) == N.MOE_ERR_INVALID_ARG
+    assert L.moe_quantize_act_nvfp4(16, 4, 100, 1.0, 16, 16, None) == N.MOE_ERR_INVALID_ARG
+    assert L.moe_quantize_act_nvfp4(16, 4, 128, 0.0, 16, 16, None) == N.MOE_ERR_INVALID_ARG
+    assert L.moe_quantize_act_nvfp4(None, 0, 128, 1.0, None, None, None) == N.MOE_OK

@@ -1,0 +1,225 @@
+"""NVFP4 path on the GPU: the quantisers bit-exact against the oracle's codec
+(E2M1 codes, e4m3 block scales, tensor scales), and the whole layer against
+the oracle's NVFP4 layer (max |err| <= 6e-2 x RMS, mean relative <= 5e-3),
+small layers on every token and full size on sampled tokens; layer stacks
+give each layer's bits."""
+import numpy as np
+import pytest
+import torch
+
+import moe_expert_layer_router_gb300 as m
+import workload as wl
+from oracle import moe as om
+from oracle import nvfp4 as onv
+from parity import (NVFP4_MAX_OVER_RMS, NVFP4_MEAN_REL, assert_close_layer, f64,
+                    logit_tolerance, near_tie_tokens)
+
+pytestmark = pytest.mark.gpu
+
+
+# ---------------------------------------------------------------- layouts (test side)
+def unpack(codes) -> np.ndarray:
+    """uint8 [rows, K/2] (element 2i in the low nibble of byte i) -> codes [rows, K]."""
+    c = codes.cpu().numpy() if hasattr(codes, "cpu") else np.asarray(codes)
+    out = np.empty((c.shape[0], 2 * c.shape[1]), np.uint8)
+    out[:, 0::2] = c & 15
+    out[:, 1::2] = c >> 4
+    return out
+
+
+def sf_rowmajor(sf, rows, K) -> np.ndarray:
+    """MMA scale layout (512-byte atoms of 128 rows x 4 blocks) -> [rows, K/16]."""
+    s = sf.cpu().numpy() if hasattr(sf, "cpu") else np.asarray(sf)
+    r = np.arange(rows)[:, None]
+    kb = np.arange(K // 16)[None, :]
+    off = ((r // 128) * (K // 64) + kb // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + kb % 4
+    return s[off]
+
+
+def stacked_order(I) -> np.ndarray:
+    """Row v of the interleaved gate/up matrix -> row of [W_g; W_u]."""
+    v = np.arange(2 * I)
+    b, i = v // 128, v % 128
+    return np.where(i < 64, 64 * b + i, I + 64 * b + (i - 64))
+
+
+# ---------------------------------------------------------------- quantisers
+def test_weight_quantiser_bit_exact_stacked_and_plain():
+    dev = torch.device("cuda")
+    I, H = 192, 320
+    wg = wl.rng.normal_bf16(0, 91, (I, H), 0.02, dev)
+    wu = wl.rng.normal_bf16(0, 92, (I, H), 0.03, dev)
+    wg[:64, :64] = 0                                    # all-zero blocks
+    wu[7, 5] = 0.9                                      # the tensor's amax, in the up half
+    codes, sf, ts = m.moe_quantize_weight_nvfp4(wg, wu)
+    torch.cuda.synchronize()
+    ref_q, ref_s, ref_g = onv.quantize_weight(np.concatenate([f64(wg), f64(wu)]))
+    order = stacked_order(I)
+    assert ts.item() == float(ref_g)
+    assert (unpack(codes) == ref_q[order]).all()
+    assert (sf_rowmajor(sf, 2 * I, H) == ref_s[order]).all()
+
+    wd = wl.rng.normal_bf16(0, 93, (256, 192), 0.02, dev)
+    codes, sf, ts = m.moe_quantize_weight_nvfp4(wd)
+    torch.cuda.synchronize()
+    ref_q, ref_s, ref_g = onv.quantize_weight(f64(wd))
+    assert ts.item() == float(ref_g)
+    assert (unpack(codes) == ref_q).all()
+    assert (sf_rowmajor(sf, 256, 192) == ref_s).all()
+
+
+def test_weight_quantiser_all_zero_matrix():
+    dev = torch.device("cuda")
+    w = torch.zeros(128, 64, dtype=torch.bfloat16, device=dev)
+    codes, sf, ts = m.moe_quantize_weight_nvfp4(w)
+    torch.cuda.synchronize()
+    assert ts.item() == 1.0 and int(codes.sum()) == 0 and int(sf.sum()) == 0
+
+
+def test_activation_quantiser_bit_exact():
+    dev = torch.device("cuda")
+    g = 2.0 ** -8
+    x = wl.rng.normal_bf16(0, 94, (300, 512), 1.0, dev)
+    x[3] = 0                                            # zero blocks
+    x[5, :16] = 5000.0                                  # saturates the block scale (448)
+    x[6, 16:32] = 1e-4                                  # scale in the e4m3 subnormal range
+    codes, sf = m.moe_quantize_act_nvfp4(x, g)
+    torch.cuda.synchronize()
+    ref_q, ref_s = onv.quantize_blocks(f64(x).astype(np.float32), np.float32(g))
+    assert (unpack(codes) == ref_q).all()
+    assert (sf.cpu().numpy() == ref_s).all()
+    assert ref_s[5, 0] == 0x7E and ref_s[3].max() == 0
+
+
+# ---------------------------------------------------------------- the layer
+class Nvfp4Layer:
+    """Seeded NVFP4 layer: bf16 weights on the device, quantised by the library
+    for the GPU path; the oracle quantises its own copy of the same bf16 values."""
+
+    def __init__(self, lc, dev):
+        self.lc, self.dev = lc, dev
+        self.x = wl.gen_x(lc, dev)
+        self.wr = wl.gen_router(lc, dev)
+        b = wl.gen_bias(lc)
+        self.bias = b.to(dev) if b is not None else None
+        self.gx, self.gh = wl.nvfp4_act_scales(lc)
+        self.Wb = [tuple(wl.gen_expert(lc, e, w, dev) for w in ("gate", "up", "down"))
+                   for e in range(lc.E)]
+        self.Sb = (tuple(wl.gen_shared(lc, w, dev) for w in ("gate", "up", "down"))
+                   if lc.I_shared else None)
+        self.cfg = m.config_from(lc)
+        self.weights = m.quantize_experts_nvfp4(
+            self.cfg, [w[0] for w in self.Wb], [w[1] for w in self.Wb], [w[2] for w in self.Wb],
+            shared=self.Sb, input_scale=self.gx, hidden_scale=self.gh)
+        self._cache = {}
+
+    def oracle_expert(self, e):
+        if e not in self._cache:
+            self._cache[e] = onv.dequantize_expert(*onv.quantize_expert(*(f64(t) for t in self.Wb[e])))
+        return self._cache[e]
+
+    def oracle_shared(self):
+        if self.Sb is None:
+            return None
+        if "shared" not in self._cache:
+            self._cache["shared"] = onv.dequantize_expert(
+                *onv.quantize_expert(*(f64(t) for t in self.Sb)))
+        return self._cache["shared"]
+
+    def forward(self, ws=None):
+        ws = ws or m.Workspace(self.cfg, "forward")
+        out, ids, w = m.moe_forward(self.cfg, self.weights, self.x, self.wr, self.bias,
+                                    return_routing=True, ws=ws)
+        torch.cuda.synchronize()
+        assert m.moe_get_device_error(ws) == 0
+        return out, ids.cpu().numpy(), w
+
+
+def check_layer(L, n_sample=None, seed=0):
+    lc = L.lc
+    out, ids, _ = L.forward()
+    b = None if L.bias is None else f64(L.bias)
+    ref_lg = om.router_logits(f64(L.x), f64(L.wr), b)
+    ref_ids = om.select_topk(ref_lg, lc.k)
+    tie = near_tie_tokens(ref_lg, lc.k, logit_tolerance(L.x, L.wr))
+    assert (ids[~tie] == ref_ids[~tie]).all()
+    cand = np.flatnonzero(~tie)
+    if n_sample is not None:
+        cand = np.sort(np.random.default_rng(seed).choice(cand, size=n_sample, replace=False))
+    ref_w = om.routing_weights(ref_lg[cand], ref_ids[cand], lc.score, lc.renormalize,
+                               lc.route_scale)
+    ref = onv.moe_tokens_nvfp4(f64(L.x[torch.from_numpy(cand).to(L.dev)]), ref_ids[cand], ref_w,
+                               L.oracle_expert, L.oracle_shared(), L.gx, L.gh)
+    assert_close_layer(out[torch.from_numpy(cand).to(L.dev)], ref, max_over_rms=NVFP4_MAX_OVER_RMS,
+                       mean_rel=NVFP4_MEAN_REL, what=lc.name)
+    assert torch.isfinite(out.float()).all()
+    return out
+
+
+SMALL = [
+    wl.DSV3_NVFP4.with_(name="nvfp4_small", T=200, H=512, E=8, k=2, I=256, I_shared=256),
+    # ragged expert rows (some experts with a few rows, maybe none), no shared expert
+    wl.DSV3_NVFP4.with_(name="nvfp4_ragged", T=150, H=1024, E=16, k=4, I=512, I_shared=0,
+                        score="softmax", route_scale=1.0),
+    # one token, one expert: every row block is 1 real row + 127 padding rows
+    wl.DSV3_NVFP4.with_(name="nvfp4_one_token", T=1, H=512, E=4, k=1, I=256, I_shared=256),
+    # several 128-row blocks per expert and a ragged last block
+    wl.DSV3_NVFP4.with_(name="nvfp4_multi_block", T=700, H=768, E=4, k=2, I=768, I_shared=512),
+]
+
+
+@pytest.mark.parametrize("lc", SMALL, ids=lambda c: c.name)
+def test_nvfp4_forward_matches_oracle(lc):
+    check_layer(Nvfp4Layer(lc, torch.device("cuda")))
+
+
+def test_nvfp4_forward_full_size_sampled():
+    """The DeepSeek-V3 NVFP4 layer at T = 16384 in the launch configuration the
+    bench times; the oracle evaluates 3 sampled tokens through their experts."""
+    L = Nvfp4Layer(wl.DSV3_NVFP4, torch.device("cuda"))
+    check_layer(L, n_sample=3)
+
+
+def test_nvfp4_deterministic_and_empty_batch():
+    lc = SMALL[0]
+    L = Nvfp4Layer(lc, torch.device("cuda"))
+    a = L.forward()[0]
+    b = L.forward()[0]
+    assert torch.equal(a, b)
+    cfg0 = m.config_from(lc, T=0)
+    W0 = m.quantize_experts_nvfp4(cfg0, [w[0] for w in L.Wb], [w[1] for w in L.Wb],
+                                  [w[2] for w in L.Wb], shared=L.Sb, input_scale=L.gx,
+                                  hidden_scale=L.gh)
+    out = m.moe_forward(cfg0, W0, L.x[:0], L.wr)
+    torch.cuda.synchronize()
+    assert tuple(out.shape) == (0, lc.H)
+
+
+def test_nvfp4_stack_layers_match_single_layer_calls():
+    """A layer stack of NVFP4 layers: every layer gives the bits of that layer
+    run alone, directly and through one CUDA graph replayed for every layer."""
+    dev = torch.device("cuda")
+    lc = SMALL[0]
+    layers = [Nvfp4Layer(lc.with_(seed=s), dev) for s in range(2)]
+    x = layers[0].x
+    cfg = layers[0].cfg
+    refs = [m.moe_forward(cfg, L.weights, x, L.wr) for L in layers]
+    stack = m.LayerStack(cfg, [L.weights for L in layers], [L.wr for L in layers])
+    layer = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = m.Workspace(cfg, "forward")
+    out = torch.empty(lc.T, lc.H, dtype=torch.bfloat16, device=dev)
+    for l in (1, 0, 1):
+        layer.fill_(l)
+        m.moe_forward_stack(cfg, stack, layer, x, out=out, ws=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out, refs[l]), f"layer {l}"
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        m.moe_forward_stack(cfg, stack, layer, x, out=out, ws=ws, stream=torch.cuda.current_stream())
+    for l in (0, 1):
+        layer.fill_(l)
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, refs[l]), f"graph, layer {l}"
+    assert m.moe_get_device_error(ws) == 0

@@ -4,14 +4,21 @@ Shapes follow the pages' models: a tiny layer, a Qwen3-235B-A22B-shaped
 layer (E=128, top-8), a DeepSeek-V3-shaped layer (H=7168, 256 routed experts
 + 1 shared, top-8; ASAP, section 5.1 "MoE Model"), the same layer on a skewed
 batch of four concatenated sequences of 0.8x8K..8K tokens (DWDP, section
-4.1, table 1 workload), and the DeepSeek-V3 shape at T=512 with fp8 e4m3
-expert weights (AFD write-up, section 1: fp8 expert GEMMs).
+4.1, table 1 workload), the DeepSeek-V3 shape at T=512 with fp8 e4m3
+expert weights (AFD write-up, section 1: fp8 expert GEMMs), and the
+DeepSeek-V3 layer with NVFP4 expert weights (DWDP write-up, section A4: the
+DeepSeek-R1 NVFP4 checkpoint).
 
 Input recipe (all seeded, counter-based, see workload.rng):
   x        [T,H]  ~N(0, 1)     rounded to bf16
   w_router [E,H]  ~N(0, 0.02)  bf16
   w_gate/w_up [I,H], w_down [H,I] per expert, ~N(0, 0.02) (bf16, or fp32 before
-  fp8 block quantisation); shared-expert matrices likewise.
+  fp8 block quantisation; bf16 before NVFP4 quantisation); shared-expert
+  matrices likewise.
+  NVFP4 static activation scales (what a checkpoint would carry): g_x =
+  2^-8 * x_std, so a block amax up to 10.5 x_std keeps an unsaturated e4m3
+  scale; g_h = 2^-4, room for |h| up to 168 (h = silu(g) u with g, u ~ N(0,
+  (0.02^2) H), std 1.7 at H = 7168).
   Skewed batch: per-expert logit bias b_e = -gamma * 1.2 * ln(r_e) with r a
   seeded permutation of 1..E (Zipf, s = 1.2), and the four coldest ranks
   pushed to -30 so that they receive no tokens.
@@ -38,7 +45,7 @@ class LayerConfig:
     score: str = "softmax"          # "softmax" | "sigmoid"
     renormalize: bool = True
     route_scale: float = 1.0
-    wtype: str = "bf16"             # "bf16" | "fp8_e4m3"
+    wtype: str = "bf16"             # "bf16" | "fp8_e4m3" | "nvfp4"
     zipf_bias: bool = False
     x_std: float = 1.0
     w_std: float = 0.02
@@ -90,8 +97,18 @@ DSV3_SLICE = DSV3.with_(name="dsv3_slice", T=4096, E=64)
 # fp8 profiling slice: 16 tokens per expert as in the 512-token fp8 batch, 1/4 of the experts
 DSV3_FP8_SLICE = DSV3_FP8.with_(name="dsv3_fp8_slice", T=128, E=64)
 
+# DeepSeek-V3 layer with NVFP4 expert weights and activations, the prefill
+# batch of the bf16 layer; its profiling slice like dsv3_slice.
+DSV3_NVFP4 = DSV3.with_(name="dsv3_nvfp4", wtype="nvfp4")
+DSV3_NVFP4_SLICE = DSV3_NVFP4.with_(name="dsv3_nvfp4_slice", T=4096, E=64)
+
 CONFIGS = {c.name: c for c in (TINY, QWEN3, DSV3, DSV3_SKEW, DSV3_FP8, DSV3_T512, DSV3_SLICE,
-                                DSV3_FP8_SLICE)}
+                                DSV3_FP8_SLICE, DSV3_NVFP4, DSV3_NVFP4_SLICE)}
+
+
+def nvfp4_act_scales(cfg: LayerConfig) -> tuple[float, float]:
+    """Static NVFP4 tensor scales (g_x, g_h) of the synthetic checkpoint."""
+    return 2.0 ** -8 * cfg.x_std, 2.0 ** -4
 
 
 # ---------------------------------------------------------------- tensors
