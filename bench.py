@@ -144,7 +144,12 @@ def load_peaks():
 KERNEL_SOURCES = {
     "bf16": ("grouped_gemm.cu", "moe_internal.h", "ptx.cuh"),
     "fp8": ("grouped_gemm_fp8.cu", "moe_internal.h", "ptx.cuh"),
+    "nvfp4": ("grouped_gemm_nvfp4.cu", "nvfp4.cuh", "moe_internal.h", "ptx.cuh"),
 }
+
+# Dense tensor rate of fp4 (E2M1, block-scaled) relative to bf16 on GB300
+# (nominal 13.5 vs 2.25 PFLOP/s): the fp4 peak is the measured bf16 peak x 6.
+FP4_OVER_BF16 = 6.0
 
 
 def kernel_source_hash(kind: str) -> str:
@@ -174,6 +179,13 @@ def recorded_traffic(kernel: str, workload: str, kind: str):
         return None
 
 
+def weight_gb(lc) -> float:
+    """Bytes of the layer's expert weights (routed + shared) as stored."""
+    n = 3.0 * lc.H * (lc.E * lc.I + lc.I_shared)
+    per = {"bf16": 2.0, "fp8_e4m3": 1.0 + 4.0 / 128 / 128, "nvfp4": 0.5 + 1.0 / 16}[lc.wtype]
+    return n * per / 1e9
+
+
 def describe(lc) -> str:
     s = (f"{lc.name}: T={lc.T} H={lc.H} E={lc.E} top-{lc.k} I={lc.I} {lc.score}"
          f"{' x' + str(lc.route_scale) if lc.route_scale != 1.0 else ''}")
@@ -201,7 +213,18 @@ class Layer:
         self.S = (tuple(wl.gen_shared(lc, w, dev) for w in ("gate", "up", "down"))
                   if lc.I_shared else None)
         self.cfg = m.config_from(lc)
-        if lc.wtype == "fp8_e4m3":
+        if lc.wtype == "nvfp4":
+            # NVFP4: the library quantises the bf16 weights (W keeps the bf16
+            # originals, from which the oracle quantises its own copy)
+            gx, gh = wl.nvfp4_act_scales(lc)
+            self.weights = m.quantize_experts_nvfp4(
+                self.cfg, [w[0] for w in self.W], [w[1] for w in self.W], [w[2] for w in self.W],
+                shared=self.S, input_scale=gx, hidden_scale=gh)
+            torch.cuda.synchronize(dev)
+            if not keep_fp32:
+                self.W = self.S = None
+                torch.cuda.empty_cache()
+        elif lc.wtype == "fp8_e4m3":
             Q = [tuple(m.moe_quantize_weight_fp8(t) for t in w3) for w3 in self.W]
             SQ = tuple(m.moe_quantize_weight_fp8(t) for t in self.S) if self.S else None
             self.Q, self.SQ = Q, SQ
@@ -241,6 +264,16 @@ def _oracle_fp8_weights(key, t):
     return _QCACHE[key]
 
 
+def _oracle_nvfp4_expert(key, mats):
+    """The oracle's own NVFP4 quantisation of one expert's bf16 matrices (input
+    preparation, outside any timing; cached)."""
+    from oracle import nvfp4 as onv
+    if key not in _QCACHE:
+        _QCACHE[key] = onv.dequantize_expert(*onv.quantize_expert(
+            *(t.float().cpu().numpy() for t in mats)))
+    return _QCACHE[key]
+
+
 def oracle_sample(lc, layer, tokens):
     """Time the CPU oracle on `tokens` of the workload; returns (seconds, n)."""
     from oracle import moe as om
@@ -252,7 +285,11 @@ def oracle_sample(lc, layer, tokens):
     lg = om.router_logits(x, wr, b)
     need = sorted(set(om.select_topk(lg, lc.k).reshape(-1).tolist()))
     fp8 = lc.wtype == "fp8_e4m3"
-    if fp8:
+    fp4 = lc.wtype == "nvfp4"
+    if fp4:
+        host = {e: _oracle_nvfp4_expert(e, layer.W[e]) for e in need}
+        sh = _oracle_nvfp4_expert("s", layer.S) if layer.S is not None else None
+    elif fp8:
         host = {e: tuple(_oracle_fp8_weights((e, i), t) for i, t in enumerate(layer.W[e]))
                 for e in need}
         sh = (tuple(_oracle_fp8_weights(("s", i), t) for i, t in enumerate(layer.S))
@@ -261,7 +298,12 @@ def oracle_sample(lc, layer, tokens):
         host = {e: tuple(t.cpu() for t in layer.W[e]) for e in need}
         sh = tuple(t.cpu() for t in layer.S) if layer.S is not None else None
     t0 = time.perf_counter()
-    if fp8:
+    if fp4:
+        from oracle import nvfp4 as onv
+        gx, gh = wl.nvfp4_act_scales(lc)
+        onv.moe_layer_nvfp4(x, wr, b, lambda e: host[e], sh, lc.k, lc.score, lc.renormalize,
+                            lc.route_scale, gx, gh)
+    elif fp8:
         from oracle import fp8 as of8
         of8.moe_layer_fp8(x, wr, b, lambda e: tuple(of8.dequant_weight(*q) for q in host[e]),
                           tuple(of8.dequant_weight(*q) for q in sh) if sh is not None else None,
@@ -274,7 +316,7 @@ def oracle_sample(lc, layer, tokens):
 
 def cpu_baseline(lc, layer, n_tokens=None):
     if n_tokens is None:
-        n_tokens = 2 if lc.wtype == "fp8_e4m3" else 8
+        n_tokens = 2 if lc.wtype in ("fp8_e4m3", "nvfp4") else 8
     g = np.random.default_rng(1)
     tokens = sorted(g.choice(lc.T, size=n_tokens, replace=False).tolist())
     secs, n = oracle_sample(lc, layer, tokens)
@@ -428,7 +470,38 @@ def run_ours(args, lc, rank, world, dev):
     flops = lc.flops()
     tflops = flops * world / (ms * 1e-3) / 1e12
     g1_ms = kernels_ms.get("gemm1_gate_up_swiglu")
-    if lc.wtype == "fp8_e4m3":
+    fp4_peak = FP4_OVER_BF16 * float(peaks.get("bf16_tflops_sustained",
+                                               FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    if lc.wtype == "nvfp4":
+        # NVFP4 GEMM1: fp4 tensor cores or, if slower at the peaks, HBM (E2M1 codes
+        # + one e4m3 scale per 16 of the gate/up weights of every expert with
+        # tokens, the padded token rows in, h out) -- whichever takes longer
+        g1_flops = 4.0 * lc.R * lc.H * lc.I + 4.0 * lc.T * lc.H * lc.I_shared
+        counts = torch.bincount(route_ids(layer, ws, dev).reshape(-1).long(), minlength=lc.E)
+        active = int((counts > 0).sum().item())
+        rows_pad = int(((counts + 127) // 128 * 128).sum().item())
+        t_pad = (lc.T + 127) // 128 * 128
+        nib = 0.5 + 1.0 / 16  # bytes per element: code + scale
+        g1_bytes = nib * (2.0 * active * lc.I * lc.H + 2.0 * lc.I_shared * lc.H
+                          + (rows_pad + t_pad) * lc.H + rows_pad * lc.I + t_pad * lc.I_shared)
+        hpeak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        if g1_bytes / (hpeak * 1e9) > g1_flops / (fp4_peak * 1e12):
+            g1_ach = g1_bytes / (g1_ms * 1e-3) / 1e9 if g1_ms else None
+            roof = {"kernel": "gemm1_gate_up_swiglu (nvfp4)", "bound": "hbm", "achieved": g1_ach,
+                    "peak": hpeak, "unit": "GB/s", "frac": (g1_ach / hpeak) if g1_ach else None,
+                    "peak_kind": f"HBM copy, of {peak_src}",
+                    "algorithmic_bytes_per_launch": g1_bytes, "experts_with_tokens": active,
+                    "traffic": recorded_traffic("gemm1_gate_up_swiglu", lc.name, "nvfp4")}
+        else:
+            g1_tf = g1_flops / (g1_ms * 1e-3) / 1e12 if g1_ms else None
+            roof = {"kernel": "gemm1_gate_up_swiglu (nvfp4)", "bound": "tensor",
+                    "achieved": g1_tf, "peak": fp4_peak, "unit": "TFLOP/s",
+                    "frac": (g1_tf / fp4_peak) if g1_tf else None,
+                    "peak_kind": f"fp4 = {FP4_OVER_BF16:g} x bf16 sustained, of {peak_src}",
+                    "algorithmic_flop_per_launch": g1_flops,
+                    "algorithmic_bytes_per_launch": g1_bytes,
+                    "traffic": recorded_traffic("gemm1_gate_up_swiglu", lc.name, "nvfp4")}
+    elif lc.wtype == "fp8_e4m3":
         # small-batch fp8: GEMM1 streams the gate/up weights of every expert that
         # received a token (HBM-bound); algorithmic bytes per launch
         counts = torch.bincount(route_ids(layer, ws, dev).reshape(-1).long(), minlength=lc.E)
@@ -481,18 +554,23 @@ def run_ours(args, lc, rank, world, dev):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp8_e4m3 (fp32 accumulate)" if lc.wtype == "fp8_e4m3" else "bf16",
+        "dtype": {"fp8_e4m3": "fp8_e4m3 (fp32 accumulate)",
+                  "nvfp4": "nvfp4 (E2M1 x E2M1, e4m3 scale per 16, fp32 accumulate)"}.get(
+                      lc.wtype, "bf16"),
         "data": "synthetic (seeded counter-based generator; x ~N(0,1), weights ~N(0,0.02))",
         "config": {"workload": describe(lc), "tokens_per_gpu": lc.T,
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (x, 22.6 GB of expert weights); no flush"},
+                   "l2": "inputs larger than L2 (x and the expert weights: "
+                         f"{weight_gb(lc):.1f} GB); no flush"},
         "tflops": tflops,
         "pct_of_peak": {"bf16_burst": 100 * tflops / world / float(
                             peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
                         "bf16_sustained": 100 * tflops / world / float(
                             peaks.get("bf16_tflops_sustained",
                                       FALLBACK_PEAKS["bf16_tflops_sustained"])),
-                        "source": peak_src},
+                        "source": peak_src,
+                        **({"fp4_sustained": 100 * tflops / world / fp4_peak}
+                           if lc.wtype == "nvfp4" else {})},
         "kernels_ms": {k: round(v, 4) for k, v in sorted(kernels_ms.items(),
                                                            key=lambda kv: -kv[1])},
         "roofline": roof,
@@ -587,7 +665,7 @@ def run_reference(args, lc, rank, world, dev):
     # fp8: draw the per-step samples from a small fixed pool of tokens, so the
     # (untimed, cached) oracle quantisation of their experts' weights is done once
     pool = (sorted(g.choice(lc.T, size=4, replace=False).tolist())
-            if lc.wtype == "fp8_e4m3" else None)
+            if lc.wtype in ("fp8_e4m3", "nvfp4") else None)
     times, n_tok = [], 0
     for i in range(args.warmup + args.steps):
         if pool is not None:
