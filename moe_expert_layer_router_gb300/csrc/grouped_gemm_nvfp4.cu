@@ -13,10 +13,15 @@
 // scales are whole 512-byte atoms (see nvfp4.cuh, sf_offset).
 //   stage = A 16 KB | B 16 KB | A scales 2 KB | B scales 2 KB  (6 stages)
 // A and B arrive by TMA (128-byte swizzle), the scale atoms by 1-D bulk copies.
-// The MMA lane copies the 8 atoms of a stage into that stage's TMEM scale slot
-// (tcgen05.cp, ordered before the MMAs that read them) and issues 4 MMAs of
-// K = 64.  A slot is rewritten only after the stage's smem was released, i.e.
-// after the MMAs that read the slot completed.
+// Four scale warps, one per TMEM lane quarter, move each stage's scales from
+// shared memory into that stage's TMEM scale slot with tcgen05.st, in the
+// layout the block-scaled MMA reads for 128 rows: lane j (of every quarter),
+// column 4m + i holds the four K-block scales of row 32i + j for MMA m.  They
+// then arrive on the stage's sf_ready barrier, on which the MMA lane waits
+// before issuing the stage's 4 MMAs of K = 64.  (Issued from the
+// MMA lane, tcgen05.cp of the same atoms blocked it for about 60 cycles each.)
+// A slot is rewritten only once the stage's smem was refilled, i.e. after the
+// MMAs that read the slot completed.
 // TMEM: accumulators 2 x 128 columns (the epilogue of tile i overlaps the MMAs
 // of tile i+1), scale slots at 256 + 32 s (A: +4m, B: +16+4m).
 //
@@ -27,10 +32,12 @@
 //     g_h: packed codes and MMA-layout scales of every row of the row block.
 //   GEMM2: B = 128 rows of W_down; y = accumulator * g_h * g_w * row weight,
 //     written as fp16 with a power-of-two scale per 32 columns (only the
-//     block's real rows, at their unpadded row index).
+//     block's real rows, at their unpadded row index), staged in shared memory
+//     per warp so that each store instruction writes 16 rows x 32 bytes.
 // Warp roles: warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer, warps
-// 2..5 epilogue (one row per thread).  Persistent CTAs over the device-built
-// tile schedule (heaviest experts first, tiles of one weight block adjacent).
+// 2..5 epilogue (one row per thread), warps 6..9 scale warps.  Persistent CTAs
+// over the device-built tile schedule (heaviest experts first, tiles of one
+// weight block adjacent), which every CTA first copies into shared memory.
 #include <cuda_fp16.h>
 
 #include "moe_internal.h"
@@ -40,7 +47,7 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kRows = 128;                  // token rows per tile
 constexpr int kCols = 128;                  // weight rows per tile
 constexpr int kRowBytes = 128;              // K bytes per stage and row (256 elements)
@@ -56,33 +63,41 @@ constexpr uint32_t kIdesc = ptx::idesc_nvf4(kRows, kCols);
 static_assert(kSfCol + 32 * kStages <= int(kTmemCols), "TMEM budget");
 
 struct __align__(8) SmemCtl {
-  uint64_t full[kStages];
+  uint64_t full[kStages];     // A and B of the stage landed
+  uint64_t sf_full[kStages];  // the stage's scale atoms landed (loaded first)
   uint64_t empty[kStages];
+  uint64_t sf_ready[kStages];
   uint64_t afull[2];
   uint64_t aempty[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  int32_t sched[2 * kMaxGroups + 2];  // copy of the tile schedule
+  int32_t off[kMaxExperts + 1];       // copies of the row offsets and the padded offsets
+  int32_t pad[kMaxExperts + 1];
 };
 
-constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + sizeof(SmemCtl);
+constexpr int kStageOutBytes = 1024;  // per epilogue warp: 32 rows x 32 B of fp16 y
+constexpr size_t kSmemBytes =
+    1024 + size_t(kStages) * kStageBytes + 4 * kStageOutBytes + sizeof(SmemCtl);
 
 struct Tile {
   int g, rb, nb, rows, K;
 };
 
-__device__ __forceinline__ Tile decode_tile(int t, const Nvfp4GemmArgs& a, int G) {
-  const int32_t* ts = a.sched + 1;
+__device__ __forceinline__ Tile decode_tile(int t, const Nvfp4GemmArgs& a, const int32_t* sched,
+                                            const int32_t* off, int G) {
+  const int32_t* ts = sched + 1;
   int lo = 0, hi = G - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(ts + mid) <= t) lo = mid; else hi = mid - 1;
+    if (ts[mid] <= t) lo = mid; else hi = mid - 1;
   }
   Tile x;
-  x.g = __ldg(a.sched + G + 2 + lo);
-  const int local = t - __ldg(ts + lo);
+  x.g = sched[G + 2 + lo];
+  const int local = t - ts[lo];
   const bool routed = x.g < a.E;
-  x.rows = routed ? __ldg(a.offsets + x.g + 1) - __ldg(a.offsets + x.g) : a.T;
+  x.rows = routed ? off[x.g + 1] - off[x.g] : a.T;
   x.K = routed ? a.K_routed : a.K_shared;
   const int mt = (x.rows + kRows - 1) / kRows;
   x.nb = local / mt;
@@ -125,7 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  SmemCtl& c = *reinterpret_cast<SmemCtl*>(smem + kStages * kStageBytes);
+  uint8_t* out_stage = smem + kStages * kStageBytes;
+  SmemCtl& c = *reinterpret_cast<SmemCtl*>(out_stage + 4 * kStageOutBytes);
   auto stage_a = [&](int s) { return smem + s * kStageBytes; };
   auto stage_b = [&](int s) { return smem + s * kStageBytes + kABytes; };
   auto stage_sfa = [&](int s) { return smem + s * kStageBytes + kABytes + kBBytes; };
@@ -140,7 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&c.full[s], 1);
+      ptx::mbar_init(&c.sf_full[s], 1);
       ptx::mbar_init(&c.empty[s], 1);
+      ptx::mbar_init(&c.sf_ready[s], 4);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&c.afull[b], 1);
@@ -154,11 +172,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_alloc(&c.tmem_base, kTmemCols);
     ptx::tmem_relinquish();
   }
+  for (int i = threadIdx.x; i < 2 * G + 2; i += kThreads) c.sched[i] = __ldg(args.sched + i);
+  for (int i = threadIdx.x; i <= args.E; i += kThreads) {
+    c.off[i] = __ldg(args.offsets + i);
+    c.pad[i] = __ldg(args.pad_offsets + i);
+  }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = c.tmem_base;
-  const int num_tiles = __ldg(args.sched);
+  const int num_tiles = c.sched[0];
   volatile int* abort = &c.abort;
 
   if (warp == 0) {
@@ -166,9 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------- TMA producer
       uint32_t it = 0;
       for (int t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
-        const Tile x = decode_tile(t, args, G);
+        const Tile x = decode_tile(t, args, c.sched, c.off, G);
         const bool routed = x.g < args.E;
-        const int prow0 = (routed ? __ldg(args.pad_offsets + x.g) : 0) + x.rb * kRows;
+        const int prow0 = (routed ? c.pad[x.g] : 0) + x.rb * kRows;
         const void* map_a = routed ? static_cast<const void*>(&map_a0)
                                    : static_cast<const void*>(&map_a1);
         const int widx = kGemm1 ? 2 * x.g : x.g;
@@ -182,18 +205,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
           if (!ptx::mbar_wait(&c.empty[s], ph ^ 1, abort, args.err)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(&c.full[s], kStageBytes);
+          // the scale atoms first, on their own barrier: the scale warps move
+          // them into TMEM while A and B are still in flight
+          ptx::mbar_arrive_expect_tx(&c.sf_full[s], 2 * kSfBytes);
+          ptx::bulk_load(stage_sfa(s), asf + ks * kSfBytes, kSfBytes, &c.sf_full[s]);
+          ptx::bulk_load(stage_sfb(s), bsf + ks * kSfBytes, kSfBytes, &c.sf_full[s]);
+          ptx::mbar_arrive_expect_tx(&c.full[s], kABytes + kBBytes);
           ptx::tma_load_2d(stage_a(s), map_a, &c.full[s], ks * kRowBytes, prow0);
           ptx::tma_load_2d(stage_b(s), map_b, &c.full[s], ks * kRowBytes, x.nb * kCols);
-          ptx::bulk_load(stage_sfa(s), asf + ks * kSfBytes, kSfBytes, &c.full[s]);
-          ptx::bulk_load(stage_sfb(s), bsf + ks * kSfBytes, kSfBytes, &c.full[s]);
         }
         if (!ok) break;
       }
       if (*abort) {
         const uint32_t first = it > uint32_t(kStages) ? it - kStages : 0;
-        for (uint32_t j = first; j < it; ++j)
+        for (uint32_t j = first; j < it; ++j) {
+          drain_wait(&c.sf_full[j % kStages], (j / kStages) & 1, args.err);
           drain_wait(&c.full[j % kStages], (j / kStages) & 1, args.err);
+        }
       }
     }
   } else if (warp == 1) {
@@ -201,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------- MMA issuer
       uint32_t it = 0, tc = 0;
       for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tc) {
-        const Tile x = decode_tile(t, args, G);
+        const Tile x = decode_tile(t, args, c.sched, c.off, G);
         const int buf = tc & 1;
         const uint32_t bph = (tc >> 1) & 1;
         if (!ptx::mbar_wait(&c.aempty[buf], bph ^ 1, abort, args.err)) break;
@@ -212,15 +240,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ks = 0; ks < ks_n; ++ks, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
+          // data in smem, scales in TMEM
           if (!ptx::mbar_wait(&c.full[s], ph, abort, args.err)) { ok = false; break; }
+          if (!ptx::mbar_wait(&c.sf_ready[s], ph, abort, args.err)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t slot = tmem_base + kSfCol + 32 * s;
-          const uint32_t sa = ptx::smem_u32(stage_sfa(s)), sb = ptx::smem_u32(stage_sfb(s));
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            ptx::tmem_cp_sf(slot + 4 * m, ptx::sf_atom_desc(sa + 512 * m));
-            ptx::tmem_cp_sf(slot + 16 + 4 * m, ptx::sf_atom_desc(sb + 512 * m));
-          }
           const uint64_t da = ptx::sw128_desc(ptx::smem_u32(stage_a(s)));
           const uint64_t db = ptx::sw128_desc(ptx::smem_u32(stage_b(s)));
 #pragma unroll
@@ -235,6 +259,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mma_commit(&c.drain);
       drain_wait(&c.drain, 0, args.err);
     }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------ scale warps (6..9)
+    const int q = warp & 3;  // TMEM lane quarter of this warp
+    const uint32_t lane_q = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t it = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      const Tile x = decode_tile(t, args, c.sched, c.off, G);
+      const int ks_n = x.K / 256;
+      bool ok = true;
+      for (int ks = 0; ks < ks_n; ++ks, ++it) {
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1;
+        if (!ptx::mbar_wait(&c.sf_full[s], ph, abort, args.err)) { ok = false; break; }
+        const uint32_t slot = tmem_base + kSfCol + 32 * s;
+        // every lane quarter gets the whole atom layout: lane j, column 4m + i
+        // holds the scales of row 32i + j for MMA m (A at +0, B at +16)
+#pragma unroll
+        for (int ab = 0; ab < 2; ++ab) {
+          const uint8_t* src = (ab ? stage_sfb(s) : stage_sfa(s)) + lane * 16;
+          uint32_t v[16];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const uint4 w = *reinterpret_cast<const uint4*>(src + 512 * m);
+            v[4 * m] = w.x;
+            v[4 * m + 1] = w.y;
+            v[4 * m + 2] = w.z;
+            v[4 * m + 3] = w.w;
+          }
+          ptx::tmem_st16(slot + lane_q + 16 * ab, v);
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&c.sf_ready[s]);
+      }
+      if (!ok) break;
+    }
   } else {
     // ------------------------------------------------------ epilogue (warps 2..5)
     const int q = warp & 3;
@@ -243,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float gh = __ldg(args.act_scales + 2 * layer + 1);
     uint32_t tc = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tc) {
-      const Tile x = decode_tile(t, args, G);
+      const Tile x = decode_tile(t, args, c.sched, c.off, G);
       const bool routed = x.g < args.E;
       const int buf = tc & 1;
       const uint32_t bph = (tc >> 1) & 1;
@@ -265,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // columns [0,64) gate, [64,128) up of h columns [64 nb, 64 nb + 64)
         const float alpha = __fmul_rn(gx, gw);
         const int n_h = routed ? args.N_routed : args.N_shared;  // I or I_shared
-        const int64_t p = (routed ? __ldg(args.pad_offsets + x.g) : 0) + int64_t(x.rb) * kRows + r;
+        const int64_t p = (routed ? c.pad[x.g] : 0) + int64_t(x.rb) * kRows + r;
         uint8_t* codes = static_cast<uint8_t*>(routed ? args.out0 : args.out1) + p * (n_h / 2) + x.nb * 32;
         uint8_t* sf = routed ? args.out_sf0 : args.out_sf1;
 #pragma unroll
@@ -288,36 +349,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float alpha = __fmul_rn(gh, gw);
         const int n_out = args.N_routed;  // H
         const int valid_rows = x.rows - x.rb * kRows;
-        if (r < valid_rows) {
-          const int64_t row = (routed ? int64_t(__ldg(args.offsets + x.g)) : 0) +
-                              int64_t(x.rb) * kRows + r;
-          const float w = (routed && args.row_weight) ? args.row_weight[row] : 1.0f;
-          const float wa = w * alpha;
-          __half* y = static_cast<__half*>(routed ? args.out0 : args.out1) + row * n_out + x.nb * kCols;
-          float* ys = (routed ? args.out_scales0 : args.out_scales1) + row * (n_out / 32) + x.nb * 4;
+        // rows of this warp: tile rows 32q .. 32q + 31 (lane = row), output row
+        // of lane 0 and how many of the warp's rows exist
+        const int64_t wrow0 = (routed ? int64_t(c.off[x.g]) : 0) + int64_t(x.rb) * kRows + q * 32;
+        const int valid_w = valid_rows - q * 32;
+        const bool valid = lane < valid_w;
+        const float w = (valid && routed && args.row_weight) ? args.row_weight[wrow0 + lane] : 1.0f;
+        const float wa = w * alpha;
+        __half* y = static_cast<__half*>(routed ? args.out0 : args.out1) + x.nb * kCols;
+        float* ys = (routed ? args.out_scales0 : args.out_scales1) + x.nb * 4;
+        uint4* stg = reinterpret_cast<uint4*>(out_stage + (warp - 2) * kStageOutBytes);
+        const int swz = (lane >> 2) & 1;
 #pragma unroll
-          for (int cb = 0; cb < 4; ++cb) {
-            float amax = 0.0f;
+        for (int cb = 0; cb < 4; ++cb) {
+          float amax = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(wa * __uint_as_float(acc[cb][j])));
-            // fp16 with a power-of-two scale s = 2^(floor(log2 amax) - 14): |y| / s < 2^15
-            int sb = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 14;
-            sb = sb < 1 ? 1 : sb;
-            const float scale = __uint_as_float(static_cast<uint32_t>(sb) << 23);
-            const float inv = __uint_as_float(static_cast<uint32_t>(254 - sb) << 23);
+          for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(wa * __uint_as_float(acc[cb][j])));
+          // fp16 with a power-of-two scale s = 2^(floor(log2 amax) - 14): |y| / s < 2^15
+          int sb = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 14;
+          sb = sb < 1 ? 1 : sb;
+          const float scale = __uint_as_float(static_cast<uint32_t>(sb) << 23);
+          const float inv = __uint_as_float(static_cast<uint32_t>(254 - sb) << 23);
+          if (valid) ys[(wrow0 + lane) * (n_out / 32) + cb] = scale;
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint32_t pk[4];
+          for (int hf = 0; hf < 2; ++hf) {
+            // 16 columns of this lane's row -> 32 B in the warp's staging buffer
+            uint32_t pk[8];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int i = v * 8 + e * 2;
-                const __half2 hh = __floats2half2_rn(wa * __uint_as_float(acc[cb][i]) * inv,
-                                                     wa * __uint_as_float(acc[cb][i + 1]) * inv);
-                pk[e] = *reinterpret_cast<const uint32_t*>(&hh);
-              }
-              *reinterpret_cast<uint4*>(y + cb * 32 + v * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            for (int e = 0; e < 8; ++e) {
+              const int i = hf * 16 + e * 2;
+              const __half2 hh = __floats2half2_rn(wa * __uint_as_float(acc[cb][i]) * inv,
+                                                   wa * __uint_as_float(acc[cb][i + 1]) * inv);
+              pk[e] = *reinterpret_cast<const uint32_t*>(&hh);
             }
-            ys[cb] = scale;
+            stg[lane * 2 + swz] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            stg[lane * 2 + (swz ^ 1)] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            __syncwarp();
+            // read back transposed: each store instruction writes 16 rows x 32 B
+#pragma unroll
+            for (int it2 = 0; it2 < 2; ++it2) {
+              const int i = it2 * 16 + (lane >> 1), vv = lane & 1;
+              const uint4 val = stg[i * 2 + (vv ^ ((i >> 2) & 1))];
+              if (i < valid_w)
+                *reinterpret_cast<uint4*>(y + (wrow0 + i) * n_out + cb * 32 + hf * 16 + vv * 8) = val;
+            }
+            __syncwarp();
           }
         }
       }
