@@ -133,7 +133,7 @@ typedef struct moe_config {
  * NVFP4 (MOE_DTYPE_NVFP4), as written by moe_quantize_weight_nvfp4:
  *   gate[e]         the expert's stacked gate/up matrix, E2M1 codes [2I, H/2]
  *                   bytes (two values per byte, the even element in the low
- *                   nibble), rows interleaved in 64-row blocks [gate 64 | up 64];
+ *                   nibble), rows interleaved in 128-row blocks [gate 128 | up 128];
  *                   up[] and the *_scales arrays are unused (may be NULL)
  *   down[e]         E2M1 codes [H, I/2]
  *   gate_sf[e], down_sf[e]   their e4m3 block scales in the MMA scale layout
@@ -353,8 +353,8 @@ MOE_API moe_status_t moe_quantize_act_fp8(const void* x, int64_t M, int64_t K, u
  * Data Parallelism for High-Performance LLM Inference on NVL72", section A4,
  * experimental setup).  w: bf16 [N, K]; w2: NULL, or a second bf16 [N, K]
  * matrix stacked with w (an expert's up projection next to its gate), in
- * which case the output has 2N rows interleaved in 64-row blocks
- * [w rows 64b..64b+63 | w2 rows 64b..64b+63].  Computed in fp32:
+ * which case the output has 2N rows interleaved in 128-row blocks
+ * [w rows 128b..128b+127 | w2 rows 128b..128b+127].  Computed in fp32:
  *   g = amax / (6 * 448) over the whole (stacked) matrix (1 if all zero),
  *   per 16 consecutive elements of a row: s = e4m3_rn_satfinite(amax_b / (6 g)),
  *   q = E2M1 round-to-nearest-even, saturating at 6, of x / (s g)  (q = 0 if s g = 0).
@@ -364,7 +364,7 @@ MOE_API moe_status_t moe_quantize_act_fp8(const void* x, int64_t M, int64_t K, u
  *               block b) is byte ((r/128) * (K/64) + b/4) * 512 + (r%32) * 16
  *               + ((r%128)/32) * 4 + b%4
  *   tensor_scale  device fp32, receives g
- * N a multiple of 128 (of 64 with w2), K of 64.  Asynchronous; tensor_scale is
+ * N a multiple of 128, K of 64.  Asynchronous; tensor_scale is
  * used as scratch until the call's last kernel has run. */
 MOE_API moe_status_t moe_quantize_weight_nvfp4(const void* w, const void* w2, int64_t N, int64_t K,
                                                uint8_t* codes, uint8_t* sf, float* tensor_scale,

@@ -172,7 +172,7 @@ class Nvfp4ExpertWeights:
     """NVFP4 expert weights (MOE_DTYPE_NVFP4) -> device descriptor table.
 
     Per expert e: ``gate_up[e]`` uint8 [2I, H/2] (stacked gate/up E2M1 codes,
-    rows interleaved in 64-row blocks), ``down[e]`` uint8 [H, I/2], their
+    rows interleaved in 128-row blocks), ``down[e]`` uint8 [H, I/2], their
     MMA-layout block scales ``gate_up_sf[e]`` / ``down_sf[e]`` (uint8, rows*K/16
     bytes) and fp32 tensor scales ``gate_up_ts`` / ``down_ts`` (device float32
     tensors [E]: entry e is expert e's).  ``shared`` = (gate_up, down,
@@ -480,7 +480,7 @@ def moe_quantize_act_fp8(x, stream=None):
 
 def moe_quantize_weight_nvfp4(w, w2=None, tensor_scale=None, stream=None):
     """NVFP4 weights (moe_quantize_weight_nvfp4): bf16 [N, K] (w2: a second
-    [N, K] matrix stacked with w, rows interleaved in 64-row blocks) ->
+    [N, K] matrix stacked with w, rows interleaved in 128-row blocks) ->
     (codes uint8 [rows, K/2], MMA-layout scales uint8 [rows*K/16], tensor scale
     float32 [1], or written into ``tensor_scale`` (a float32 view of one element))."""
     Nr, K = w.shape

@@ -521,8 +521,8 @@ static moe_status_t encode_layer(const moe_config_t* cfg, const moe_weight_list_
 }
 
 // NVFP4: GEMM1 descriptor of group g at 2g (the stacked gate/up codes, 2I x H/2
-// bytes; 2g+1 repeats it), GEMM2 at 2G+g (down codes, H x I/2 bytes); boxes of
-// 128 rows x 128 bytes.  scales[] hold the MMA-layout scale bytes, gs[] the
+// bytes, boxes of 256 rows x 128 bytes; 2g+1 repeats it), GEMM2 at 2G+g (down
+// codes, H x I/2 bytes, boxes of 128 rows x 128 bytes).  scales[] hold the MMA-layout scale bytes, gs[] the
 // tensor-scale pointers (same indexing); act[0..1] = g_x, g_h.
 static moe_status_t encode_layer_nvfp4(const moe_config_t* cfg, const moe_weight_list_t* wl,
                                        CUtensorMap* maps, const float** scales, const float** gs,
@@ -569,7 +569,7 @@ static moe_status_t encode_layer_nvfp4(const moe_config_t* cfg, const moe_weight
     const uint64_t inter = sh ? Is : I;
     const void* wgu = sh ? wl->shared_gate : wl->gate[g];
     const void* wd = sh ? wl->shared_down : wl->down[g];
-    MOE_TRY(encode_2d(&m1[2 * g], false, wgu, H / 2, 2 * inter, 128, kNvfp4Rows));
+    MOE_TRY(encode_2d(&m1[2 * g], false, wgu, H / 2, 2 * inter, 128, 2 * kNvfp4Rows));
     m1[2 * g + 1] = m1[2 * g];
     MOE_TRY(encode_2d(&m2[g], false, wd, inter / 2, H, 128, kNvfp4Rows));
     scales[2 * g] = static_cast<const float*>(sh ? wl->shared_gate_sf : wl->gate_sf[g]);
@@ -978,8 +978,8 @@ static moe_status_t run_nvfp4(const moe_config_t& c, const WeightView& W, const 
   uint8_t* hs = at<uint8_t*>(ws, L.hs);
   uint8_t* h_sf = at<uint8_t*>(ws, L.h_sc);
   uint8_t* hs_sf = at<uint8_t*>(ws, L.hs_sc);
-  // GEMM1 tiles: 64 h columns (128 stacked gate/up rows); GEMM2 tiles: 128 y columns
-  const int n1r = c.I / 64, n1s = c.I_shared / 64, n2 = c.H / kNvfp4Rows;
+  // GEMM1 tiles: 128 h columns (256 stacked gate/up rows); GEMM2 tiles: 128 y columns
+  const int n1r = c.I / 128, n1s = c.I_shared / 128, n2 = c.H / kNvfp4Rows;
   trace_mark(st, MOE_K_PLAN);
   MOE_CUDA(launch_plan(offsets, c.E, shared ? 1 : 0, c.T, n1r, n1s, n2, n2, s1, s2, kNvfp4Rows,
                        kNvfp4Rows, st));
@@ -1331,9 +1331,9 @@ moe_status_t moe_quantize_act_fp8(const void* x, int64_t M, int64_t K, uint8_t* 
 moe_status_t moe_quantize_weight_nvfp4(const void* w, const void* w2, int64_t N, int64_t K,
                                        uint8_t* codes, uint8_t* sf, float* tensor_scale,
                                        moe_stream_t stream) {
-  if (N <= 0 || K <= 0 || K % 64 || (w2 ? N % 64 : N % 128))
+  if (N <= 0 || K <= 0 || K % 64 || N % 128)
     return fail(MOE_ERR_INVALID_ARG,
-                "NVFP4 weights need K a positive multiple of 64 and N of 128 (of 64 with w2)");
+                "NVFP4 weights need K a positive multiple of 64 and N of 128");
   MOE_TRY(check_ptr(w, "w"));
   if (w2) MOE_TRY(check_ptr(w2, "w2"));
   MOE_TRY(check_ptr(codes, "codes"));

@@ -7,37 +7,43 @@
 // Weight Data Parallelism for High-Performance LLM Inference on NVL72",
 // section 4.2.
 //
-// Tile: 128 token rows (UMMA M) x 128 weight rows (UMMA N), K in stages of 256
-// elements (128 bytes per row).  Each expert's rows are padded to a multiple
-// of 128 in the permuted buffers, so a tile is one aligned row block and its
-// scales are whole 512-byte atoms (see nvfp4.cuh, sf_offset).
-//   stage = A 16 KB | B 16 KB | A scales 2 KB | B scales 2 KB  (6 stages)
-// A and B arrive by TMA (128-byte swizzle), the scale atoms by 1-D bulk copies.
-// Four scale warps, one per TMEM lane quarter, move each stage's scales from
-// shared memory into that stage's TMEM scale slot with tcgen05.st, in the
-// layout the block-scaled MMA reads for 128 rows: lane j (of every quarter),
-// column 4m + i holds the four K-block scales of row 32i + j for MMA m.  They
-// then arrive on the stage's sf_ready barrier, on which the MMA lane waits
-// before issuing the stage's 4 MMAs of K = 64.  (Issued from the
-// MMA lane, tcgen05.cp of the same atoms blocked it for about 60 cycles each.)
-// A slot is rewritten only once the stage's smem was refilled, i.e. after the
-// MMAs that read the slot completed.
-// TMEM: accumulators 2 x 128 columns (the epilogue of tile i overlaps the MMAs
-// of tile i+1), scale slots at 256 + 32 s (A: +4m, B: +16+4m).
+// A tile is 128 token rows (UMMA M) x 128 W weight rows (UMMA N = 128 W), K in
+// stages of 256 elements (128 bytes per row).  Each expert's rows are padded to
+// a multiple of 128 in the permuted buffers, so a tile is one aligned row block
+// and its scales are whole 512-byte atoms (see nvfp4.cuh, sf_offset).
+//   stage = A 16 KB | B 16 W KB | A scales 2 KB | B scales 2 W KB
+// A block-scaled MMA of M = 128 costs the same ~135 cycles for N = 128 and
+// N = 256, so GEMM1 (K = H, long) uses W = 2: one MMA per K = 64 covers 256
+// weight rows, with a single 256-column accumulator (TMEM cannot hold two next
+// to the scale slots) that 8 epilogue warps drain quickly.  GEMM2 (K = I,
+// short) keeps W = 1 with two 128-column accumulators, so that its epilogue
+// overlaps the next tile's MMAs.
+// A and B arrive by TMA (128-byte swizzle), the scale atoms by 1-D bulk copies
+// on their own barrier, issued first.  Four scale warps, one per TMEM lane
+// quarter, move each stage's scales into that stage's TMEM scale slot with
+// tcgen05.st, in the layout the MMA reads for 128 rows: lane j (of every
+// quarter), column c + i holds the four K-block scales of row 32i + j (A: 4
+// columns per MMA, B: 4 W).  They then arrive on the stage's sf_ready barrier,
+// on which the MMA lane waits before issuing the stage's 4 MMAs of K = 64.
+// (Issued from the MMA lane, tcgen05.cp of the same atoms blocked it for about
+// 60 cycles each.)  A slot is rewritten only once the stage's smem was
+// refilled, i.e. after the MMAs that read the slot completed.
+// TMEM: accumulators in columns [0, 256), scale slots from column 256.
 //
-//   GEMM1 (kGemm1): B = 128 rows of the expert's stacked gate/up matrix, whose
-//     rows are interleaved in 64-row blocks [gate 64 | up 64]: tile n holds the
-//     gate and up rows of h columns [64 n, 64 n + 64).  h = silu(g) * u with
-//     g, u = accumulator * g_x * g_w, quantised to NVFP4 with the static scale
-//     g_h: packed codes and MMA-layout scales of every row of the row block.
+//   GEMM1 (kGemm1): B = 256 rows of the expert's stacked gate/up matrix, whose
+//     rows are interleaved in 128-row blocks [gate 128 | up 128]: tile n holds
+//     the gate and up rows of h columns [128 n, 128 n + 128).  h = silu(g) * u
+//     with g, u = accumulator * g_x * g_w, quantised to NVFP4 with the static
+//     scale g_h: packed codes and MMA-layout scales of every row of the block.
 //   GEMM2: B = 128 rows of W_down; y = accumulator * g_h * g_w * row weight,
 //     written as fp16 with a power-of-two scale per 32 columns (only the
 //     block's real rows, at their unpadded row index), staged in shared memory
 //     per warp so that each store instruction writes 16 rows x 32 bytes.
-// Warp roles: warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer, warps
-// 2..5 epilogue (one row per thread), warps 6..9 scale warps.  Persistent CTAs
-// over the device-built tile schedule (heaviest experts first, tiles of one
-// weight block adjacent), which every CTA first copies into shared memory.
+// Warp roles: warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer, then
+// the epilogue warps (one row per thread; GEMM1: two warps per lane quarter,
+// one per 64-column half), then the 4 scale warps.  Persistent CTAs over the
+// device-built tile schedule (heaviest experts first, tiles of one weight
+// block adjacent), which every CTA first copies into shared memory.
 #include <cuda_fp16.h>
 
 #include "moe_internal.h"
@@ -47,26 +53,41 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 320;
 constexpr int kRows = 128;                  // token rows per tile
-constexpr int kCols = 128;                  // weight rows per tile
 constexpr int kRowBytes = 128;              // K bytes per stage and row (256 elements)
 constexpr int kABytes = kRows * kRowBytes;  // 16 KB
-constexpr int kBBytes = kCols * kRowBytes;  // 16 KB
-constexpr int kSfBytes = 2048;              // 4 atoms of 512 bytes (4 MMAs of K = 64)
-constexpr int kStageBytes = kABytes + kBBytes + 2 * kSfBytes;
-constexpr int kStages = 6;
+constexpr int kSfaBytes = 2048;             // 4 atoms of 512 bytes (4 MMAs of K = 64)
 constexpr uint32_t kTmemCols = 512;
-constexpr int kAccCols = 128;
 constexpr int kSfCol = 256;                 // first scale slot
-constexpr uint32_t kIdesc = ptx::idesc_nvf4(kRows, kCols);
-static_assert(kSfCol + 32 * kStages <= int(kTmemCols), "TMEM budget");
+constexpr int kStageOutBytes = 1024;        // GEMM2, per epilogue warp: 32 rows x 32 B of fp16 y
 
+template <bool kGemm1>
+struct Cfg {
+  static constexpr int W = kGemm1 ? 2 : 1;           // 128-row weight blocks per tile
+  static constexpr int kCols = 128 * W;              // UMMA N
+  static constexpr int kBBytes = kCols * kRowBytes;
+  static constexpr int kSfbBytes = 2048 * W;
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr int kStages = kGemm1 ? 4 : 6;
+  static constexpr int kAccBufs = kGemm1 ? 1 : 2;
+  static constexpr int kAccCols = kCols;
+  static constexpr int kEpiWarps = kGemm1 ? 8 : 4;
+  static constexpr int kSfWarp0 = 2 + kEpiWarps;    // first scale warp
+  static constexpr int kThreads = 32 * (kSfWarp0 + 4);
+  static constexpr int kSlotCols = 16 + 16 * W;      // A scales 16, B scales 16 W
+  static constexpr int kOutBytes = kGemm1 ? 0 : 4 * kStageOutBytes;
+  static constexpr uint32_t kIdesc = ptx::idesc_nvf4(kRows, kCols);
+  static_assert(kAccBufs * kAccCols <= kSfCol, "accumulators below the scale slots");
+  static_assert(kSfCol + kSlotCols * kStages <= int(kTmemCols), "TMEM budget");
+};
+
+template <bool kGemm1>
 struct __align__(8) SmemCtl {
-  uint64_t full[kStages];     // A and B of the stage landed
-  uint64_t sf_full[kStages];  // the stage's scale atoms landed (loaded first)
-  uint64_t empty[kStages];
-  uint64_t sf_ready[kStages];
+  static constexpr int S = Cfg<kGemm1>::kStages;
+  uint64_t full[S];     // A and B of the stage landed
+  uint64_t sf_full[S];  // the stage's scale atoms landed (loaded first)
+  uint64_t empty[S];
+  uint64_t sf_ready[S];
   uint64_t afull[2];
   uint64_t aempty[2];
   uint64_t drain;
@@ -77,9 +98,11 @@ struct __align__(8) SmemCtl {
   int32_t pad[kMaxExperts + 1];
 };
 
-constexpr int kStageOutBytes = 1024;  // per epilogue warp: 32 rows x 32 B of fp16 y
-constexpr size_t kSmemBytes =
-    1024 + size_t(kStages) * kStageBytes + 4 * kStageOutBytes + sizeof(SmemCtl);
+template <bool kGemm1>
+constexpr size_t smem_bytes() {
+  using C = Cfg<kGemm1>;
+  return 1024 + size_t(C::kStages) * C::kStageBytes + C::kOutBytes + sizeof(SmemCtl<kGemm1>);
+}
 
 struct Tile {
   int g, rb, nb, rows, K;
@@ -115,17 +138,18 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint3
   }
 }
 
-// Barrier over the 4 epilogue warps that also ORs `v` over them, so that a
+// Barrier over the epilogue warps that also ORs `v` over them, so that a
 // decision to stop is taken by all of them together.
+template <int kEpiThreads>
 __device__ __forceinline__ bool epi_any(bool v) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(static_cast<uint32_t>(v))
+      : "r"(static_cast<uint32_t>(v)), "n"(kEpiThreads)
       : "memory");
   return r != 0;
 }
@@ -133,19 +157,25 @@ __device__ __forceinline__ bool epi_any(bool v) {
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 template <bool kGemm1>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<kGemm1>::kThreads, 1)
     grouped_gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap map_a0,
                               const __grid_constant__ CUtensorMap map_a1,
                               const Nvfp4GemmArgs args) {
+  using C = Cfg<kGemm1>;
+  constexpr int kStages = C::kStages;
+  constexpr int kStageBytes = C::kStageBytes;
+  constexpr int kThreads = C::kThreads;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* out_stage = smem + kStages * kStageBytes;
-  SmemCtl& c = *reinterpret_cast<SmemCtl*>(out_stage + 4 * kStageOutBytes);
+  SmemCtl<kGemm1>& c = *reinterpret_cast<SmemCtl<kGemm1>*>(out_stage + C::kOutBytes);
   auto stage_a = [&](int s) { return smem + s * kStageBytes; };
   auto stage_b = [&](int s) { return smem + s * kStageBytes + kABytes; };
-  auto stage_sfa = [&](int s) { return smem + s * kStageBytes + kABytes + kBBytes; };
-  auto stage_sfb = [&](int s) { return smem + s * kStageBytes + kABytes + kBBytes + kSfBytes; };
+  auto stage_sfa = [&](int s) { return smem + s * kStageBytes + kABytes + C::kBBytes; };
+  auto stage_sfb = [&](int s) {
+    return smem + s * kStageBytes + kABytes + C::kBBytes + kSfaBytes;
+  };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -162,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&c.afull[b], 1);
-      ptx::mbar_init(&c.aempty[b], 4);
+      ptx::mbar_init(&c.aempty[b], C::kEpiWarps);
     }
     ptx::mbar_init(&c.drain, 1);
     c.abort = 0;
@@ -198,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* map_b = args.w_maps + tab + widx;
         const int atoms = x.K / 64;  // scale atoms per 128-row block
         const uint8_t* asf = (routed ? args.a_sf0 : args.a_sf1) + int64_t(prow0 / kRows) * atoms * 512;
-        const uint8_t* bsf = args.w_sf[tab + widx] + int64_t(x.nb) * atoms * 512;
+        const uint8_t* bsf = args.w_sf[tab + widx] + int64_t(C::W * x.nb) * atoms * 512;
         const int ks_n = x.K / 256;
         bool ok = true;
         for (int ks = 0; ks < ks_n; ++ks, ++it) {
@@ -207,12 +237,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ptx::mbar_wait(&c.empty[s], ph ^ 1, abort, args.err)) { ok = false; break; }
           // the scale atoms first, on their own barrier: the scale warps move
           // them into TMEM while A and B are still in flight
-          ptx::mbar_arrive_expect_tx(&c.sf_full[s], 2 * kSfBytes);
-          ptx::bulk_load(stage_sfa(s), asf + ks * kSfBytes, kSfBytes, &c.sf_full[s]);
-          ptx::bulk_load(stage_sfb(s), bsf + ks * kSfBytes, kSfBytes, &c.sf_full[s]);
-          ptx::mbar_arrive_expect_tx(&c.full[s], kABytes + kBBytes);
+          ptx::mbar_arrive_expect_tx(&c.sf_full[s], kSfaBytes + C::kSfbBytes);
+          ptx::bulk_load(stage_sfa(s), asf + ks * kSfaBytes, kSfaBytes, &c.sf_full[s]);
+#pragma unroll
+          for (int h = 0; h < C::W; ++h)  // the tile's 128-row weight blocks
+            ptx::bulk_load(stage_sfb(s) + h * 2048, bsf + (int64_t(h) * atoms + 4 * ks) * 512, 2048,
+                           &c.sf_full[s]);
+          ptx::mbar_arrive_expect_tx(&c.full[s], kABytes + C::kBBytes);
           ptx::tma_load_2d(stage_a(s), map_a, &c.full[s], ks * kRowBytes, prow0);
-          ptx::tma_load_2d(stage_b(s), map_b, &c.full[s], ks * kRowBytes, x.nb * kCols);
+          ptx::tma_load_2d(stage_b(s), map_b, &c.full[s], ks * kRowBytes, x.nb * C::kCols);
         }
         if (!ok) break;
       }
@@ -230,11 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, tc = 0;
       for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tc) {
         const Tile x = decode_tile(t, args, c.sched, c.off, G);
-        const int buf = tc & 1;
-        const uint32_t bph = (tc >> 1) & 1;
+        const int buf = tc % C::kAccBufs;
+        const uint32_t bph = (tc / C::kAccBufs) & 1;
         if (!ptx::mbar_wait(&c.aempty[buf], bph ^ 1, abort, args.err)) break;
         ptx::tc_fence_after();
-        const uint32_t d = tmem_base + buf * kAccCols;
+        const uint32_t d = tmem_base + buf * C::kAccCols;
         const int ks_n = x.K / 256;
         bool ok = true;
         for (int ks = 0; ks < ks_n; ++ks, ++it) {
@@ -244,13 +277,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ptx::mbar_wait(&c.full[s], ph, abort, args.err)) { ok = false; break; }
           if (!ptx::mbar_wait(&c.sf_ready[s], ph, abort, args.err)) { ok = false; break; }
           ptx::tc_fence_after();
-          const uint32_t slot = tmem_base + kSfCol + 32 * s;
+          const uint32_t slot = tmem_base + kSfCol + C::kSlotCols * s;
           const uint64_t da = ptx::sw128_desc(ptx::smem_u32(stage_a(s)));
           const uint64_t db = ptx::sw128_desc(ptx::smem_u32(stage_b(s)));
 #pragma unroll
           for (int m = 0; m < 4; ++m)
-            ptx::mma_nvf4(d, da + 2 * m, db + 2 * m, kIdesc, slot + 4 * m, slot + 16 + 4 * m,
-                          (ks | m) != 0);
+            ptx::mma_nvf4(d, da + 2 * m, db + 2 * m, C::kIdesc, slot + 4 * m,
+                          slot + 16 + 4 * C::W * m, (ks | m) != 0);
           ptx::mma_commit(&c.empty[s]);
         }
         if (!ok) break;
@@ -259,8 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mma_commit(&c.drain);
       drain_wait(&c.drain, 0, args.err);
     }
-  } else if (warp >= 6) {
-    // ------------------------------------------------------ scale warps (6..9)
+  } else if (warp >= C::kSfWarp0) {
+    // ------------------------------------------------------ scale warps
     const int q = warp & 3;  // TMEM lane quarter of this warp
     const uint32_t lane_q = static_cast<uint32_t>(q * 32) << 16;
     uint32_t it = 0;
@@ -272,12 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1;
         if (!ptx::mbar_wait(&c.sf_full[s], ph, abort, args.err)) { ok = false; break; }
-        const uint32_t slot = tmem_base + kSfCol + 32 * s;
-        // every lane quarter gets the whole atom layout: lane j, column 4m + i
-        // holds the scales of row 32i + j for MMA m (A at +0, B at +16)
-#pragma unroll
-        for (int ab = 0; ab < 2; ++ab) {
-          const uint8_t* src = (ab ? stage_sfb(s) : stage_sfa(s)) + lane * 16;
+        const uint32_t slot = tmem_base + kSfCol + C::kSlotCols * s;
+        // every lane quarter gets the whole atom layout: lane j, column
+        // 4 (W) m + i holds the scales of row 32i + j for MMA m (A at +0, B at +16)
+        {
+          const uint8_t* src = stage_sfa(s) + lane * 16;
           uint32_t v[16];
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
@@ -287,7 +319,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[4 * m + 2] = w.z;
             v[4 * m + 3] = w.w;
           }
-          ptx::tmem_st16(slot + lane_q + 16 * ab, v);
+          ptx::tmem_st16(slot + lane_q, v);
+        }
+#pragma unroll
+        for (int h = 0; h < C::W; ++h) {
+          // B rows 128 h + 32 i + j of MMA m -> column 16 + 4 W m + 4 h + i
+          const uint8_t* src = stage_sfb(s) + h * 2048 + lane * 16;
+          uint32_t v[16];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const uint4 w = *reinterpret_cast<const uint4*>(src + 512 * m);
+            v[4 * m] = w.x;
+            v[4 * m + 1] = w.y;
+            v[4 * m + 2] = w.z;
+            v[4 * m + 3] = w.w;
+          }
+          if constexpr (C::W == 1) {
+            ptx::tmem_st16(slot + lane_q + 16, v);
+          } else {
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+              ptx::tmem_st4(slot + lane_q + 16 + 8 * m + 4 * h, v[4 * m], v[4 * m + 1],
+                            v[4 * m + 2], v[4 * m + 3]);
+          }
         }
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
@@ -297,55 +351,80 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
     }
   } else {
-    // ------------------------------------------------------ epilogue (warps 2..5)
+    // ------------------------------------------------------ epilogue warps
     const int q = warp & 3;
     const int r = q * 32 + lane;  // row of the tile (TMEM lane)
+    const int half = (warp - 2) / 4;  // GEMM1: which 64 of the tile's 128 h columns
     const float gx = __ldg(args.act_scales + 2 * layer);
     const float gh = __ldg(args.act_scales + 2 * layer + 1);
     uint32_t tc = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tc) {
       const Tile x = decode_tile(t, args, c.sched, c.off, G);
       const bool routed = x.g < args.E;
-      const int buf = tc & 1;
-      const uint32_t bph = (tc >> 1) & 1;
+      const int buf = tc % C::kAccBufs;
+      const uint32_t bph = (tc / C::kAccBufs) & 1;
       const bool ok = ptx::mbar_wait(&c.afull[buf], bph, abort, args.err);
-      if (epi_any(!ok || *abort)) break;  // uniform over the epilogue warps
+      if (epi_any<32 * C::kEpiWarps>(!ok || *abort)) break;  // uniform over the epilogue warps
       ptx::tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kAccCols;
-      uint32_t acc[4][32];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) ptx::tmem_ld32(taddr + 32 * j, acc[j]);
-      ptx::tmem_ld_wait();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&c.aempty[buf]);  // accumulator free for tile i+2
-
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::kAccCols;
       const int widx = kGemm1 ? 2 * x.g : x.g;
-      const float gw = *args.w_gs[tab + widx];
       if constexpr (kGemm1) {
-        // columns [0,64) gate, [64,128) up of h columns [64 nb, 64 nb + 64)
-        const float alpha = __fmul_rn(gx, gw);
+        // accumulator columns [0,128) gate, [128,256) up of h columns
+        // [128 nb, 128 nb + 128); this warp: h columns 64 half + [0, 64), in
+        // two chunks of 32, the single accumulator released once both are read
+        float h[2][32];
+        {
+          uint32_t g0[32], u0[32];
+          ptx::tmem_ld32(taddr + 64 * half, g0);
+          ptx::tmem_ld32(taddr + 128 + 64 * half, u0);
+          ptx::tmem_ld_wait();
+          uint32_t g1[32], u1[32];
+          ptx::tmem_ld32(taddr + 64 * half + 32, g1);
+          ptx::tmem_ld32(taddr + 128 + 64 * half + 32, u1);
+          const float alpha = __fmul_rn(gx, *args.w_gs[tab + widx]);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            h[0][i] = silu_f(__uint_as_float(g0[i]) * alpha) * (__uint_as_float(u0[i]) * alpha);
+          ptx::tmem_ld_wait();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&c.aempty[buf]);  // accumulator free
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            h[1][i] = silu_f(__uint_as_float(g1[i]) * alpha) * (__uint_as_float(u1[i]) * alpha);
+        }
         const int n_h = routed ? args.N_routed : args.N_shared;  // I or I_shared
         const int64_t p = (routed ? c.pad[x.g] : 0) + int64_t(x.rb) * kRows + r;
-        uint8_t* codes = static_cast<uint8_t*>(routed ? args.out0 : args.out1) + p * (n_h / 2) + x.nb * 32;
+        uint8_t* codes = static_cast<uint8_t*>(routed ? args.out0 : args.out1) + p * (n_h / 2) +
+                         x.nb * 64 + half * 32;
         uint8_t* sf = routed ? args.out_sf0 : args.out_sf1;
+        uint32_t scw = 0;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          float h[2][16];
+          float b0[16], b1[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float gv = __uint_as_float(acc[hh][i]) * alpha;
-            const float uv = __uint_as_float(acc[2 + hh][i]) * alpha;
-            h[i >> 4][i & 15] = silu_f(gv) * uv;
+          for (int i = 0; i < 16; ++i) {
+            b0[i] = h[hh][i];
+            b1[i] = h[hh][16 + i];
           }
           uint2 q0, q1;
-          const uint32_t s0 = nvfp4::quantize16(h[0], gh, q0);
-          const uint32_t s1 = nvfp4::quantize16(h[1], gh, q1);
+          const uint32_t s0 = nvfp4::quantize16(b0, gh, q0);
+          const uint32_t s1 = nvfp4::quantize16(b1, gh, q1);
           *reinterpret_cast<uint4*>(codes + hh * 16) = make_uint4(q0.x, q0.y, q1.x, q1.y);
-          *reinterpret_cast<uint16_t*>(sf + nvfp4::sf_offset(p, 4 * x.nb + 2 * hh, n_h)) =
-              static_cast<uint16_t>(s0 | (s1 << 8));
+          scw |= (s0 | (s1 << 8)) << (16 * hh);
         }
+        // the 4 scales of h blocks 8 nb + 4 half + [0, 4): one word of the atom
+        *reinterpret_cast<uint32_t*>(sf + nvfp4::sf_offset(p, 8 * x.nb + 4 * half, n_h)) = scw;
       } else {
+        uint32_t acc[4][32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) ptx::tmem_ld32(taddr + 32 * j, acc[j]);
+        ptx::tmem_ld_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&c.aempty[buf]);  // accumulator free for tile i+2
+        const float gw = *args.w_gs[tab + widx];
         const float alpha = __fmul_rn(gh, gw);
         const int n_out = args.N_routed;  // H
         const int valid_rows = x.rows - x.rb * kRows;
@@ -356,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool valid = lane < valid_w;
         const float w = (valid && routed && args.row_weight) ? args.row_weight[wrow0 + lane] : 1.0f;
         const float wa = w * alpha;
-        __half* y = static_cast<__half*>(routed ? args.out0 : args.out1) + x.nb * kCols;
+        __half* y = static_cast<__half*>(routed ? args.out0 : args.out1) + x.nb * C::kCols;
         float* ys = (routed ? args.out_scales0 : args.out_scales1) + x.nb * 4;
         uint4* stg = reinterpret_cast<uint4*>(out_stage + (warp - 2) * kStageOutBytes);
         const int swz = (lane >> 2) & 1;
@@ -411,11 +490,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool kGemm1>
 cudaError_t launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const Nvfp4GemmArgs& args,
                         int grid, cudaStream_t stream) {
-  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  constexpr size_t smem = smem_bytes<kGemm1>();
+  static_assert(smem <= 232448, "shared memory budget");
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(grouped_gemm_nvfp4_kernel<kGemm1>),
-                                   static_cast<int>(kSmemBytes));
+                                   static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  grouped_gemm_nvfp4_kernel<kGemm1><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, args);
+  grouped_gemm_nvfp4_kernel<kGemm1><<<grid, Cfg<kGemm1>::kThreads, smem, stream>>>(a0, a1, args);
   return cudaGetLastError();
 }
 

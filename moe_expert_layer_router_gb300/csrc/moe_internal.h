@@ -215,7 +215,7 @@ cudaError_t launch_quant_act_fp8(const void* x, int64_t M, int64_t K, uint8_t* q
                                  cudaStream_t stream);
 
 // NVFP4 weights: bf16 [N, K] (w2 null) or the stacked gate/up pair (w, w2 both
-// [N, K]; output rows interleaved in 64-row blocks [w 64 | w2 64]); codes
+// [N, K]; output rows interleaved in 128-row blocks [w 128 | w2 128]); codes
 // [rows, K/2], MMA-layout scales, tensor scale amax / 2688 into *tensor_scale.
 cudaError_t launch_quant_weight_nvfp4(const void* w, const void* w2, int64_t N, int64_t K,
                                       uint8_t* codes, uint8_t* sf, float* tensor_scale,

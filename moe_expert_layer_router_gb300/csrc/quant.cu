@@ -122,7 +122,7 @@ __device__ __forceinline__ float weight_tensor_scale(uint32_t amax_bits) {
 }
 
 // One thread per (output row, 16-element block).  With w2, output row v is row
-// 64 (v / 128) + v % 64 of w (v % 128 < 64) or of w2 (otherwise).
+// 128 (v / 256) + v % 128 of w (v % 256 < 128) or of w2 (otherwise).
 __global__ void __launch_bounds__(256)
     nvfp4_quant_weight_kernel(const __nv_bfloat16* __restrict__ w,
                               const __nv_bfloat16* __restrict__ w2, int64_t N, int64_t K,
@@ -136,8 +136,8 @@ __global__ void __launch_bounds__(256)
   const int kb = static_cast<int>(i - v * nb);
   const __nv_bfloat16* src;
   if (w2) {
-    const int64_t r = (v >> 7) * 64 + (v & 63);
-    src = ((v & 127) < 64 ? w : w2) + r * K;
+    const int64_t r = (v >> 8) * 128 + (v & 127);
+    src = ((v & 255) < 128 ? w : w2) + r * K;
   } else {
     src = w + v * K;
   }

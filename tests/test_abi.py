@@ -216,7 +216,7 @@ def test_nvfp4_weights_create_validates(L):
 
 def test_nvfp4_quantize_validation(L):
     assert L.moe_quantize_weight_nvfp4(16, None, 100, 128, 16, 16, 16, None) == N.MOE_ERR_INVALID_ARG
-    assert L.moe_quantize_weight_nvfp4(16, 16, 96, 128, 16, 16, 16, None) == N.MOE_ERR_INVALID_ARG
+    assert L.moe_quantize_weight_nvfp4(16, 16, 64, 128, 16, 16, 16, None) == N.MOE_ERR_INVALID_ARG
     assert L.moe_quantize_weight_nvfp4(16, None, 128, 96, 16, 16, 16, None) == N.MOE_ERR_INVALID_ARG
     assert L.moe_quantize_act_nvfp4(16, 4, 100, 1.0, 16, 16, None) == N.MOE_ERR_INVALID_ARG
     assert L.moe_quantize_act_nvfp4(16, 4, 128, 0.0, 16, 16, None) == N.MOE_ERR_INVALID_ARG

@@ -39,18 +39,19 @@ def sf_rowmajor(sf, rows, K) -> np.ndarray:
 def stacked_order(I) -> np.ndarray:
     """Row v of the interleaved gate/up matrix -> row of [W_g; W_u]."""
     v = np.arange(2 * I)
-    b, i = v // 128, v % 128
-    return np.where(i < 64, 64 * b + i, I + 64 * b + (i - 64))
+    b, i = v // 256, v % 256
+    return np.where(i < 128, 128 * b + i, I + 128 * b + (i - 128))
 
 
 # ---------------------------------------------------------------- quantisers
 def test_weight_quantiser_bit_exact_stacked_and_plain():
     dev = torch.device("cuda")
-    I, H = 192, 320
+    I, H = 384, 320
     wg = wl.rng.normal_bf16(0, 91, (I, H), 0.02, dev)
     wu = wl.rng.normal_bf16(0, 92, (I, H), 0.03, dev)
     wg[:64, :64] = 0                                    # all-zero blocks
     wu[7, 5] = 0.9                                      # the tensor's amax, in the up half
+    wg[200:, 64:80] = 0                                 # zero blocks in the second 128-row block
     codes, sf, ts = m.moe_quantize_weight_nvfp4(wg, wu)
     torch.cuda.synchronize()
     ref_q, ref_s, ref_g = onv.quantize_weight(np.concatenate([f64(wg), f64(wu)]))
