@@ -521,8 +521,8 @@ static moe_status_t encode_layer(const moe_config_t* cfg, const moe_weight_list_
 }
 
 // NVFP4: GEMM1 descriptor of group g at 2g (the stacked gate/up codes, 2I x H/2
-// bytes, boxes of 256 rows x 128 bytes; 2g+1 repeats it), GEMM2 at 2G+g (down
-// codes, H x I/2 bytes, boxes of 128 rows x 128 bytes).  scales[] hold the MMA-layout scale bytes, gs[] the
+// bytes; 2g+1 repeats it), GEMM2 at 2G+g (down codes, H x I/2 bytes); boxes of
+// 256 rows x 128 bytes.  scales[] hold the MMA-layout scale bytes, gs[] the
 // tensor-scale pointers (same indexing); act[0..1] = g_x, g_h.
 static moe_status_t encode_layer_nvfp4(const moe_config_t* cfg, const moe_weight_list_t* wl,
                                        CUtensorMap* maps, const float** scales, const float** gs,
@@ -571,7 +571,7 @@ static moe_status_t encode_layer_nvfp4(const moe_config_t* cfg, const moe_weight
     const void* wd = sh ? wl->shared_down : wl->down[g];
     MOE_TRY(encode_2d(&m1[2 * g], false, wgu, H / 2, 2 * inter, 128, 2 * kNvfp4Rows));
     m1[2 * g + 1] = m1[2 * g];
-    MOE_TRY(encode_2d(&m2[g], false, wd, inter / 2, H, 128, kNvfp4Rows));
+    MOE_TRY(encode_2d(&m2[g], false, wd, inter / 2, H, 128, 2 * kNvfp4Rows));
     scales[2 * g] = static_cast<const float*>(sh ? wl->shared_gate_sf : wl->gate_sf[g]);
     scales[2 * g + 1] = scales[2 * g];
     scales[2 * G + g] = static_cast<const float*>(sh ? wl->shared_down_sf : wl->down_sf[g]);
@@ -978,8 +978,8 @@ static moe_status_t run_nvfp4(const moe_config_t& c, const WeightView& W, const 
   uint8_t* hs = at<uint8_t*>(ws, L.hs);
   uint8_t* h_sf = at<uint8_t*>(ws, L.h_sc);
   uint8_t* hs_sf = at<uint8_t*>(ws, L.hs_sc);
-  // GEMM1 tiles: 128 h columns (256 stacked gate/up rows); GEMM2 tiles: 128 y columns
-  const int n1r = c.I / 128, n1s = c.I_shared / 128, n2 = c.H / kNvfp4Rows;
+  // GEMM1 tiles: 128 h columns (256 stacked gate/up rows); GEMM2 tiles: 256 y columns
+  const int n1r = c.I / 128, n1s = c.I_shared / 128, n2 = c.H / 256;
   trace_mark(st, MOE_K_PLAN);
   MOE_CUDA(launch_plan(offsets, c.E, shared ? 1 : 0, c.T, n1r, n1s, n2, n2, s1, s2, kNvfp4Rows,
                        kNvfp4Rows, st));

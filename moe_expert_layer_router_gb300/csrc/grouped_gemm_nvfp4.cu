@@ -59,23 +59,23 @@ constexpr int kABytes = kRows * kRowBytes;  // 16 KB
 constexpr int kSfaBytes = 2048;             // 4 atoms of 512 bytes (4 MMAs of K = 64)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSfCol = 256;                 // first scale slot
-constexpr int kStageOutBytes = 1024;        // GEMM2, per epilogue warp: 32 rows x 32 B of fp16 y
+constexpr int kStageOutBytes = 512;         // GEMM2, per epilogue warp: 16 rows x 32 B of fp16 y
 
 template <bool kGemm1>
 struct Cfg {
-  static constexpr int W = kGemm1 ? 2 : 1;           // 128-row weight blocks per tile
+  static constexpr int W = 2;                        // 128-row weight blocks per tile
   static constexpr int kCols = 128 * W;              // UMMA N
   static constexpr int kBBytes = kCols * kRowBytes;
   static constexpr int kSfbBytes = 2048 * W;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-  static constexpr int kStages = kGemm1 ? 4 : 6;
-  static constexpr int kAccBufs = kGemm1 ? 1 : 2;
+  static constexpr int kStages = W == 2 ? 4 : 6;
+  static constexpr int kAccBufs = W == 2 ? 1 : 2;
   static constexpr int kAccCols = kCols;
-  static constexpr int kEpiWarps = kGemm1 ? 8 : 4;
+  static constexpr int kEpiWarps = W == 2 ? 8 : 4;
   static constexpr int kSfWarp0 = 2 + kEpiWarps;    // first scale warp
   static constexpr int kThreads = 32 * (kSfWarp0 + 4);
   static constexpr int kSlotCols = 16 + 16 * W;      // A scales 16, B scales 16 W
-  static constexpr int kOutBytes = kGemm1 ? 0 : 4 * kStageOutBytes;
+  static constexpr int kOutBytes = kGemm1 ? 0 : kEpiWarps * kStageOutBytes;
   static constexpr uint32_t kIdesc = ptx::idesc_nvf4(kRows, kCols);
   static_assert(kAccBufs * kAccCols <= kSfCol, "accumulators below the scale slots");
   static_assert(kSfCol + kSlotCols * kStages <= int(kTmemCols), "TMEM budget");
@@ -417,61 +417,71 @@ __global__ void __launch_bounds__(Cfg<kGemm1>::kThreads, 1)
         // the 4 scales of h blocks 8 nb + 4 half + [0, 4): one word of the atom
         *reinterpret_cast<uint32_t*>(sf + nvfp4::sf_offset(p, 8 * x.nb + 4 * half, n_h)) = scw;
       } else {
-        uint32_t acc[4][32];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) ptx::tmem_ld32(taddr + 32 * j, acc[j]);
-        ptx::tmem_ld_wait();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&c.aempty[buf]);  // accumulator free for tile i+2
-        const float gw = *args.w_gs[tab + widx];
-        const float alpha = __fmul_rn(gh, gw);
+        // y columns 256 nb + 128 half + [0, 128) of this warp's 32 rows, as fp16
+        // with a power-of-two scale s = 2^(floor(log2 amax) - 14) per 32 columns
+        // (|y| / s < 2^15); packed right after each TMEM load so that the single
+        // accumulator is released after the fourth
+        const float alpha = __fmul_rn(gh, *args.w_gs[tab + widx]);
         const int n_out = args.N_routed;  // H
         const int valid_rows = x.rows - x.rb * kRows;
-        // rows of this warp: tile rows 32q .. 32q + 31 (lane = row), output row
-        // of lane 0 and how many of the warp's rows exist
         const int64_t wrow0 = (routed ? int64_t(c.off[x.g]) : 0) + int64_t(x.rb) * kRows + q * 32;
         const int valid_w = valid_rows - q * 32;
         const bool valid = lane < valid_w;
         const float w = (valid && routed && args.row_weight) ? args.row_weight[wrow0 + lane] : 1.0f;
         const float wa = w * alpha;
-        __half* y = static_cast<__half*>(routed ? args.out0 : args.out1) + x.nb * C::kCols;
-        float* ys = (routed ? args.out_scales0 : args.out_scales1) + x.nb * 4;
+        uint32_t pk[4][16];
+        float scl[4];
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+          uint32_t a32[32];
+          ptx::tmem_ld32(taddr + 128 * half + 32 * cb, a32);
+          ptx::tmem_ld_wait();
+          if (cb == 3) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&c.aempty[buf]);  // accumulator free
+          }
+          float amax = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(wa * __uint_as_float(a32[j])));
+          int sb = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 14;
+          sb = sb < 1 ? 1 : sb;
+          scl[cb] = __uint_as_float(static_cast<uint32_t>(sb) << 23);
+          const float inv = __uint_as_float(static_cast<uint32_t>(254 - sb) << 23);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const __half2 hh = __floats2half2_rn(wa * __uint_as_float(a32[2 * e]) * inv,
+                                                 wa * __uint_as_float(a32[2 * e + 1]) * inv);
+            pk[cb][e] = *reinterpret_cast<const uint32_t*>(&hh);
+          }
+        }
+        const int col0 = x.nb * C::kCols + 128 * half;
+        __half* y = static_cast<__half*>(routed ? args.out0 : args.out1) + col0;
+        float* ys = (routed ? args.out_scales0 : args.out_scales1) + col0 / 32;
+        if (valid) {
+#pragma unroll
+          for (int cb = 0; cb < 4; ++cb) ys[(wrow0 + lane) * (n_out / 32) + cb] = scl[cb];
+        }
+        // staged stores: per 16 columns, 16 rows at a time, each store
+        // instruction writing 16 rows x 32 bytes
         uint4* stg = reinterpret_cast<uint4*>(out_stage + (warp - 2) * kStageOutBytes);
         const int swz = (lane >> 2) & 1;
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-          float amax = 0.0f;
+        for (int sc = 0; sc < 8; ++sc) {   // 16-column sub-chunks
+          const uint32_t* v = &pk[sc >> 1][8 * (sc & 1)];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(wa * __uint_as_float(acc[cb][j])));
-          // fp16 with a power-of-two scale s = 2^(floor(log2 amax) - 14): |y| / s < 2^15
-          int sb = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 14;
-          sb = sb < 1 ? 1 : sb;
-          const float scale = __uint_as_float(static_cast<uint32_t>(sb) << 23);
-          const float inv = __uint_as_float(static_cast<uint32_t>(254 - sb) << 23);
-          if (valid) ys[(wrow0 + lane) * (n_out / 32) + cb] = scale;
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            // 16 columns of this lane's row -> 32 B in the warp's staging buffer
-            uint32_t pk[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int i = hf * 16 + e * 2;
-              const __half2 hh = __floats2half2_rn(wa * __uint_as_float(acc[cb][i]) * inv,
-                                                   wa * __uint_as_float(acc[cb][i + 1]) * inv);
-              pk[e] = *reinterpret_cast<const uint32_t*>(&hh);
+          for (int r2 = 0; r2 < 2; ++r2) {
+            if ((lane >> 4) == r2) {
+              const int l = lane & 15;
+              stg[l * 2 + swz] = make_uint4(v[0], v[1], v[2], v[3]);
+              stg[l * 2 + (swz ^ 1)] = make_uint4(v[4], v[5], v[6], v[7]);
             }
-            stg[lane * 2 + swz] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            stg[lane * 2 + (swz ^ 1)] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
             __syncwarp();
-            // read back transposed: each store instruction writes 16 rows x 32 B
-#pragma unroll
-            for (int it2 = 0; it2 < 2; ++it2) {
-              const int i = it2 * 16 + (lane >> 1), vv = lane & 1;
-              const uint4 val = stg[i * 2 + (vv ^ ((i >> 2) & 1))];
-              if (i < valid_w)
-                *reinterpret_cast<uint4*>(y + (wrow0 + i) * n_out + cb * 32 + hf * 16 + vv * 8) = val;
-            }
+            const int i = lane >> 1, vv = lane & 1;
+            const uint4 val = stg[i * 2 + (vv ^ ((i >> 2) & 1))];
+            const int row = 16 * r2 + i;
+            if (row < valid_w)
+              *reinterpret_cast<uint4*>(y + (wrow0 + row) * n_out + sc * 16 + vv * 8) = val;
             __syncwarp();
           }
         }
