@@ -38,7 +38,7 @@
 //   GEMM2: B = 128 rows of W_down; y = accumulator * g_h * g_w * row weight,
 //     written as fp16 with a power-of-two scale per 32 columns (only the
 //     block's real rows, at their unpadded row index), staged in shared memory
-//     per warp so that each store instruction writes 16 rows x 32 bytes.
+//     per warp so that each store instruction writes 4 rows x 128 bytes.
 // Warp roles: warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer, then
 // the epilogue warps (one row per thread; GEMM1: two warps per lane quarter,
 // one per 64-column half), then the 4 scale warps.  Persistent CTAs over the
@@ -59,7 +59,7 @@ constexpr int kABytes = kRows * kRowBytes;  // 16 KB
 constexpr int kSfaBytes = 2048;             // 4 atoms of 512 bytes (4 MMAs of K = 64)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSfCol = 256;                 // first scale slot
-constexpr int kStageOutBytes = 512;         // GEMM2, per epilogue warp: 16 rows x 32 B of fp16 y
+constexpr int kStageOutBytes = 512;         // GEMM2, per epilogue warp: 4 rows x 128 B of fp16 y
 
 template <bool kGemm1>
 struct Cfg {
@@ -96,6 +96,7 @@ struct __align__(8) SmemCtl {
   int32_t sched[2 * kMaxGroups + 2];  // copy of the tile schedule
   int32_t off[kMaxExperts + 1];       // copies of the row offsets and the padded offsets
   int32_t pad[kMaxExperts + 1];
+  float gw[kMaxGroups];               // each group's weight tensor scale
 };
 
 template <bool kGemm1>
@@ -207,6 +208,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1>::kThreads, 1)
     c.off[i] = __ldg(args.offsets + i);
     c.pad[i] = __ldg(args.pad_offsets + i);
   }
+  for (int g = threadIdx.x; g < G; g += kThreads) c.gw[g] = *args.w_gs[tab + (kGemm1 ? 2 * g : g)];
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -363,12 +365,19 @@ __global__ void __launch_bounds__(Cfg<kGemm1>::kThreads, 1)
       const bool routed = x.g < args.E;
       const int buf = tc % C::kAccBufs;
       const uint32_t bph = (tc / C::kAccBufs) & 1;
+      // this tile's scale and (GEMM2) row weight, loaded before the wait
+      const float gw = c.gw[x.g];
+      const int valid_rows = x.rows - x.rb * kRows;
+      const int64_t wrow0 = (routed ? int64_t(c.off[x.g]) : 0) + int64_t(x.rb) * kRows + q * 32;
+      const int valid_w = valid_rows - q * 32;
+      const bool valid = lane < valid_w;
+      const float rw = (!kGemm1 && valid && routed && args.row_weight)
+                           ? __ldg(args.row_weight + wrow0 + lane) : 1.0f;
       const bool ok = ptx::mbar_wait(&c.afull[buf], bph, abort, args.err);
       if (epi_any<32 * C::kEpiWarps>(!ok || *abort)) break;  // uniform over the epilogue warps
       ptx::tc_fence_after();
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::kAccCols;
-      const int widx = kGemm1 ? 2 * x.g : x.g;
       if constexpr (kGemm1) {
         // accumulator columns [0,128) gate, [128,256) up of h columns
         // [128 nb, 128 nb + 128); this warp: h columns 64 half + [0, 64), in
@@ -382,7 +391,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1>::kThreads, 1)
           uint32_t g1[32], u1[32];
           ptx::tmem_ld32(taddr + 64 * half + 32, g1);
           ptx::tmem_ld32(taddr + 128 + 64 * half + 32, u1);
-          const float alpha = __fmul_rn(gx, *args.w_gs[tab + widx]);
+          const float alpha = __fmul_rn(gx, gw);
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             h[0][i] = silu_f(__uint_as_float(g0[i]) * alpha) * (__uint_as_float(u0[i]) * alpha);
@@ -421,14 +430,9 @@ __global__ void __launch_bounds__(Cfg<kGemm1>::kThreads, 1)
         // with a power-of-two scale s = 2^(floor(log2 amax) - 14) per 32 columns
         // (|y| / s < 2^15); packed right after each TMEM load so that the single
         // accumulator is released after the fourth
-        const float alpha = __fmul_rn(gh, *args.w_gs[tab + widx]);
+        const float alpha = __fmul_rn(gh, gw);
         const int n_out = args.N_routed;  // H
-        const int valid_rows = x.rows - x.rb * kRows;
-        const int64_t wrow0 = (routed ? int64_t(c.off[x.g]) : 0) + int64_t(x.rb) * kRows + q * 32;
-        const int valid_w = valid_rows - q * 32;
-        const bool valid = lane < valid_w;
-        const float w = (valid && routed && args.row_weight) ? args.row_weight[wrow0 + lane] : 1.0f;
-        const float wa = w * alpha;
+        const float wa = rw * alpha;
         uint32_t pk[4][16];
         float scl[4];
 #pragma unroll
@@ -458,30 +462,32 @@ __global__ void __launch_bounds__(Cfg<kGemm1>::kThreads, 1)
         const int col0 = x.nb * C::kCols + 128 * half;
         __half* y = static_cast<__half*>(routed ? args.out0 : args.out1) + col0;
         float* ys = (routed ? args.out_scales0 : args.out_scales1) + col0 / 32;
-        if (valid) {
-#pragma unroll
-          for (int cb = 0; cb < 4; ++cb) ys[(wrow0 + lane) * (n_out / 32) + cb] = scl[cb];
-        }
-        // staged stores: per 16 columns, 16 rows at a time, each store
-        // instruction writing 16 rows x 32 bytes
+        // the row's 4 scales are contiguous: one 16-byte store
+        if (valid)
+          __stcs(reinterpret_cast<float4*>(ys + (wrow0 + lane) * (n_out / 32)),
+                 make_float4(scl[0], scl[1], scl[2], scl[3]));
+        // staged stores, 64 columns (128 bytes of a row) at a time: 4 rows per
+        // round go through the warp's 512-byte buffer, so that each store
+        // instruction writes 4 whole 128-byte lines (8 lanes per row)
         uint4* stg = reinterpret_cast<uint4*>(out_stage + (warp - 2) * kStageOutBytes);
-        const int swz = (lane >> 2) & 1;
 #pragma unroll
-        for (int sc = 0; sc < 8; ++sc) {   // 16-column sub-chunks
-          const uint32_t* v = &pk[sc >> 1][8 * (sc & 1)];
+        for (int c64 = 0; c64 < 2; ++c64) {
 #pragma unroll
-          for (int r2 = 0; r2 < 2; ++r2) {
-            if ((lane >> 4) == r2) {
-              const int l = lane & 15;
-              stg[l * 2 + swz] = make_uint4(v[0], v[1], v[2], v[3]);
-              stg[l * 2 + (swz ^ 1)] = make_uint4(v[4], v[5], v[6], v[7]);
+          for (int r4 = 0; r4 < 8; ++r4) {
+            if ((lane >> 2) == r4) {
+              const int l = lane & 3;
+#pragma unroll
+              for (int c16 = 0; c16 < 8; ++c16) {
+                const uint32_t* v = &pk[2 * c64 + (c16 >> 2)][4 * (c16 & 3)];
+                stg[l * 8 + (c16 ^ l)] = make_uint4(v[0], v[1], v[2], v[3]);
+              }
             }
             __syncwarp();
-            const int i = lane >> 1, vv = lane & 1;
-            const uint4 val = stg[i * 2 + (vv ^ ((i >> 2) & 1))];
-            const int row = 16 * r2 + i;
-            if (row < valid_w)
-              *reinterpret_cast<uint4*>(y + (wrow0 + row) * n_out + sc * 16 + vv * 8) = val;
+            const int i = lane >> 3, cc = lane & 7;
+            const uint4 val = stg[i * 8 + (cc ^ i)];
+            const int row = 4 * r4 + i;
+            if (row < valid_w)  // streaming: y is read once, by the combine
+              __stcs(reinterpret_cast<uint4*>(y + (wrow0 + row) * n_out + 64 * c64 + cc * 8), val);
             __syncwarp();
           }
         }
