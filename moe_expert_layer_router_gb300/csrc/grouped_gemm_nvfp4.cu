@@ -71,9 +71,20 @@ struct Cfg {
   static constexpr int kStages = W == 2 ? 4 : 6;
   static constexpr int kAccBufs = W == 2 ? 1 : 2;
   static constexpr int kAccCols = kCols;
-  static constexpr int kEpiWarps = W == 2 ? 8 : 4;
-  static constexpr int kSfWarp0 = 2 + kEpiWarps;    // first scale warp
-  static constexpr int kThreads = 32 * (kSfWarp0 + 4);
+  // warpgroups (4 warps each): 0 = producer, MMA lane, two idle warps;
+  // 1, 2 = the epilogue; 3 = the scale warps
+  static constexpr int kEpiWarp0 = 4;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kSfWarp0 = kEpiWarp0 + kEpiWarps;  // first scale warp
+  static constexpr int kThreads = 32 * (kSfWarp0 + 4);     // 512
+  // register split (setmaxnreg): launched with 128 per thread, the producer
+  // group and the scale group drop to 64 and the epilogue groups rise to 192:
+  // 2 x 128 x 64 + 2 x 128 x 192 = 65536 = 512 x 128
+  static constexpr int kLaunchRegs = 128;
+  static constexpr int kLowRegs = 64;
+  static constexpr int kHighRegs = 192;
+  static_assert(2 * 128 * kLowRegs + 2 * 128 * kHighRegs == kThreads * kLaunchRegs,
+                "register split must add up to the launch's registers");
   static constexpr int kSlotCols = 16 + 16 * W;      // A scales 16, B scales 16 W
   static constexpr int kOutBytes = kGemm1 ? 0 : kEpiWarps * kStageOutBytes;
   static constexpr uint32_t kIdesc = ptx::idesc_nvf4(kRows, kCols);
@@ -215,7 +226,11 @@ __global__ void __launch_bounds__(Cfg<kGemm1>::kThreads, 1)
   const uint32_t tmem_base = c.tmem_base;
   const int num_tiles = c.sched[0];
   volatile int* abort = &c.abort;
-
+  // each warpgroup changes its register count at the top of its own branch,
+  // every warp of the group executing the same setmaxnreg
+  const int wgrp = warp >> 2;
+  if (wgrp == 0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(C::kLowRegs) : "memory");
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------- TMA producer
@@ -294,7 +309,9 @@ __global__ void __launch_bounds__(Cfg<kGemm1>::kThreads, 1)
       ptx::mma_commit(&c.drain);
       drain_wait(&c.drain, 0, args.err);
     }
-  } else if (warp >= C::kSfWarp0) {
+  }  // warps 2 and 3 have no role
+  } else if (wgrp == 3) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(C::kLowRegs) : "memory");
     // ------------------------------------------------------ scale warps
     const int q = warp & 3;  // TMEM lane quarter of this warp
     const uint32_t lane_q = static_cast<uint32_t>(q * 32) << 16;
@@ -353,10 +370,11 @@ __global__ void __launch_bounds__(Cfg<kGemm1>::kThreads, 1)
       if (!ok) break;
     }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(C::kHighRegs) : "memory");
     // ------------------------------------------------------ epilogue warps
     const int q = warp & 3;
     const int r = q * 32 + lane;  // row of the tile (TMEM lane)
-    const int half = (warp - 2) / 4;  // GEMM1: which 64 of the tile's 128 h columns
+    const int half = (warp - C::kEpiWarp0) / 4;  // which 128 (GEMM1: 64) of the tile's columns
     const float gx = __ldg(args.act_scales + 2 * layer);
     const float gh = __ldg(args.act_scales + 2 * layer + 1);
     uint32_t tc = 0;
@@ -384,24 +402,21 @@ __global__ void __launch_bounds__(Cfg<kGemm1>::kThreads, 1)
         // two chunks of 32, the single accumulator released once both are read
         float h[2][32];
         {
-          uint32_t g0[32], u0[32];
+          uint32_t g0[32], u0[32], g1[32], u1[32];
           ptx::tmem_ld32(taddr + 64 * half, g0);
           ptx::tmem_ld32(taddr + 128 + 64 * half, u0);
-          ptx::tmem_ld_wait();
-          uint32_t g1[32], u1[32];
           ptx::tmem_ld32(taddr + 64 * half + 32, g1);
           ptx::tmem_ld32(taddr + 128 + 64 * half + 32, u1);
-          const float alpha = __fmul_rn(gx, gw);
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            h[0][i] = silu_f(__uint_as_float(g0[i]) * alpha) * (__uint_as_float(u0[i]) * alpha);
           ptx::tmem_ld_wait();
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&c.aempty[buf]);  // accumulator free
+          const float alpha = __fmul_rn(gx, gw);
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
+          for (int i = 0; i < 32; ++i) {
+            h[0][i] = silu_f(__uint_as_float(g0[i]) * alpha) * (__uint_as_float(u0[i]) * alpha);
             h[1][i] = silu_f(__uint_as_float(g1[i]) * alpha) * (__uint_as_float(u1[i]) * alpha);
+          }
         }
         const int n_h = routed ? args.N_routed : args.N_shared;  // I or I_shared
         const int64_t p = (routed ? c.pad[x.g] : 0) + int64_t(x.rb) * kRows + r;
@@ -435,16 +450,16 @@ __global__ void __launch_bounds__(Cfg<kGemm1>::kThreads, 1)
         const float wa = rw * alpha;
         uint32_t pk[4][16];
         float scl[4];
+        uint32_t a128[4][32];
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) ptx::tmem_ld32(taddr + 128 * half + 32 * cb, a128[cb]);
+        ptx::tmem_ld_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&c.aempty[buf]);  // accumulator free
 #pragma unroll
         for (int cb = 0; cb < 4; ++cb) {
-          uint32_t a32[32];
-          ptx::tmem_ld32(taddr + 128 * half + 32 * cb, a32);
-          ptx::tmem_ld_wait();
-          if (cb == 3) {
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&c.aempty[buf]);  // accumulator free
-          }
+          const uint32_t* a32 = a128[cb];
           float amax = 0.0f;
 #pragma unroll
           for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(wa * __uint_as_float(a32[j])));
@@ -469,7 +484,8 @@ __global__ void __launch_bounds__(Cfg<kGemm1>::kThreads, 1)
         // staged stores, 64 columns (128 bytes of a row) at a time: 4 rows per
         // round go through the warp's 512-byte buffer, so that each store
         // instruction writes 4 whole 128-byte lines (8 lanes per row)
-        uint4* stg = reinterpret_cast<uint4*>(out_stage + (warp - 2) * kStageOutBytes);
+        uint4* stg =
+            reinterpret_cast<uint4*>(out_stage + (warp - C::kEpiWarp0) * kStageOutBytes);
 #pragma unroll
         for (int c64 = 0; c64 < 2; ++c64) {
 #pragma unroll
@@ -508,9 +524,18 @@ cudaError_t launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const Nvfp
                         int grid, cudaStream_t stream) {
   constexpr size_t smem = smem_bytes<kGemm1>();
   static_assert(smem <= 232448, "shared memory budget");
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(grouped_gemm_nvfp4_kernel<kGemm1>),
-                                   static_cast<int>(smem));
+  const void* fn = reinterpret_cast<const void*>(grouped_gemm_nvfp4_kernel<kGemm1>);
+  cudaError_t e = ensure_smem_attr(fn, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  // the register split assumes the block is launched with kLaunchRegs per
+  // thread; with fewer, the epilogue's setmaxnreg.inc could never be served
+  cudaFuncAttributes fa{};
+  e = cudaFuncGetAttributes(&fa, fn);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != Cfg<kGemm1>::kLaunchRegs) {
+    set_last_error_text("NVFP4 GEMM kernel built with an unexpected register count");
+    return cudaErrorInvalidConfiguration;
+  }
   grouped_gemm_nvfp4_kernel<kGemm1><<<grid, Cfg<kGemm1>::kThreads, smem, stream>>>(a0, a1, args);
   return cudaGetLastError();
 }
