@@ -291,7 +291,7 @@ MOE_API moe_status_t moe_forward(const moe_config_t* cfg, moe_weights_t weights,
  *     Compute Disaggregation for Large-Model Inference: AFD Architecture
  *     Analysis and Performance Validation", section 5 (operator fusion).  Same
  *     results; on GB300 the row gathers are slower than one permuted copy plus
- *     tile loads, so it is off by default.  Ignored for fp8 layers.
+ *     tile loads, so it is off by default.  Ignored for fp8 and NVFP4 layers.
  * Unknown flag bits give MOE_ERR_INVALID_ARG. */
 #define MOE_FORWARD_FUSED_DISPATCH 0x1u
 MOE_API moe_status_t moe_forward_ex(const moe_config_t* cfg, moe_weights_t weights, const void* x,
