@@ -13,11 +13,10 @@
 // and its scales are whole 512-byte atoms (see nvfp4.cuh, sf_offset).
 //   stage = A 16 KB | B 16 W KB | A scales 2 KB | B scales 2 W KB
 // A block-scaled MMA of M = 128 costs the same ~135 cycles for N = 128 and
-// N = 256, so GEMM1 (K = H, long) uses W = 2: one MMA per K = 64 covers 256
-// weight rows, with a single 256-column accumulator (TMEM cannot hold two next
-// to the scale slots) that 8 epilogue warps drain quickly.  GEMM2 (K = I,
-// short) keeps W = 1 with two 128-column accumulators, so that its epilogue
-// overlaps the next tile's MMAs.
+// N = 256, so both GEMMs use W = 2: one MMA per K = 64 covers 256 weight rows,
+// into a single 256-column accumulator (TMEM cannot hold two next to the scale
+// slots).  Eight epilogue warps, given 192 registers each by setmaxnreg, read
+// all of it with one wait and release it at once.
 // A and B arrive by TMA (128-byte swizzle), the scale atoms by 1-D bulk copies
 // on their own barrier, issued first.  Four scale warps, one per TMEM lane
 // quarter, move each stage's scales into that stage's TMEM scale slot with
@@ -35,15 +34,18 @@
 //     the gate and up rows of h columns [128 n, 128 n + 128).  h = silu(g) * u
 //     with g, u = accumulator * g_x * g_w, quantised to NVFP4 with the static
 //     scale g_h: packed codes and MMA-layout scales of every row of the block.
-//   GEMM2: B = 128 rows of W_down; y = accumulator * g_h * g_w * row weight,
-//     written as fp16 with a power-of-two scale per 32 columns (only the
-//     block's real rows, at their unpadded row index), staged in shared memory
-//     per warp so that each store instruction writes 4 rows x 128 bytes.
-// Warp roles: warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer, then
-// the epilogue warps (one row per thread; GEMM1: two warps per lane quarter,
-// one per 64-column half), then the 4 scale warps.  Persistent CTAs over the
-// device-built tile schedule (heaviest experts first, tiles of one weight
-// block adjacent), which every CTA first copies into shared memory.
+//   GEMM2: y = accumulator * g_h * g_w * row weight,
+//     B = 256 rows of W_down; written as fp16 with a power-of-two scale per 32
+//     columns (only the block's real rows, at their unpadded row index),
+//     staged in shared memory per warp so that each store instruction writes
+//     4 rows x 128 bytes.
+// Warp roles, by warpgroup: 0 = TMA producer (warp 0), TMEM allocator + MMA
+// issuer (warp 1) and two idle warps; 1 and 2 = the epilogue (one row per
+// thread, two warps per TMEM lane quarter, one per 128-column half); 3 = the
+// scale warps.  Persistent CTAs over the device-built tile schedule (heaviest
+// experts first, tiles of one weight block adjacent), which every CTA first
+// copies into shared memory together with the row offsets and the weight
+// tensor scales.
 #include <cuda_fp16.h>
 
 #include "moe_internal.h"

@@ -174,10 +174,18 @@ def test_nvfp4_forward_matches_oracle(lc):
     check_layer(Nvfp4Layer(lc, torch.device("cuda")))
 
 
-def test_nvfp4_forward_full_size_sampled():
-    """The DeepSeek-V3 NVFP4 layer at T = 16384 in the launch configuration the
-    bench times; the oracle evaluates 3 sampled tokens through their experts."""
-    L = Nvfp4Layer(wl.DSV3_NVFP4, torch.device("cuda"))
+FULL = [
+    wl.DSV3_NVFP4,                                            # the bench workload
+    wl.DSV3_NVFP4.with_(name="dsv3_nvfp4_t512", T=512),       # 16 rows per expert
+    wl.QWEN3.with_(name="qwen3_nvfp4", wtype="nvfp4"),        # softmax, no shared expert
+]
+
+
+@pytest.mark.parametrize("lc", FULL, ids=lambda c: c.name)
+def test_nvfp4_forward_full_size_sampled(lc):
+    """Full-size NVFP4 layers in the launch configuration the bench times: routing
+    over every token, and 3 sampled tokens through their experts by the oracle."""
+    L = Nvfp4Layer(lc, torch.device("cuda"))
     check_layer(L, n_sample=3)
 
 
