@@ -18,15 +18,24 @@ constexpr int kBlock = 16;           // elements per scale
 constexpr float kE2M1Max = 6.0f;
 constexpr float kTensorDiv = 2688.0f;  // 6 * 448: weight tensor scale g = amax / 2688
 
-// E2M1 code of r: the magnitude code is the number of rounding thresholds at or
-// below |r| (ties to the even code: 0.25 -> 0, 0.75 -> 1.0, 1.25 -> 1.0,
-// 1.75 -> 2, 2.5 -> 2, 3.5 -> 4, 5 -> 4), saturating at 6 (code 7).
-__device__ __forceinline__ uint32_t e2m1(float r) {
-  const float a = fabsf(r);
-  const uint32_t m = uint32_t(a > 0.25f) + uint32_t(a >= 0.75f) + uint32_t(a > 1.25f) +
-                     uint32_t(a >= 1.75f) + uint32_t(a > 2.5f) + uint32_t(a >= 3.5f) +
-                     uint32_t(a > 5.0f);
-  return (r < 0.0f && m != 0u) ? (m | 8u) : m;
+// Eight values -> their E2M1 codes packed into 32 bits (value 2i in the low
+// nibble of byte i, 2i + 1 in the high one), by the hardware conversion
+// cvt.rn.satfinite.e2m1x2.f32: round to nearest, ties to the even code
+// (0.25 -> 0, 0.75 -> 1.0, 1.25 -> 1.0, 1.75 -> 2, 2.5 -> 2, 3.5 -> 4,
+// 5 -> 4), saturating at 6.  It keeps the sign of a value that rounds to zero;
+// those codes are cleared to +0.
+__device__ __forceinline__ uint32_t e2m1x8(const float* r) {
+  uint32_t w;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(w)
+      : "f"(r[0]), "f"(r[1]), "f"(r[2]), "f"(r[3]), "f"(r[4]), "f"(r[5]), "f"(r[6]), "f"(r[7]));
+  const uint32_t nonzero = (w | (w >> 1) | (w >> 2)) & 0x11111111u;  // bit 0 of each nibble
+  return (w & 0x77777777u) | (w & (nonzero << 3));
 }
 
 // Value of a non-negative e4m3 code (bias 7, 3 mantissa bits).
@@ -47,11 +56,11 @@ __device__ __forceinline__ uint32_t quantize16(const float (&v)[16], float g, ui
   const float den = __fmul_rn(e4m3_value(sc), g);
   uint32_t lo = 0u, hi = 0u;
   if (den != 0.0f) {
+    float r[16];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      lo |= e2m1(__fdiv_rn(v[i], den)) << (4 * i);
-      hi |= e2m1(__fdiv_rn(v[i + 8], den)) << (4 * i);
-    }
+    for (int i = 0; i < 16; ++i) r[i] = __fdiv_rn(v[i], den);
+    lo = e2m1x8(r);
+    hi = e2m1x8(r + 8);
   }
   packed = make_uint2(lo, hi);
   return sc;

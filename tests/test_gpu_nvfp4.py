@@ -84,12 +84,20 @@ def test_activation_quantiser_bit_exact():
     x[3] = 0                                            # zero blocks
     x[5, :16] = 5000.0                                  # saturates the block scale (448)
     x[6, 16:32] = 1e-4                                  # scale in the e4m3 subnormal range
+    # a block whose scale is exactly 1 (amax = 6 g): every other quotient is an
+    # exact rounding threshold (ties to the even code), and the negative ones
+    # that round to zero must give +0 (code 0, not 8)
+    ties = [6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -0.75, -1.25, -1.75, -2.5, -3.5, -5.0, -0.1]
+    x[7, :16] = torch.tensor(ties, dtype=torch.float32).to(x.dtype).to(dev) * g
     codes, sf = m.moe_quantize_act_nvfp4(x, g)
     torch.cuda.synchronize()
     ref_q, ref_s = onv.quantize_blocks(f64(x).astype(np.float32), np.float32(g))
     assert (unpack(codes) == ref_q).all()
     assert (sf.cpu().numpy() == ref_s).all()
     assert ref_s[5, 0] == 0x7E and ref_s[3].max() == 0
+    # codes of 6, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5 and their negatives, -0.1
+    assert ref_s[7, 0] == 0x38 and list(ref_q[7, :16]) == [7, 0, 2, 2, 4, 4, 6, 6,
+                                                           0, 10, 10, 12, 12, 14, 14, 0]
 
 
 # ---------------------------------------------------------------- the layer
