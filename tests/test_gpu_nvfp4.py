@@ -174,6 +174,9 @@ SMALL = [
     wl.DSV3_NVFP4.with_(name="nvfp4_one_token", T=1, H=512, E=4, k=1, I=256, I_shared=256),
     # several 128-row blocks per expert and a ragged last block
     wl.DSV3_NVFP4.with_(name="nvfp4_multi_block", T=700, H=768, E=4, k=2, I=768, I_shared=512),
+    # Zipf-biased routing: a few hot experts with many row blocks, the coldest with none
+    wl.DSV3_NVFP4.with_(name="nvfp4_skewed", T=600, H=512, E=16, k=4, I=256, I_shared=256,
+                        zipf_bias=True),
 ]
 
 
@@ -186,6 +189,7 @@ FULL = [
     wl.DSV3_NVFP4,                                            # the bench workload
     wl.DSV3_NVFP4.with_(name="dsv3_nvfp4_t512", T=512),       # 16 rows per expert
     wl.QWEN3.with_(name="qwen3_nvfp4", wtype="nvfp4"),        # softmax, no shared expert
+    wl.DSV3_SKEW.with_(name="dsv3_skewed_nvfp4", wtype="nvfp4"),  # hottest expert ~10x the mean rows
 ]
 
 
