@@ -101,9 +101,11 @@ DSV3_FP8_SLICE = DSV3_FP8.with_(name="dsv3_fp8_slice", T=128, E=64)
 # batch of the bf16 layer; its profiling slice like dsv3_slice.
 DSV3_NVFP4 = DSV3.with_(name="dsv3_nvfp4", wtype="nvfp4")
 DSV3_NVFP4_SLICE = DSV3_NVFP4.with_(name="dsv3_nvfp4_slice", T=4096, E=64)
+# the NVFP4 layer at the small batch of the fp8 layer (16 rows per expert): weight streaming
+DSV3_NVFP4_T512 = DSV3_NVFP4.with_(name="dsv3_nvfp4_t512", T=512)
 
 CONFIGS = {c.name: c for c in (TINY, QWEN3, DSV3, DSV3_SKEW, DSV3_FP8, DSV3_T512, DSV3_SLICE,
-                                DSV3_FP8_SLICE, DSV3_NVFP4, DSV3_NVFP4_SLICE)}
+                                DSV3_FP8_SLICE, DSV3_NVFP4, DSV3_NVFP4_SLICE, DSV3_NVFP4_T512)}
 
 
 def nvfp4_act_scales(cfg: LayerConfig) -> tuple[float, float]:
