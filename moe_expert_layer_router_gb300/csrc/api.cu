@@ -1014,7 +1014,7 @@ static moe_status_t run_nvfp4(const moe_config_t& c, const WeightView& W, const 
   g1.N_routed = c.I;
   g1.N_shared = c.I_shared;
   trace_mark(st, MOE_K_GEMM1);
-  MOE_CUDA(launch_grouped_gemm_nvfp4(true, a0, a1, g1, grid, st));
+  MOE_CUDA(launch_grouped_gemm_nvfp4(true, a0, a1, a0, a1, g1, grid, st));  // no y maps
 
   CUtensorMap b0, b1;
   MOE_TRY(encode_2d(&b0, false, h, c.I / 2, Rp, 128, kNvfp4Rows));
@@ -1038,9 +1038,14 @@ static moe_status_t run_nvfp4(const moe_config_t& c, const WeightView& W, const 
   g2.K_shared = c.I_shared;
   g2.N_routed = c.H;
   g2.N_shared = c.H;
+  // fp16 y and shared output for GEMM2's TMA stores: 32-row x 64-column boxes
+  // (the 2-byte element type only sets the element size; the bits are copied)
+  CUtensorMap y0, y1;
+  MOE_TRY(encode_2d(&y0, true, y, c.H, R, 64, 32));
+  if (shared) MOE_TRY(encode_2d(&y1, true, shared_out, c.H, c.T, 64, 32));
+  else y1 = y0;
   trace_mark(st, MOE_K_GEMM2);
-  MOE_CUDA(launch_grouped_gemm_nvfp4(false, b0, b1, g2, grid, st));
-  (void)R;
+  MOE_CUDA(launch_grouped_gemm_nvfp4(false, b0, b1, y0, y1, g2, grid, st));
   return MOE_OK;
 }
 

@@ -190,8 +190,11 @@ cudaError_t launch_grouped_gemm_fp8(bool gate_up, const CUtensorMap& tok_map0,
                                     const CUtensorMap& tok_map1, const Fp8GemmArgs& args, int grid,
                                     cudaStream_t stream);
 
+// map_y0 / map_y1: GEMM2's fp16 outputs (routed rows, shared-expert rows) as
+// 2-byte tensors with 32-row x 64-column boxes, 128-byte swizzle; unused by GEMM1.
 cudaError_t launch_grouped_gemm_nvfp4(bool gemm1, const CUtensorMap& map_a0,
-                                      const CUtensorMap& map_a1, const Nvfp4GemmArgs& args,
+                                      const CUtensorMap& map_a1, const CUtensorMap& map_y0,
+                                      const CUtensorMap& map_y1, const Nvfp4GemmArgs& args,
                                       int grid, cudaStream_t stream);
 
 cudaError_t launch_grouped_gemm(bool swiglu, const CUtensorMap& map_a0, const CUtensorMap& map_a1,

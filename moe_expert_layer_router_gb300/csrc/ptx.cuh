@@ -286,6 +286,40 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// ---------------------------------------------------------------- TMA stores
+// Make this thread's generic-proxy writes to shared memory visible to the
+// async proxy (before a TMA store reads them).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 2-D tiled store of the box of `map` at {c0, c1} from this CTA's shared
+// memory (laid out as the map's swizzle places it), in this thread's current
+// bulk-async group.  c0 * element size must be a multiple of 16 bytes and
+// neither coordinate may be negative.
+__device__ __forceinline__ void tma_store_2d(const void* map, const void* src, int32_t c0,
+                                             int32_t c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until this thread's bulk-async groups have finished reading shared
+// memory (the source may be rewritten) ...
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// ... or have completed entirely.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
