@@ -20,7 +20,9 @@
 // Work unit: a 256-row x 256-column pair tile computed by the two CTAs of a
 // cluster with one 256x256x16 MMA per 16-wide K step.  Each CTA loads its own
 // 128 rows of A and one half of B, so a stage is 32 KB per CTA (instead of 48
-// KB for a single-CTA 128x256 tile) and the ring holds 6 stages.  B halves:
+// KB for a single-CTA 128x256 tile) and the ring holds 5 stages (6 were
+// slower under the power cap: GEMM1 6.34 vs 6.07 ms, GEMM2 3.38 vs 3.26 ms on
+// DeepSeek-V3; 4 were slower still).  B halves:
 //   GEMM1: CTA r loads W_gate and W_up rows [128 n + 64 r, +64) (64 + 64 rows),
 //          so TMEM columns are [gate | up] of output columns 128 n + 64 r + [0,64)
 //   GEMM2: CTA r loads W_down rows [256 n + 128 r, +128)
@@ -47,7 +49,7 @@
 namespace moe {
 namespace {
 
-constexpr int kStages = 6;
+constexpr int kStages = 5;
 constexpr int kThreads = 192;
 constexpr int kPairRows = kGemmTileRows;      // 256 rows per pair tile (128 per CTA)
 static_assert(kPairRows == 2 * kTileM, "a pair tile is two CTA tiles");
