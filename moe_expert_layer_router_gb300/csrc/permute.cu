@@ -499,13 +499,26 @@ cudaError_t launch_scatter_nvfp4(const int32_t* ids, const float* topk_w, const 
                                  float* row_weight, const Nvfp4Scatter& q, uint32_t* err,
                                  cudaStream_t stream) {
   const int nblk = static_cast<int>((T + kPermTok - 1) / kPermTok);
-  // about 16 blocks per SM: the quantisation is latency-bound at a few warps
-  // per SM (0.39 ms with 2 blocks per SM, 0.29 ms with 16 on DeepSeek-V3)
+  // Column slices: about 12 blocks per SM (3 waves of 4 resident blocks; the
+  // quantisation is latency-bound at fewer warps), each slice a whole number
+  // of 512 columns (one 16-element block per lane and step) unless that leaves
+  // less than one wave.  DeepSeek-V3 shapes: T = 16384 0.393 ms with 2 blocks
+  // per SM -> 0.277 ms; T = 4096 0.131 -> 0.064 ms with 512-column slices;
+  // T = 512 0.052 ms with the finest slices (128 columns).
   int sm = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev);
-  int ysplit = (16 * sm + nblk - 1) / nblk;
-  if (ysplit > H / 128) ysplit = H / 128;
+  if (nblk <= 0) return cudaSuccess;
+  const int groups = H / 128;
+  const int wide = groups / 4 > 0 ? groups / 4 : 1;  // slices of 512 columns
+  int ysplit = (12 * sm + nblk - 1) / nblk;
+  if (ysplit <= wide) {
+    const int per = (wide + ysplit / 2) / ysplit;  // 512-column units per slice
+    ysplit = wide / (per > 0 ? per : 1);
+  } else if (int64_t(nblk) * wide >= 4 * int64_t(sm)) {
+    ysplit = wide;
+  }
+  if (ysplit > groups) ysplit = groups;
   if (ysplit < 1) ysplit = 1;
   scatter_nvfp4_kernel<<<dim3(nblk, ysplit), kScatterThreads, 0, stream>>>(
       ids, topk_w, static_cast<const __nv_bfloat16*>(x), T, k, E, H, nblk, blk_base, offsets,
