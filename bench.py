@@ -29,6 +29,7 @@ os.environ.setdefault("MKL_NUM_THREADS", "1")
 import argparse  # noqa: E402
 import hashlib  # noqa: E402
 import json  # noqa: E402
+import re  # noqa: E402
 import statistics  # noqa: E402
 import subprocess  # noqa: E402
 import sys  # noqa: E402
@@ -152,11 +153,19 @@ KERNEL_SOURCES = {
 FP4_OVER_BF16 = 6.0
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and blank lines: edits to comments leave
+    the kernel's code, and so the recorded hash, unchanged."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
 def kernel_source_hash(kind: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_expert_layer_router_gb300", "csrc")
     for f in KERNEL_SOURCES[kind]:
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        h.update(_code_only(open(os.path.join(csrc, f), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

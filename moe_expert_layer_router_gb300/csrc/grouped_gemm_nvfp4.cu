@@ -11,7 +11,7 @@
 // stages of 256 elements (128 bytes per row).  Each expert's rows are padded to
 // a multiple of 128 in the permuted buffers, so a tile is one aligned row block
 // and its scales are whole 512-byte atoms (see nvfp4.cuh, sf_offset).
-//   stage = A 16 KB | B 16 W KB | A scales 2 KB | B scales 2 W KB
+//   stage = A 16 KB | B 16 W KB | A scales 2 KB | B scales 2 W KB (W = 2: 54 KB)
 // A block-scaled MMA of M = 128 costs the same ~135 cycles for N = 128 and
 // N = 256, so both GEMMs use W = 2: one MMA per K = 64 covers 256 weight rows,
 // into a single 256-column accumulator (TMEM cannot hold two next to the scale
@@ -36,9 +36,12 @@
 //     scale g_h: packed codes and MMA-layout scales of every row of the block.
 //   GEMM2: y = accumulator * g_h * g_w * row weight,
 //     B = 256 rows of W_down; written as fp16 with a power-of-two scale per 32
-//     columns (only the block's real rows, at their unpadded row index),
-//     staged in shared memory per warp so that each store instruction writes
-//     4 rows x 128 bytes.
+//     columns (only the block's real rows, at their unpadded row index).  Each
+//     epilogue warp puts its 32 rows x 64 columns into a 4 KB shared-memory box
+//     (128-byte swizzle) that one lane writes out with a TMA store; a warp with
+//     fewer than 32 real rows (the segment's end) stages them through 512 bytes
+//     of that buffer instead, 4 rows x 128 bytes per store instruction.  GEMM2
+//     runs 3 stages, GEMM1 4.
 // Warp roles, by warpgroup: 0 = TMA producer (warp 0), TMEM allocator + MMA
 // issuer (warp 1) and two idle warps; 1 and 2 = the epilogue (one row per
 // thread, two warps per TMEM lane quarter, one per 128-column half); 3 = the
