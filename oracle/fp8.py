@@ -194,3 +194,12 @@ def moe_tokens_fp8(x_rows, ids, w, experts, shared):
         if shared is not None:
             out[t] += swiglu_ffn_fp8(xd[t:t + 1], *shared)[0]
     return out
+
+
+def expert_rows_fp8(x_rows, w_gate, w_up, w_down) -> np.ndarray:
+    """One fp8 expert on raw (unquantised) input rows: each row quantised in
+    1x128 groups and dequantised, then ``swiglu_ffn_fp8`` on the dequantised
+    weights.  The row function ``moe.moe_tokens_by_expert`` takes; with it the
+    fp8 layer's per-token sum equals ``moe_tokens_fp8``."""
+    q, s = quantize_act_groups(np.asarray(moe._f64(x_rows), dtype=np.float32))
+    return swiglu_ffn_fp8(dequant_act(q, s), w_gate, w_up, w_down)

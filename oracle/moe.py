@@ -260,3 +260,36 @@ def moe_tokens(x_rows, ids, w, experts, shared) -> np.ndarray:
     if out is None:
         out = np.zeros((0, x_rows.shape[1]), dtype=np.float64)
     return out
+
+
+def moe_tokens_by_expert(x_rows, ids, w, expert_rows, shared_rows=None, map_fn=map):
+    """The same per-token sum as ``moe_tokens``, evaluated expert by expert so
+    that only one expert's weights need to exist at a time: for every expert e
+    that some token selected, the rows of the tokens that selected it go
+    through ``expert_rows(e, rows) -> [n, H]`` in one call, and each token adds
+    w[t, j] times its row of the result; then ``shared_rows(x_rows)`` (the
+    always-on shared expert, weight 1) when given.
+
+    The expert functions are row-independent (each output row depends on its
+    own input row only), so this equals the token-by-token sum.  ``map_fn``
+    runs the per-expert calls; any function with the signature of the builtin
+    ``map`` (which is the default) serves, e.g. a process pool's ``map``."""
+    x_rows = _f64(x_rows)
+    ids = np.asarray(ids)
+    w = _f64(w)
+    T = x_rows.shape[0]
+    experts = sorted({int(e) for e in ids.reshape(-1)})
+    where = [np.nonzero(ids == e) for e in experts]          # (tokens, slots) per expert
+    ys = list(map_fn(expert_rows, experts, [x_rows[t] for t, _ in where]))
+    out = None
+    for (t, j), y in zip(where, ys):
+        y = _f64(y)
+        if out is None:
+            out = np.zeros((T, y.shape[1]), dtype=np.float64)
+        np.add.at(out, t, w[t, j][:, None] * y)
+    if shared_rows is not None:
+        s = _f64(shared_rows(x_rows))
+        out = s.copy() if out is None else out + s
+    if out is None:
+        out = np.zeros((T, x_rows.shape[1]), dtype=np.float64)
+    return out

@@ -209,3 +209,13 @@ def moe_tokens_nvfp4(x_rows, ids, w, experts, shared, g_x, g_h):
         if shared is not None:
             out[t] += swiglu_ffn_nvfp4(xd[t:t + 1], *shared, g_h)[0]
     return out
+
+
+def expert_rows_nvfp4(x_rows, w_gate, w_up, w_down, g_x, g_h) -> np.ndarray:
+    """One NVFP4 expert on raw input rows: each row quantised with the static
+    tensor scale g_x and dequantised, then ``swiglu_ffn_nvfp4`` (h quantised
+    with g_h) on the dequantised weights.  The row function
+    ``moe.moe_tokens_by_expert`` takes; with it the NVFP4 layer's per-token sum
+    equals ``moe_tokens_nvfp4``."""
+    xd = quantize_act(np.asarray(moe._f64(x_rows), dtype=np.float32), g_x)[0]
+    return swiglu_ffn_nvfp4(xd, w_gate, w_up, w_down, g_h)

@@ -188,6 +188,21 @@ def test_bruteforce_equals_grouped_nvfp4_layer():
     assert 1e-3 < rel < 0.3
 
 
+def test_by_expert_equals_bruteforce_nvfp4():
+    T, H, E, k, I = 13, 128, 5, 2, 64
+    x, wr, W, sh = _layer_inputs(T, H, E, k, I)
+    Wd = [nvfp4.dequantize_expert(*nvfp4.quantize_expert(*w)) for w in W]
+    shd = nvfp4.dequantize_expert(*nvfp4.quantize_expert(*sh))
+    gx, gh = 2.0 ** -8, 2.0 ** -4
+    r = nvfp4.moe_layer_nvfp4(x, wr, None, lambda e: Wd[e], shd, k, "sigmoid", True, 2.5, gx, gh)
+    be = moe.moe_tokens_by_expert(x, r["ids"], r["weights"],
+                                  lambda e, xr: nvfp4.expert_rows_nvfp4(xr, *Wd[e], gx, gh),
+                                  lambda xr: nvfp4.expert_rows_nvfp4(xr, *shd, gx, gh))
+    np.testing.assert_allclose(be, r["out"], rtol=1e-12, atol=1e-12)
+    bf = nvfp4.moe_tokens_nvfp4(x, r["ids"], r["weights"], lambda e: Wd[e], shd, gx, gh)
+    np.testing.assert_allclose(be, bf, rtol=1e-12, atol=1e-12)
+
+
 def test_activation_quantisation_is_per_row():
     """Each token is quantised on its own: quantising a stack of rows equals
     quantising each row alone (so quantise-then-gather equals gather-then-quantise)."""

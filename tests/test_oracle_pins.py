@@ -216,6 +216,28 @@ def test_grouped_equals_bruteforce(score, scale, Is):
     np.testing.assert_allclose(r["out"], bf, rtol=1e-12, atol=1e-12)
 
 
+@pytest.mark.parametrize("score,scale,Is", [("softmax", 1.0, 0), ("sigmoid", 2.5, 6)])
+def test_by_expert_equals_bruteforce(score, scale, Is):
+    """The expert-by-expert evaluation (one expert's weights at a time) gives the
+    per-token sum, on all tokens and on a subset of them, whatever order the
+    per-expert calls run in."""
+    T, H, E, k, I = 31, 8, 7, 3, 5
+    x, wr, W, sh = _layer_inputs(T, H, E, k, I, Is)
+    r = moe.moe_layer(x, wr, None, lambda e: W[e], sh, k, score, True, scale)
+    rows = lambda e, xr: moe.swiglu_ffn(xr, *W[e])
+    shared = (lambda xr: moe.swiglu_ffn(xr, *sh)) if sh else None
+    be = moe.moe_tokens_by_expert(x, r["ids"], r["weights"], rows, shared)
+    np.testing.assert_allclose(be, r["out"], rtol=1e-12, atol=1e-12)
+    sub = np.array([0, 4, 5, 17, 30])
+    rev = lambda f, a, b: reversed([f(*z) for z in reversed(list(zip(a, b)))])
+    be2 = moe.moe_tokens_by_expert(x[sub], r["ids"][sub], r["weights"][sub], rows, shared, rev)
+    bf = moe.moe_tokens(x[sub], r["ids"][sub], r["weights"][sub], lambda e: W[e], sh)
+    np.testing.assert_allclose(be2, bf, rtol=1e-12, atol=1e-12)
+    # a wrong weight or a dropped shared expert is visible
+    assert not np.allclose(moe.moe_tokens_by_expert(x, r["ids"], r["weights"][:, ::-1], rows,
+                                                    shared), r["out"])
+
+
 def test_single_expert_is_dense_swiglu():
     T, H, I = 9, 6, 4
     x, wr, W, _ = _layer_inputs(T, H, 1, 1, I, 0)
@@ -357,6 +379,21 @@ def test_fp8_bruteforce_equals_grouped_fp8_layer():
     r = fp8.moe_layer_fp8(x, wr, None, lambda e: Wd[e], shd, k, "sigmoid", True, 2.5)
     bf = fp8.moe_tokens_fp8(x, r["ids"], r["weights"], lambda e: Wd[e], shd)
     np.testing.assert_allclose(bf, r["out"], rtol=1e-12, atol=1e-12)
+
+
+def test_fp8_by_expert_equals_bruteforce():
+    T, H, E, k, I = 13, 256, 5, 2, 128
+    x, wr, W, sh = _layer_inputs(T, H, E, k, I, 128)
+    Wd = [tuple(fp8.dequant_weight(*fp8.quantize_weight_blocks(m_.astype(np.float32))) for m_ in w3)
+          for w3 in W]
+    shd = tuple(fp8.dequant_weight(*fp8.quantize_weight_blocks(m_.astype(np.float32))) for m_ in sh)
+    r = fp8.moe_layer_fp8(x, wr, None, lambda e: Wd[e], shd, k, "sigmoid", True, 2.5)
+    be = moe.moe_tokens_by_expert(x, r["ids"], r["weights"],
+                                  lambda e, xr: fp8.expert_rows_fp8(xr, *Wd[e]),
+                                  lambda xr: fp8.expert_rows_fp8(xr, *shd))
+    np.testing.assert_allclose(be, r["out"], rtol=1e-12, atol=1e-12)
+    bf = fp8.moe_tokens_fp8(x, r["ids"], r["weights"], lambda e: Wd[e], shd)
+    np.testing.assert_allclose(be, bf, rtol=1e-12, atol=1e-12)
 
 
 def test_e4m3_table_encoder_equals_bitfield_encoder():
