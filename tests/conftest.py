@@ -24,3 +24,16 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Print the routing and sampled-parity records the GPU tests kept, so that
+    near ties, flips and float errors are visible in a quiet (-q) run."""
+    mod = sys.modules.get("parity")
+    recs = getattr(mod, "REPORT", None) if mod else None
+    if not recs:
+        return
+    terminalreporter.section("parity records")
+    for r in recs:
+        terminalreporter.write_line(" ".join(f"{k}={v:.3g}" if isinstance(v, float) else f"{k}={v}"
+                                             for k, v in sorted(r.items())))

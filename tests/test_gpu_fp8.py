@@ -9,7 +9,7 @@ import moe_expert_layer_router_gb300 as m
 import workload as wl
 from oracle import fp8 as of8
 from oracle import moe as om
-from parity import FP8_MAX_OVER_RMS, assert_close_layer, f64, logit_tolerance, near_tie_tokens
+from parity import FP8_MAX_OVER_RMS, Routing, assert_close_layer, check_sampled, f64, with_flips
 
 pytestmark = pytest.mark.gpu
 
@@ -107,27 +107,54 @@ def test_fp8_grouped_ffn_matches_oracle(lc):
                            max_over_rms=FP8_MAX_OVER_RMS, mean_rel=1.0, what="fp8 shared")
 
 
-@pytest.mark.parametrize("lc", [
-    wl.DSV3_FP8.with_(name="fp8_layer_small", T=200, H=1024, E=16, k=4, I=256, I_shared=256),
-    wl.DSV3_FP8,
-], ids=lambda c: c.name)
-def test_fp8_forward_matches_oracle(lc):
+def test_fp8_forward_small_matches_oracle():
+    """A small fp8 layer, every output row against the oracle's fp8 layer."""
     dev = torch.device("cuda")
+    lc = wl.DSV3_FP8.with_(name="fp8_layer_small", T=200, H=1024, E=16, k=4, I=256, I_shared=256)
     L = Fp8Layer(lc, dev)
     ws = m.Workspace(L.cfg, "forward")
     out, ids, w = m.moe_forward(L.cfg, L.weights, L.x, L.wr, return_routing=True, ws=ws)
     torch.cuda.synchronize()
     m.moe_get_device_error(ws)
-    ids = ids.cpu().numpy()
-    ref_lg = om.router_logits(f64(L.x), f64(L.wr))
-    ref_ids = om.select_topk(ref_lg, lc.k)
-    tie = near_tie_tokens(ref_lg, lc.k, logit_tolerance(L.x, L.wr))
-    assert (ids[~tie] == ref_ids[~tie]).all()
-    g = np.random.default_rng(3)
-    sample = np.sort(g.choice(np.flatnonzero(~tie), size=min(3, lc.T), replace=False))
-    ref_w = om.routing_weights(ref_lg[sample], ref_ids[sample], lc.score, lc.renormalize,
-                               lc.route_scale)
-    ref = of8.moe_tokens_fp8(f64(L.x[torch.from_numpy(sample).to(dev)]), ref_ids[sample], ref_w,
-                             L.oracle_expert, L.oracle_shared())
-    assert_close_layer(out[torch.from_numpy(sample).to(dev)], ref,
-                       max_over_rms=FP8_MAX_OVER_RMS, mean_rel=1.0, what=f"{lc.name} sampled")
+    r = Routing(lc.name, lc, L.cfg, L.x, L.wr, None, ids.cpu().numpy(), m)
+    ref = of8.moe_layer_fp8(f64(L.x), f64(L.wr), None, L.oracle_expert, L.oracle_shared(), lc.k,
+                            lc.score, lc.renormalize, lc.route_scale)
+    ref_out = with_flips(r, ref["out"], lambda t, i, w_: of8.moe_tokens_fp8(
+        f64(L.x)[t], i, w_, L.oracle_expert, L.oracle_shared()))
+    assert_close_layer(out, ref_out, max_over_rms=FP8_MAX_OVER_RMS, mean_rel=1.0, what=lc.name)
+
+
+FP8_FAMILY = [wl.DSV3_FP8, *wl.DSV3_FP8_DECODE]
+
+
+@pytest.fixture(scope="module")
+def fp8_family():
+    """The fp8 workload (DeepSeek-V3 shapes, T = 512) and its decode-sized batches,
+    which share one set of fp8 expert weights: each runs on the GPU, its routing
+    is checked, and every output row of all of them (each token through all of
+    its experts) goes through one oracle pass."""
+    dev = torch.device("cuda")
+    L = Fp8Layer(wl.DSV3_FP8.with_(T=max(lc.T for lc in FP8_FAMILY)), dev)
+    cases, failed = [], {}
+    for lc in FP8_FAMILY:
+        x = L.x[:lc.T]
+        cfg = m.config_from(lc)
+        ws = m.Workspace(cfg, "forward")
+        out, ids, _ = m.moe_forward(cfg, L.weights, x, L.wr, return_routing=True, ws=ws)
+        torch.cuda.synchronize()
+        try:
+            m.moe_get_device_error(ws)
+            r = Routing(lc.name, lc, cfg, x, L.wr, None, ids.cpu().numpy(), m)
+            cases.append(Case(lc.name, lc, r, x, out, FP8_MAX_OVER_RMS, 1.0))
+        except (AssertionError, m.MoeError) as e:
+            failed[lc.name] = str(e)
+    res = family_parity(cases)
+    res.update(failed)
+    return res
+
+
+@pytest.mark.parametrize("lc", FP8_FAMILY, ids=lambda c: c.name)
+def test_fp8_forward_full_size(fp8_family, lc):
+    rec = fp8_family[lc.name]
+    assert isinstance(rec, dict), rec
+    assert rec["rows_compared"] == lc.T and rec["experts_covered"] == rec["experts_with_rows"]

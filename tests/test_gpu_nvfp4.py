@@ -11,8 +11,8 @@ import moe_expert_layer_router_gb300 as m
 import workload as wl
 from oracle import moe as om
 from oracle import nvfp4 as onv
-from parity import (NVFP4_MAX_OVER_RMS, NVFP4_MEAN_REL, assert_close_layer, f64,
-                    logit_tolerance, near_tie_tokens)
+from parity import (NVFP4_MAX_OVER_RMS, NVFP4_MEAN_REL, Case, Routing, assert_close_layer,
+                    check_sampled, f64, family_parity, with_flips)
 
 pytestmark = pytest.mark.gpu
 
@@ -144,24 +144,25 @@ class Nvfp4Layer:
         return out, ids.cpu().numpy(), w
 
 
-def check_layer(L, n_sample=None, seed=0):
+def check_layer(L, full_size=False):
+    """Routing over every token (bit-exact off measured near ties); then every
+    output row against the oracle's NVFP4 layer (small layers), or the
+    stratified sample of at least 512 rows reaching every expert (full size)."""
     lc = L.lc
     out, ids, _ = L.forward()
-    b = None if L.bias is None else f64(L.bias)
-    ref_lg = om.router_logits(f64(L.x), f64(L.wr), b)
-    ref_ids = om.select_topk(ref_lg, lc.k)
-    tie = near_tie_tokens(ref_lg, lc.k, logit_tolerance(L.x, L.wr))
-    assert (ids[~tie] == ref_ids[~tie]).all()
-    cand = np.flatnonzero(~tie)
-    if n_sample is not None:
-        cand = np.sort(np.random.default_rng(seed).choice(cand, size=n_sample, replace=False))
-    ref_w = om.routing_weights(ref_lg[cand], ref_ids[cand], lc.score, lc.renormalize,
-                               lc.route_scale)
-    ref = onv.moe_tokens_nvfp4(f64(L.x[torch.from_numpy(cand).to(L.dev)]), ref_ids[cand], ref_w,
-                               L.oracle_expert, L.oracle_shared(), L.gx, L.gh)
-    assert_close_layer(out[torch.from_numpy(cand).to(L.dev)], ref, max_over_rms=NVFP4_MAX_OVER_RMS,
-                       mean_rel=NVFP4_MEAN_REL, what=lc.name)
+    r = Routing(lc.name, lc, L.cfg, L.x, L.wr, L.bias, ids, m)
     assert torch.isfinite(out.float()).all()
+    if full_size:
+        rec = check_sampled(lc.name, lc, r, L.x, out, NVFP4_MAX_OVER_RMS, NVFP4_MEAN_REL)
+        assert rec["experts_covered"] == rec["experts_with_rows"]
+        return out
+    b = None if L.bias is None else f64(L.bias)
+    ref = onv.moe_layer_nvfp4(f64(L.x), f64(L.wr), b, L.oracle_expert, L.oracle_shared(), lc.k,
+                              lc.score, lc.renormalize, lc.route_scale, L.gx, L.gh)
+    ref_out = with_flips(r, ref["out"], lambda t, i, w_: onv.moe_tokens_nvfp4(
+        f64(L.x)[t], i, w_, L.oracle_expert, L.oracle_shared(), L.gx, L.gh))
+    assert_close_layer(out, ref_out, max_over_rms=NVFP4_MAX_OVER_RMS, mean_rel=NVFP4_MEAN_REL,
+                       what=lc.name)
     return out
 
 
@@ -185,20 +186,51 @@ def test_nvfp4_forward_matches_oracle(lc):
     check_layer(Nvfp4Layer(lc, torch.device("cuda")))
 
 
-FULL = [
-    wl.DSV3_NVFP4,                                            # the bench workload
-    wl.DSV3_NVFP4.with_(name="dsv3_nvfp4_t512", T=512),       # 16 rows per expert
-    wl.QWEN3.with_(name="qwen3_nvfp4", wtype="nvfp4"),        # softmax, no shared expert
-    wl.DSV3_SKEW.with_(name="dsv3_skewed_nvfp4", wtype="nvfp4"),  # hottest expert ~10x the mean rows
-]
+# Full-size NVFP4 layers sharing the DeepSeek-V3 weights (the bench workload, its
+# 512-token batch and the skewed batch), plus the Qwen3 shape on its own.
+NVFP4_FAMILY = [wl.DSV3_NVFP4,                                         # the bench workload
+                wl.DSV3_NVFP4.with_(name="dsv3_nvfp4_t512", T=512),    # 16 rows per expert
+                wl.DSV3_SKEW.with_(name="dsv3_skewed_nvfp4", wtype="nvfp4")]  # ~10x hottest
 
 
-@pytest.mark.parametrize("lc", FULL, ids=lambda c: c.name)
-def test_nvfp4_forward_full_size_sampled(lc):
-    """Full-size NVFP4 layers in the launch configuration the bench times: routing
-    over every token, and 3 sampled tokens through their experts by the oracle."""
-    L = Nvfp4Layer(lc, torch.device("cuda"))
-    check_layer(L, n_sample=3)
+@pytest.fixture(scope="module")
+def nvfp4_family():
+    """Each DeepSeek-V3-shaped NVFP4 layer in the launch configuration the bench
+    times: routing over every token, and the stratified samples of all of them
+    through one oracle pass."""
+    dev = torch.device("cuda")
+    L = Nvfp4Layer(wl.DSV3_NVFP4.with_(T=max(lc.T for lc in NVFP4_FAMILY)), dev)
+    cases, failed = [], {}
+    for lc in NVFP4_FAMILY:
+        x = L.x[:lc.T]
+        b = wl.gen_bias(lc)
+        bias = b.to(dev) if b is not None else None
+        cfg = m.config_from(lc)
+        ws = m.Workspace(cfg, "forward")
+        out, ids, _ = m.moe_forward(cfg, L.weights, x, L.wr, bias, return_routing=True, ws=ws)
+        torch.cuda.synchronize()
+        try:
+            m.moe_get_device_error(ws)
+            r = Routing(lc.name, lc, cfg, x, L.wr, bias, ids.cpu().numpy(), m)
+            cases.append(Case(lc.name, lc, r, x, out, NVFP4_MAX_OVER_RMS, NVFP4_MEAN_REL))
+        except (AssertionError, m.MoeError) as e:
+            failed[lc.name] = str(e)
+    res = family_parity(cases)
+    res.update(failed)
+    return res
+
+
+@pytest.mark.parametrize("lc", NVFP4_FAMILY, ids=lambda c: c.name)
+def test_nvfp4_forward_full_size(nvfp4_family, lc):
+    rec = nvfp4_family[lc.name]
+    assert isinstance(rec, dict), rec
+    assert rec["experts_covered"] == rec["experts_with_rows"]
+
+
+def test_nvfp4_forward_full_size_qwen3():
+    """The Qwen3 shape with NVFP4 weights (softmax routing, no shared expert)."""
+    L = Nvfp4Layer(wl.QWEN3.with_(name="qwen3_nvfp4", wtype="nvfp4"), torch.device("cuda"))
+    check_layer(L, full_size=True)
 
 
 def test_nvfp4_deterministic_and_empty_batch():
@@ -224,7 +256,16 @@ def test_nvfp4_stack_layers_match_single_layer_calls():
     layers = [Nvfp4Layer(lc.with_(seed=s), dev) for s in range(2)]
     x = layers[0].x
     cfg = layers[0].cfg
-    refs = [m.moe_forward(cfg, L.weights, x, L.wr) for L in layers]
+    refs, oracle = [], []
+    for l, L in enumerate(layers):
+        out, ids, _ = m.moe_forward(cfg, L.weights, x, L.wr, return_routing=True)
+        torch.cuda.synchronize()
+        refs.append(out)
+        r = Routing(f"nvfp4_stack_layer{l}", lc, cfg, x, L.wr, None, ids.cpu().numpy(), m)
+        ref = onv.moe_layer_nvfp4(f64(x), f64(L.wr), None, L.oracle_expert, L.oracle_shared(),
+                                  lc.k, lc.score, lc.renormalize, lc.route_scale, L.gx, L.gh)
+        oracle.append(with_flips(r, ref["out"], lambda t, i, w_, L=L: onv.moe_tokens_nvfp4(
+            f64(x)[t], i, w_, L.oracle_expert, L.oracle_shared(), L.gx, L.gh)))
     stack = m.LayerStack(cfg, [L.weights for L in layers], [L.wr for L in layers])
     layer = torch.zeros(1, dtype=torch.int32, device=dev)
     ws = m.Workspace(cfg, "forward")
@@ -233,6 +274,8 @@ def test_nvfp4_stack_layers_match_single_layer_calls():
         layer.fill_(l)
         m.moe_forward_stack(cfg, stack, layer, x, out=out, ws=ws)
         torch.cuda.synchronize()
+        assert_close_layer(out, oracle[l], max_over_rms=NVFP4_MAX_OVER_RMS,
+                           mean_rel=NVFP4_MEAN_REL, what=f"NVFP4 stack layer {l}")
         assert torch.equal(out, refs[l]), f"layer {l}"
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
@@ -242,5 +285,7 @@ def test_nvfp4_stack_layers_match_single_layer_calls():
         out.zero_()
         graph.replay()
         torch.cuda.synchronize()
+        assert_close_layer(out, oracle[l], max_over_rms=NVFP4_MAX_OVER_RMS,
+                           mean_rel=NVFP4_MEAN_REL, what=f"graph, NVFP4 stack layer {l}")
         assert torch.equal(out, refs[l]), f"graph, layer {l}"
     assert m.moe_get_device_error(ws) == 0

@@ -104,8 +104,17 @@ DSV3_NVFP4_SLICE = DSV3_NVFP4.with_(name="dsv3_nvfp4_slice", T=4096, E=64)
 # the NVFP4 layer at the small batch of the fp8 layer (16 rows per expert): weight streaming
 DSV3_NVFP4_T512 = DSV3_NVFP4.with_(name="dsv3_nvfp4_t512", T=512)
 
+# The DeepSeek-V3 layer at decode-sized batches (the AFD write-up, section 1,
+# reads MoE utilisation at batches from 395 down to 6 tokens): T*k rows over
+# 256 experts, so most experts receive no token and the layer streams the
+# weights of those that do.
+DECODE_T = (8, 64, 128, 395)
+DSV3_DECODE = tuple(DSV3.with_(name=f"dsv3_bf16_t{t}", T=t) for t in DECODE_T)
+DSV3_FP8_DECODE = tuple(DSV3_FP8.with_(name=f"dsv3_fp8_t{t}", T=t) for t in DECODE_T)
+
 CONFIGS = {c.name: c for c in (TINY, QWEN3, DSV3, DSV3_SKEW, DSV3_FP8, DSV3_T512, DSV3_SLICE,
-                                DSV3_FP8_SLICE, DSV3_NVFP4, DSV3_NVFP4_SLICE, DSV3_NVFP4_T512)}
+                                DSV3_FP8_SLICE, DSV3_NVFP4, DSV3_NVFP4_SLICE, DSV3_NVFP4_T512,
+                                *DSV3_DECODE, *DSV3_FP8_DECODE)}
 
 
 def nvfp4_act_scales(cfg: LayerConfig) -> tuple[float, float]:
@@ -128,18 +137,26 @@ def _wshape(cfg: LayerConfig, which: str, inter: int):
     return (inter, cfg.H) if which in ("gate", "up") else (cfg.H, inter)
 
 
-def gen_expert(cfg: LayerConfig, e: int, which: str, device="cpu"):
+def _rows(shape, row_start: int, rows: int | None):
+    n = shape[0] - row_start if rows is None else rows
+    return (n,) + tuple(shape[1:])
+
+
+def gen_expert(cfg: LayerConfig, e: int, which: str, device="cpu", row_start: int = 0,
+               rows: int | None = None):
     """Routed expert e's W_gate / W_up ([I,H]) or W_down ([H,I]): bf16, or float32
-    (before block quantisation) for fp8 layers."""
-    shape = _wshape(cfg, which, cfg.I)
+    (before block quantisation) for fp8 layers.  ``row_start`` / ``rows`` give a
+    slice of rows, equal to the same rows of the whole matrix."""
+    shape = _rows(_wshape(cfg, which, cfg.I), row_start, rows)
     f = rng.normal_f32 if cfg.wtype == "fp8_e4m3" else rng.normal_bf16
-    return f(cfg.seed, rng.stream_id("w_" + which, e), shape, cfg.w_std, device)
+    return f(cfg.seed, rng.stream_id("w_" + which, e), shape, cfg.w_std, device, row_start)
 
 
-def gen_shared(cfg: LayerConfig, which: str, device="cpu"):
-    shape = _wshape(cfg, which, cfg.I_shared)
+def gen_shared(cfg: LayerConfig, which: str, device="cpu", row_start: int = 0,
+               rows: int | None = None):
+    shape = _rows(_wshape(cfg, which, cfg.I_shared), row_start, rows)
     f = rng.normal_f32 if cfg.wtype == "fp8_e4m3" else rng.normal_bf16
-    return f(cfg.seed, rng.stream_id("ws_" + which), shape, cfg.w_std, device)
+    return f(cfg.seed, rng.stream_id("ws_" + which), shape, cfg.w_std, device, row_start)
 
 
 def gen_bias(cfg: LayerConfig, gamma: float | None = None):
