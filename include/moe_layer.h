@@ -206,7 +206,9 @@ MOE_API moe_status_t moe_route(const moe_config_t* cfg, const void* x, const voi
 /* Step 2 -- histogram and permutation (ASAP table 2: per-expert token counts
  * of the dispatch metadata).  Deterministic: rows of expert e are
  * [expert_offsets[e], expert_offsets[e+1]) in ascending token order.
- *   topk_ids        int32 [T, k] in (each row k distinct ids in [0, E))
+ *   topk_ids        int32 [T, k] in (each row k distinct ids in [0, E); an id
+ *                   outside [0, E) sets status bit 0 and a repeated id within
+ *                   a row sets bit 3, and the outputs are then incomplete)
  *   topk_w          fp32 [T, k] in, or NULL
  *   x               bf16 [T, H] in, or NULL when x_perm is NULL
  *   expert_counts   int32 [E] out
@@ -232,9 +234,12 @@ MOE_API moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_id
  * Scratch: a fixed device array inside the library (about 2 MB, held by every
  * GPU that loads the library until exit), enough for E * ceil(T/64) <= 262144
  * (e.g. T <= 65536 at E = 256); larger layers get MOE_ERR_UNSUPPORTED and must
- * use moe_permute.  The first call on each device looks up the array's device
- * address (cudaGetSymbolAddress) and should come before any stream capture.
- * Calls allocate nothing.  All calls share the array: calls that run
+ * use moe_permute.  Every call made outside a stream capture looks up the
+ * array's device address in the current CUDA context (cudaGetSymbolAddress, a
+ * cheap lookup); a call made while its stream is being captured reuses the
+ * address of the last such lookup in the same context, so make one call in
+ * each context before any capture starts (a first call during capture returns
+ * MOE_ERR_INVALID_ARG).  Calls allocate nothing.  All calls share the array: calls that run
  * concurrently on the GPU race and must be ordered (one stream, or events).
  *   device_status  optional device word (4-byte aligned) that receives the
  *                  status bits (as moe_get_device_error reports them); NULL
@@ -378,8 +383,25 @@ MOE_API moe_status_t moe_quantize_act_nvfp4(const void* x, int64_t M, int64_t K,
 
 /* Waits for `stream`, reads the workspace's sticky device status word, clears
  * it and maps it to MOE_OK / MOE_ERR_BOUNDS / MOE_ERR_DEVICE_TIMEOUT.
- * *device_bits (optional) receives the raw word (bit 0 bounds, bit 1 timeout). */
+ * *device_bits (optional) receives the raw word: bit 0 an index outside its
+ * range, bit 1 a bounded wait that expired (MOE_ERR_DEVICE_TIMEOUT), bit 2 a
+ * token with fewer than k selectable (non-NaN) logits, bit 3 a token whose k
+ * expert ids are not distinct (bits 0, 2 and 3 give MOE_ERR_BOUNDS). */
 MOE_API moe_status_t moe_get_device_error(void* ws, moe_stream_t stream, int32_t* device_bits);
+
+/* Failure-path test hook (the pages have no counterpart).  Sets, for the
+ * calling thread, how many of its next bf16 grouped GEMM1 launches (inside
+ * moe_grouped_ffn, moe_forward or moe_forward_stack) stall on purpose: in such
+ * a launch the MMA issuer of the first CTA pair waits, before its first tile,
+ * on a barrier that nothing signals.  Like every wait in the kernels, that one
+ * gives up after its limit (2 s): it sets the timeout bit of the workspace
+ * status word and the pair abandons its remaining tiles, drains the loads it
+ * issued, frees its tensor memory and exits; every other pair finishes.  The
+ * call's outputs are then incomplete and moe_get_device_error returns
+ * MOE_ERR_DEVICE_TIMEOUT; the next call on the same workspace runs normally.
+ * For tests of failure detection and recovery only; 0 (the default) disables
+ * it.  count < 0 gives MOE_ERR_INVALID_ARG. */
+MOE_API moe_status_t moe_test_stall_gemm1(int32_t count);
 
 /* Kernel tracing.  While a trace is set on the calling thread, every call
  * records one of the caller's CUDA events on its stream before each kernel it

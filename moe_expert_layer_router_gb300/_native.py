@@ -75,6 +75,7 @@ _SIG = {
     "moe_quantize_weight_nvfp4": (C.c_int, [_P, _P, C.c_int64, C.c_int64, _P, _P, _P, _P]),
     "moe_quantize_act_nvfp4": (C.c_int, [_P, C.c_int64, C.c_int64, C.c_float, _P, _P, _P]),
     "moe_set_trace": (C.c_int, [C.POINTER(MoeTrace)]),
+    "moe_test_stall_gemm1": (C.c_int, [C.c_int32]),
     "moe_permute_noalloc": (C.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 

@@ -95,6 +95,15 @@ cudaError_t ensure_smem_attr(const void* func, int bytes) {
   return cudaSuccess;
 }
 
+// ------------------------------------------------------------------ failure-path test
+static thread_local int32_t g_gemm1_stalls = 0;
+
+bool take_gemm1_stall() {
+  if (g_gemm1_stalls <= 0) return false;
+  --g_gemm1_stalls;
+  return true;
+}
+
 // ------------------------------------------------------------------ tracing
 static thread_local moe_trace_t* g_trace = nullptr;
 
@@ -150,7 +159,7 @@ static moe_status_t encode_2d(CUtensorMap* m, bool bf16, const void* base, uint6
 // ------------------------------------------------------------------ validation
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-static moe_status_t check_config(const moe_config_t* c) {
+moe_status_t check_config(const moe_config_t* c) {
   if (!c) return fail(MOE_ERR_INVALID_ARG, "cfg is NULL");
   if (c->T < 0) return fail(MOE_ERR_INVALID_ARG, "T = %lld is negative", (long long)c->T);
   if (c->E < 1 || c->E > kMaxExperts)
@@ -179,13 +188,13 @@ static moe_status_t check_config(const moe_config_t* c) {
   return MOE_OK;
 }
 
-static moe_status_t check_ptr(const void* p, const char* name, bool needs16 = true) {
+moe_status_t check_ptr(const void* p, const char* name, bool needs16) {
   if (!p) return fail(MOE_ERR_INVALID_ARG, "%s is NULL", name);
   if (needs16 && !aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
   return MOE_OK;
 }
 
-static moe_status_t check_ptr4(const void* p, const char* name) {
+moe_status_t check_ptr4(const void* p, const char* name) {
   if (!p) return fail(MOE_ERR_INVALID_ARG, "%s is NULL", name);
   if (reinterpret_cast<uintptr_t>(p) & 3) return fail(MOE_ERR_INVALID_ARG, "%s is not 4-byte aligned", name);
   return MOE_OK;
@@ -393,6 +402,12 @@ extern "C" {
 
 int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
 
+moe_status_t moe_test_stall_gemm1(int32_t count) {
+  if (count < 0) return fail(MOE_ERR_INVALID_ARG, "count = %d is negative", count);
+  g_gemm1_stalls = count;
+  return MOE_OK;
+}
+
 moe_status_t moe_set_trace(moe_trace_t* trace) {
   if (trace && (!trace->events || !trace->kernel_ids || trace->capacity < 0 || trace->count < 0))
     return fail(MOE_ERR_INVALID_ARG, "trace needs events, kernel_ids and a capacity");
@@ -440,6 +455,8 @@ moe_status_t moe_get_device_error(void* ws, moe_stream_t stream, int32_t* device
   MOE_CUDA(cudaStreamSynchronize(st));
   if (device_bits) *device_bits = static_cast<int32_t>(w);
   if (w & kErrTimeout) return fail(MOE_ERR_DEVICE_TIMEOUT, "a kernel wait timed out (bits 0x%x)", w);
+  if (w & kErrDupIds)
+    return fail(MOE_ERR_BOUNDS, "a token listed the same expert twice among its k ids (bits 0x%x)", w);
   if (w & (kErrBounds | kErrNoSelect))
     return fail(MOE_ERR_BOUNDS, "a kernel met an out-of-range index (bits 0x%x)", w);
   return MOE_OK;
@@ -830,6 +847,7 @@ static moe_status_t run_ffn(const moe_config_t& c, const WeightView& W, const La
   g1.K_shared = c.H;
   g1.N_routed = c.I;
   g1.N_shared = c.I_shared;
+  g1.stall_test = take_gemm1_stall() ? 1 : 0;
   const int grid = gemm_grid();
   trace_mark(st, MOE_K_GEMM1);
   MOE_CUDA(launch_grouped_gemm(true, a0, a1, g1, grid, st));
@@ -839,6 +857,7 @@ static moe_status_t run_ffn(const moe_config_t& c, const WeightView& W, const La
   if (shared) MOE_TRY(encode_2d(&b1, true, hs, c.I_shared, c.T, kTileK, kTileM));
   else b1 = b0;
   GemmArgs g2 = g1;
+  g2.stall_test = 0;
   g2.gather_rows = nullptr;
   g2.b_maps = W.maps2;
   g2.sched = s2;

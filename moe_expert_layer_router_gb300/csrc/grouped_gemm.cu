@@ -70,6 +70,7 @@ struct __align__(8) SmemCtl {
   uint64_t tfull[2];         // both CTAs: an accumulator is complete
   uint64_t tempty[2];        // even CTA: both epilogues drained an accumulator
   uint64_t drain;
+  uint64_t stall;            // failure-path test only: never arrived on
   uint32_t tmem_base;
   int abort;
   int32_t sched[2 * kMaxGroups + 2];
@@ -188,6 +189,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&c.tempty[s], 8);  // 4 epilogue warps in each CTA
     }
     ptx::mbar_init(&c.drain, 1);
+    ptx::mbar_init(&c.stall, 1);
     c.abort = 0;
     ptx::fence_mbar_init();
   }
@@ -307,6 +309,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int acc = local & 1;
         const uint32_t acc_ph = (local >> 1) & 1;
         if (!ptx::mbar_wait(&c.tempty[acc], acc_ph ^ 1, abort, args.err)) break;
+        // failure-path test: before its first tile, pair 0 waits on a barrier
+        // that nothing arrives on; the bounded wait gives up, sets the timeout
+        // bit and the abort flag, and the pair abandons its tiles (every load
+        // already issued still lands and is drained below)
+        if (args.stall_test && pair == 0 && local == 0 &&
+            !ptx::mbar_wait(&c.stall, 0, abort, args.err))
+          break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kTileN;
         const uint32_t idesc = x.half ? kIdescHalf : kIdescFull;

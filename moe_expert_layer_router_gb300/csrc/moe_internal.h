@@ -13,6 +13,7 @@ namespace moe {
 constexpr uint32_t kErrBounds = 1u;    // an index outside its range was skipped
 constexpr uint32_t kErrTimeout = 2u;   // a bounded wait expired
 constexpr uint32_t kErrNoSelect = 4u;  // a token had fewer than k selectable logits (NaN)
+constexpr uint32_t kErrDupIds = 8u;    // a token listed one expert in two of its k slots
 
 // A wait that takes longer than this is treated as a hang: the waiting role
 // records kErrTimeout, raises the CTA's abort flag and leaves its loop.
@@ -73,7 +74,12 @@ struct GemmArgs {
   int32_t T;                   // rows of the shared group
   int32_t K_routed, K_shared;  // reduction sizes
   int32_t N_routed, N_shared;  // output columns
+  int32_t stall_test;          // failure-path test: pair 0 waits on a barrier nothing ends
 };
+
+// Failure-path test hook (moe_test_stall_gemm1): whether the next bf16 GEMM1
+// launch of the calling thread should stall its first CTA pair (consumes one).
+bool take_gemm1_stall();
 
 // fp8 grouped GEMM (weights on the MMA's M side, tokens on N).
 struct Fp8GemmArgs {
@@ -231,7 +237,16 @@ cudaError_t launch_quant_act_nvfp4(const void* x, int64_t M, int64_t K, float g,
 
 }  // namespace moe
 
+#include "../../include/moe_layer.h"
+
 namespace moe {
+// Host-side argument checks shared by every entry point (api.cu): the layer
+// configuration, and a pointer that must be non-null and 16-byte (check_ptr)
+// or 4-byte (check_ptr4) aligned.  A failure sets moe_last_error_message().
+moe_status_t check_config(const moe_config_t* c);
+moe_status_t check_ptr(const void* p, const char* name, bool needs16 = true);
+moe_status_t check_ptr4(const void* p, const char* name);
+
 // Raises a kernel's dynamic shared-memory limit on the current device (once per device).
 cudaError_t ensure_smem_attr(const void* func, int bytes);
 

@@ -35,16 +35,22 @@ __global__ void __launch_bounds__(kHistThreads)
     hist_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int E, int nblk,
                 int32_t* __restrict__ blk_counts, uint32_t* err) {
   __shared__ int cnt[kMaxExperts];
+  __shared__ int32_t sid[kPermTok * kMaxK];
   for (int e = threadIdx.x; e < E; e += kHistThreads) cnt[e] = 0;
-  __syncthreads();
   const int64_t t0 = int64_t(blockIdx.x) * kPermTok;
   const int n = static_cast<int>(T - t0 < kPermTok ? T - t0 : kPermTok) * k;
   const int32_t* src = ids + t0 * k;
+  for (int i = threadIdx.x; i < n; i += kHistThreads) sid[i] = src[i];
+  __syncthreads();
+  bool dup = false;
   for (int i = threadIdx.x; i < n; i += kHistThreads) {
-    const int e = src[i];
+    const int e = sid[i];
     if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) atomicAdd(&cnt[e], 1);
     else atomicOr(err, kErrBounds);
+    // a token must list k distinct experts: compare with its earlier slots
+    for (int j = i - i % k; j < i; ++j) dup |= sid[j] == e;
   }
+  if (dup) atomicOr(err, kErrDupIds);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += kHistThreads) blk_counts[int64_t(e) * nblk + blockIdx.x] = cnt[e];
 }

@@ -14,9 +14,13 @@
 // library is loaded holds kNoAllocScratchBytes of it until the process
 // exits.  Host code may not use the symbol itself as a device pointer (on the
 // host it names a shadow object, not GPU memory), so its device address is
-// looked up with cudaGetSymbolAddress once per device, on the first call made
-// while that device is current.  Make that first call before any stream
-// capture starts.
+// looked up with cudaGetSymbolAddress in the CUDA context that is current at
+// the call.  The lookup is cheap and is repeated on every call made outside a
+// stream capture, so a context that was destroyed and re-created (for example
+// after cudaDeviceReset) never reaches a stale address.  A call made while its
+// stream is being captured cannot look anything up; it uses the address found
+// by the last call outside capture in the same context, so make one call in
+// each context (device) before any stream capture starts.
 //
 // All calls share the one array, and it keeps whatever the previous call left
 // in it.  The kernels overwrite every count and base they read, and the call
@@ -27,6 +31,7 @@
 
 #include <cstdio>
 #include <mutex>
+#include <unordered_map>
 
 #include "../../include/moe_layer.h"
 #include "moe_internal.h"
@@ -43,40 +48,61 @@ constexpr size_t kNoAllocScratchBytes =
 
 static __device__ __align__(256) uint8_t g_permute_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-uint8_t* g_scratch_addr[kMaxDevices] = {};
+std::unordered_map<CUcontext, uint8_t*> g_scratch_addr;  // by CUDA context
 
 moe_status_t report(moe_status_t s, const char* msg) {
   set_last_error_text(msg);
   return s;
 }
 
-// Device address of g_permute_scratch on the current device (looked up once).
-moe_status_t scratch_address(uint8_t** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return report(MOE_ERR_CUDA, cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices)
-    return report(MOE_ERR_UNSUPPORTED, "moe_permute_noalloc: device index above 63");
-  std::lock_guard<std::mutex> g(g_mu);
-  if (!g_scratch_addr[dev]) {
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// The calling thread's current CUDA context (null if it cannot be read).
+CUcontext current_context() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_permute_scratch);
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  CUcontext c = nullptr;
+  if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
+  return c;
+}
+
+// Device address of g_permute_scratch in the current context: looked up afresh
+// outside stream capture, taken from the last lookup in this context during one.
+moe_status_t scratch_address(cudaStream_t st, uint8_t** out) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const cudaError_t qe = cudaStreamIsCapturing(st, &cs);
+  if (qe != cudaSuccess) (void)cudaGetLastError();  // the query's own error is not the caller's
+  const bool capturing = qe != cudaSuccess || cs != cudaStreamCaptureStatusNone;
+  const CUcontext ctx = current_context();
+  std::lock_guard<std::mutex> g(g_mu);
+  if (!capturing) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_permute_scratch);
     if (e != cudaSuccess || !p) {
       char buf[256];
       snprintf(buf, sizeof buf, "moe_permute_noalloc: cudaGetSymbolAddress failed: %s",
                cudaGetErrorString(e));
       return report(MOE_ERR_CUDA, buf);
     }
-    g_scratch_addr[dev] = static_cast<uint8_t*>(p);
+    g_scratch_addr[ctx] = static_cast<uint8_t*>(p);
   }
-  *out = g_scratch_addr[dev];
+  auto it = g_scratch_addr.find(ctx);
+  if (it == g_scratch_addr.end())
+    return report(MOE_ERR_INVALID_ARG,
+                  "moe_permute_noalloc: first call in this context made during a stream capture; "
+                  "call it once before capturing");
+  *out = it->second;
   return MOE_OK;
 }
-
-bool ok4(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
-bool ok16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
 }  // namespace moe
@@ -88,12 +114,10 @@ extern "C" MOE_API moe_status_t moe_permute_noalloc(
     int32_t* expert_counts, int32_t* expert_offsets, int32_t* perm_token, int32_t* inv_row,
     float* row_weight, void* x_perm, float* x_perm_scales, uint32_t* device_status,
     moe_stream_t stream) {
-  if (!cfg) return report(MOE_ERR_INVALID_ARG, "moe_permute_noalloc: cfg is NULL");
-  if (cfg->T < 0 || cfg->E < 1 || cfg->E > kMaxExperts || cfg->k < 1 || cfg->k > cfg->E ||
-      cfg->k > 16 || cfg->H < 128 || cfg->H % 128 ||
-      (cfg->wtype != MOE_DTYPE_BF16 && cfg->wtype != MOE_DTYPE_FP8_E4M3) ||
-      cfg->T * int64_t(cfg->k) >= (int64_t(1) << 31))
-    return report(MOE_ERR_INVALID_ARG, "moe_permute_noalloc: invalid layer configuration");
+  moe_status_t s = check_config(cfg);
+  if (s != MOE_OK) return s;
+  if (cfg->wtype == MOE_DTYPE_NVFP4)
+    return report(MOE_ERR_UNSUPPORTED, "NVFP4 layers run through moe_forward / moe_forward_stack");
   const int64_t nblk = (cfg->T + kPermTok - 1) / kPermTok;
   if (nblk * cfg->E > kNoAllocMaxEntries) {
     char buf[256];
@@ -103,28 +127,32 @@ extern "C" MOE_API moe_status_t moe_permute_noalloc(
              static_cast<long long>(nblk * cfg->E), static_cast<long long>(kNoAllocMaxEntries));
     return report(MOE_ERR_UNSUPPORTED, buf);
   }
-  if (!ok4(expert_counts) || !ok4(expert_offsets))
-    return report(MOE_ERR_INVALID_ARG, "moe_permute_noalloc: counts/offsets NULL or misaligned");
-  if (device_status && !ok4(device_status))
-    return report(MOE_ERR_INVALID_ARG, "moe_permute_noalloc: device_status misaligned");
+  if ((s = check_ptr4(expert_counts, "expert_counts")) != MOE_OK) return s;
+  if ((s = check_ptr4(expert_offsets, "expert_offsets")) != MOE_OK) return s;
+  if (device_status && (s = check_ptr4(device_status, "device_status")) != MOE_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (cfg->T == 0) {
     cudaError_t e = cudaMemsetAsync(expert_counts, 0, size_t(cfg->E) * 4, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(expert_offsets, 0, size_t(cfg->E + 1) * 4, st);
     return e == cudaSuccess ? MOE_OK : report(MOE_ERR_CUDA, cudaGetErrorString(e));
   }
-  if (!ok4(topk_ids) || !ok4(perm_token) || !ok4(inv_row))
-    return report(MOE_ERR_INVALID_ARG, "moe_permute_noalloc: ids/perm/inv NULL or misaligned");
-  if (row_weight && (!ok4(row_weight) || !ok4(topk_w)))
-    return report(MOE_ERR_INVALID_ARG, "moe_permute_noalloc: row_weight needs aligned topk_w");
-  if (x_perm && (!ok16(x) || !ok16(x_perm)))
-    return report(MOE_ERR_INVALID_ARG, "moe_permute_noalloc: x / x_perm NULL or misaligned");
-  if (x_perm && cfg->wtype == MOE_DTYPE_FP8_E4M3 && !ok4(x_perm_scales))
-    return report(MOE_ERR_INVALID_ARG, "moe_permute_noalloc: fp8 needs x_perm_scales");
+  if ((s = check_ptr4(topk_ids, "topk_ids")) != MOE_OK) return s;
+  if ((s = check_ptr4(perm_token, "perm_token")) != MOE_OK) return s;
+  if ((s = check_ptr4(inv_row, "inv_row")) != MOE_OK) return s;
+  if (row_weight) {
+    if ((s = check_ptr4(row_weight, "row_weight")) != MOE_OK) return s;
+    if (!topk_w) return report(MOE_ERR_INVALID_ARG, "row_weight needs topk_w");
+    if ((s = check_ptr4(topk_w, "topk_w")) != MOE_OK) return s;
+  }
+  if (x_perm) {
+    if ((s = check_ptr(x, "x")) != MOE_OK) return s;
+    if ((s = check_ptr(x_perm, "x_perm")) != MOE_OK) return s;
+    if (cfg->wtype == MOE_DTYPE_FP8_E4M3 && (s = check_ptr4(x_perm_scales, "x_perm_scales")) != MOE_OK)
+      return s;
+  }
 
   uint8_t* base = nullptr;
-  moe_status_t s = scratch_address(&base);
-  if (s != MOE_OK) return s;
+  if ((s = scratch_address(st, &base)) != MOE_OK) return s;
   uint32_t* own_status = reinterpret_cast<uint32_t*>(base);
   int32_t* blk_counts = reinterpret_cast<int32_t*>(base + kNoAllocStatusBytes);
   int32_t* blk_base = blk_counts + kNoAllocMaxEntries;

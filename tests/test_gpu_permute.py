@@ -111,3 +111,19 @@ def test_permute_reports_bad_ids():
     with pytest.raises(m.MoeError, match="out-of-range"):
         m.moe_get_device_error(ws)
     assert m.moe_get_device_error(ws) == 0          # cleared after reading
+
+
+def test_permute_reports_repeated_ids():
+    """A token that lists one expert in two slots is flagged (status bit 3):
+    every row index stays in range, but one row of that expert is not written."""
+    dev = torch.device("cuda")
+    lc = wl.TINY.with_(T=130, E=8, k=3, H=128)
+    cfg = m.config_from(lc)
+    ids = np.tile(np.array([0, 1, 2]), (130, 1)).astype(np.int32)
+    ids[77, 2] = 0
+    ws = m.Workspace(cfg, "permute")
+    m.moe_permute(cfg, torch.from_numpy(ids).to(dev), ws=ws)
+    torch.cuda.synchronize()
+    with pytest.raises(m.MoeError, match="same expert twice"):
+        m.moe_get_device_error(ws)
+    assert m.moe_get_device_error(ws) == 0

@@ -66,3 +66,39 @@ def test_concurrent_streams_with_separate_workspaces():
     for i in (0, 1):
         assert torch.equal(outs[i], refs[i])
         assert m.moe_get_device_error(wss[i]) == 0
+
+
+def test_a_wait_that_runs_out_is_reported_and_the_next_call_recovers():
+    """Failure detection on the GPU without a fault: the test hook makes the first
+    CTA pair of GEMM1 wait on a barrier that nothing signals.  The bounded wait
+    gives up (2 s), the pair abandons its tiles, drains its loads and frees its
+    tensor memory, and the status word reports the timeout; the next call on the
+    same workspace matches the oracle."""
+    from moe_expert_layer_router_gb300 import _native as N
+    from oracle import moe as om
+    from parity import Routing, assert_close_layer, f64, with_flips
+
+    dev = torch.device("cuda")
+    lc = LC.with_(name="stall", T=600)
+    L = Layer(lc, dev)
+    cfg = m.config_from(lc)
+    W = weights_of(L, cfg)
+    ws = m.Workspace(cfg, "forward")
+    N.check(N.lib().moe_test_stall_gemm1(1), "moe_test_stall_gemm1")
+    try:
+        m.moe_forward(cfg, W, L.x, L.wr, L.bias, ws=ws)
+        torch.cuda.synchronize()
+        with pytest.raises(m.MoeError) as ei:
+            m.moe_get_device_error(ws)
+        assert ei.value.status == N.MOE_ERR_DEVICE_TIMEOUT
+    finally:
+        N.lib().moe_test_stall_gemm1(0)
+    out, ids, _ = m.moe_forward(cfg, W, L.x, L.wr, L.bias, ws=ws, return_routing=True)
+    torch.cuda.synchronize()
+    assert m.moe_get_device_error(ws) == 0
+    r = Routing(lc.name, lc, cfg, L.x, L.wr, L.bias, ids.cpu().numpy(), m)
+    ref = om.moe_layer(f64(L.x), f64(L.wr), None, L.experts_cpu, L.shared_cpu(), lc.k, lc.score,
+                       lc.renormalize, lc.route_scale)
+    ref_out = with_flips(r, ref["out"], lambda t, i, w_: om.moe_tokens(
+        f64(L.x)[t], i, w_, L.experts_cpu, L.shared_cpu()))
+    assert_close_layer(out, ref_out, what="after the stalled call")
