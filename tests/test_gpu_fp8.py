@@ -9,7 +9,8 @@ import moe_expert_layer_router_gb300 as m
 import workload as wl
 from oracle import fp8 as of8
 from oracle import moe as om
-from parity import FP8_MAX_OVER_RMS, Routing, assert_close_layer, check_sampled, f64, with_flips
+from parity import (FP8_MAX_OVER_RMS, Case, Routing, assert_close_layer, f64, family_parity,
+                    with_flips)
 
 pytestmark = pytest.mark.gpu
 
