@@ -271,6 +271,65 @@ MOE_API moe_status_t moe_grouped_ffn(const moe_config_t* cfg, moe_weights_t weig
                              const float* x_shared_scales, void* y_perm, void* shared_out,
                              void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* NVFP4 layers (MOE_DTYPE_NVFP4, the DeepSeek-R1 NVFP4 expert weights of
+ * "DWDP: Distributed Weight Data Parallelism for High-Performance LLM
+ * Inference on NVL72", section A4) run the two middle steps through the next
+ * two calls: their permuted rows are NVFP4 codes in expert segments padded to
+ * whole 128-row blocks.  moe_route and moe_combine are the same calls as for
+ * bf16 layers, and the four calls give the bits of moe_forward.
+ *
+ * Row counts of the NVFP4 step buffers: *padded_rows (T*k + 127*E, rounded up
+ * to 128: room for every expert's padded segment) and *padded_tokens (T
+ * rounded up to 128: the token-order copy for the shared expert).  Either
+ * pointer may be NULL. */
+MOE_API moe_status_t moe_nvfp4_rows(const moe_config_t* cfg, int64_t* padded_rows,
+                                    int64_t* padded_tokens);
+
+/* Step 2 for NVFP4 layers -- histogram and permutation as moe_permute, with
+ * every token quantised once with the layer's static input scale g_x (held by
+ * `weights`) and its codes written to its k rows.
+ *   weights         the layer's NVFP4 weights (moe_weights_create)
+ *   expert_counts, expert_offsets, perm_token, inv_row, row_weight: as
+ *                   moe_permute (unpadded row order)
+ *   pad_offsets     int32 [E+1] out: expert e's rows are x_perm rows
+ *                   [pad_offsets[e], pad_offsets[e] + counts[e]); the segment
+ *                   ends at pad_offsets[e+1], a multiple of 128
+ *   x_perm          uint8 [padded_rows, H/2] out: E2M1 codes, two per byte
+ *                   (element 2i in the low nibble of byte i); 16-byte aligned
+ *   x_perm_sf       uint8 [padded_rows * H/16] out: the e4m3 block scales in
+ *                   the MMA scale layout (512-byte atoms of 128 rows x 4
+ *                   16-element blocks); padding rows get scale 0
+ *   x_tok, x_tok_sf the same for the tokens in token order ([padded_tokens,
+ *                   H/2] and [padded_tokens * H/16]): the shared expert's
+ *                   input; NULL skips it
+ * Workspace: moe_workspace_size(cfg, MOE_OP_PERMUTE). */
+MOE_API moe_status_t moe_permute_nvfp4(const moe_config_t* cfg, moe_weights_t weights,
+                                       const int32_t* topk_ids, const float* topk_w,
+                                       const void* x, int32_t* expert_counts,
+                                       int32_t* expert_offsets, int32_t* pad_offsets,
+                                       int32_t* perm_token, int32_t* inv_row, float* row_weight,
+                                       uint8_t* x_perm, uint8_t* x_perm_sf, uint8_t* x_tok,
+                                       uint8_t* x_tok_sf, void* ws, size_t ws_bytes,
+                                       moe_stream_t stream);
+
+/* Steps 3+4 for NVFP4 layers -- the grouped expert FFN on the outputs of
+ * moe_permute_nvfp4: h = silu(x W_gate^T) * (x W_up^T) quantised to NVFP4 with
+ * the layer's static g_h, then y = row_weight * (h W_down^T).
+ *   y_perm      fp32 [T*k, H] out, unpadded row order (as moe_grouped_ffn)
+ *   shared_out  fp32 [T, H] out, or NULL (skips the shared expert; needs
+ *               x_tok / x_tok_sf otherwise)
+ *   row_weight  fp32 [T*k] or NULL (all ones)
+ * The expert rows are produced as fp16 with a power-of-two scale per 32
+ * columns, as in moe_forward, and widened exactly to fp32.
+ * Workspace: moe_workspace_size(cfg, MOE_OP_GROUPED_FFN). */
+MOE_API moe_status_t moe_grouped_ffn_nvfp4(const moe_config_t* cfg, moe_weights_t weights,
+                                           const uint8_t* x_perm, const uint8_t* x_perm_sf,
+                                           const int32_t* expert_offsets,
+                                           const int32_t* pad_offsets, const float* row_weight,
+                                           const uint8_t* x_tok, const uint8_t* x_tok_sf,
+                                           float* y_perm, float* shared_out, void* ws,
+                                           size_t ws_bytes, moe_stream_t stream);
+
 /* Step 5 -- combine: out[t] = sum_j y_perm[inv_row[t, j]] (+ shared_out[t]),
  * summed in fp32 in slot order j = 0..k-1, then the shared row, rounded to bf16.
  *   y_perm fp32 [T*k, H], inv_row int32 [T, k], shared_out fp32 [T, H] or NULL,

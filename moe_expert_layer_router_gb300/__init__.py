@@ -22,6 +22,7 @@ from ._native import MoeConfig, MoeError
 
 __all__ = ["MoeConfig", "MoeError", "make_config", "config_from", "Workspace", "ExpertWeights",
            "moe_route", "moe_permute", "moe_permute_noalloc", "moe_grouped_ffn", "moe_combine",
+           "moe_nvfp4_rows", "moe_permute_nvfp4", "moe_grouped_ffn_nvfp4",
            "moe_forward", "LayerStack", "moe_forward_stack",
            "moe_quantize_weight_fp8", "moe_quantize_act_fp8", "moe_get_device_error",
            "moe_workspace_size", "load", "Nvfp4ExpertWeights", "moe_quantize_weight_nvfp4",
@@ -387,6 +388,69 @@ def moe_grouped_ffn(cfg: MoeConfig, weights: ExpertWeights, x_perm, expert_offse
                                     _ptr(x_perm_scales), _ptr(expert_offsets), _ptr(row_weight),
                                     _ptr(x_shared), _ptr(x_shared_scales), _ptr(y), _ptr(s),
                                     ws.ptr, ws.nbytes, _stream(stream)), "moe_grouped_ffn")
+    return y, s
+
+
+def moe_nvfp4_rows(cfg: MoeConfig) -> tuple[int, int]:
+    """(padded_rows, padded_tokens) of the NVFP4 step buffers of a layer."""
+    r, t = C.c_int64(0), C.c_int64(0)
+    N.check(N.lib().moe_nvfp4_rows(C.byref(cfg), C.byref(r), C.byref(t)), "moe_nvfp4_rows")
+    return int(r.value), int(t.value)
+
+
+def moe_permute_nvfp4(cfg: MoeConfig, weights, topk_ids, topk_w, x, *, shared=True, ws=None,
+                      stream=None):
+    """Histogram + permutation of an NVFP4 layer: the moe_permute outputs plus
+    pad_offsets, x_perm (E2M1 codes over the 128-row-padded expert segments),
+    x_perm_sf (their MMA-layout scales) and, with ``shared``, the token-order
+    copy x_tok / x_tok_sf for the shared expert."""
+    dev = topk_ids.device
+    T, k, E, H = cfg.T, cfg.k, cfg.E, cfg.H
+    R = T * k
+    Rp, Tp = moe_nvfp4_rows(cfg)
+    _need(topk_ids, "topk_ids", torch.int32, (T, k), dev)
+    _need(topk_w, "topk_w", torch.float32, (T, k), dev)
+    _need(x, "x", torch.bfloat16, (T, H), dev)
+    sh = shared and cfg.I_shared > 0
+    o = {"expert_counts": torch.empty(E, dtype=torch.int32, device=dev),
+         "expert_offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+         "pad_offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+         "perm_token": torch.empty(R, dtype=torch.int32, device=dev),
+         "inv_row": torch.empty(T, k, dtype=torch.int32, device=dev),
+         "row_weight": torch.empty(R, dtype=torch.float32, device=dev),
+         "x_perm": torch.empty(Rp, H // 2, dtype=torch.uint8, device=dev),
+         "x_perm_sf": torch.empty(Rp * H // 16, dtype=torch.uint8, device=dev),
+         "x_tok": torch.empty(Tp, H // 2, dtype=torch.uint8, device=dev) if sh else None,
+         "x_tok_sf": torch.empty(Tp * H // 16, dtype=torch.uint8, device=dev) if sh else None}
+    ws = _ws(ws, cfg, "permute", dev)
+    N.check(N.lib().moe_permute_nvfp4(
+        C.byref(cfg), weights.handle, _ptr(topk_ids), _ptr(topk_w), _ptr(x),
+        _ptr(o["expert_counts"]), _ptr(o["expert_offsets"]), _ptr(o["pad_offsets"]),
+        _ptr(o["perm_token"]), _ptr(o["inv_row"]), _ptr(o["row_weight"]), _ptr(o["x_perm"]),
+        _ptr(o["x_perm_sf"]), _ptr(o["x_tok"]), _ptr(o["x_tok_sf"]), ws.ptr, ws.nbytes,
+        _stream(stream)), "moe_permute_nvfp4")
+    return o
+
+
+def moe_grouped_ffn_nvfp4(cfg: MoeConfig, weights, p, row_weight=None, *, shared=True, ws=None,
+                          stream=None):
+    """Grouped SwiGLU experts of an NVFP4 layer on the outputs ``p`` of
+    moe_permute_nvfp4.  Returns (y_perm fp32 [T*k,H], shared_out fp32 [T,H] or None)."""
+    dev = p["x_perm"].device
+    T, k, H = cfg.T, cfg.k, cfg.H
+    if row_weight is not None:
+        _need(row_weight, "row_weight", torch.float32, (T * k,), dev)
+    y = torch.empty(T * k, H, dtype=torch.float32, device=dev)
+    s = None
+    if shared and cfg.I_shared > 0 and p.get("x_tok") is not None:
+        s = torch.empty(T, H, dtype=torch.float32, device=dev)
+    ws = _ws(ws, cfg, "grouped_ffn", dev)
+    N.check(N.lib().moe_grouped_ffn_nvfp4(
+        C.byref(cfg), weights.handle, _ptr(p["x_perm"]), _ptr(p["x_perm_sf"]),
+        _ptr(p["expert_offsets"]), _ptr(p["pad_offsets"]), _ptr(row_weight),
+        _ptr(p["x_tok"]) if s is not None else None,
+        _ptr(p["x_tok_sf"]) if s is not None else None, _ptr(y), _ptr(s), ws.ptr, ws.nbytes,
+        _stream(stream)), "moe_grouped_ffn_nvfp4")
     return y, s
 
 

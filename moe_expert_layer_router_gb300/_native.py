@@ -76,6 +76,11 @@ _SIG = {
     "moe_quantize_act_nvfp4": (C.c_int, [_P, C.c_int64, C.c_int64, C.c_float, _P, _P, _P]),
     "moe_set_trace": (C.c_int, [C.POINTER(MoeTrace)]),
     "moe_test_stall_gemm1": (C.c_int, [C.c_int32]),
+    "moe_nvfp4_rows": (C.c_int, [_CFG, C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
+    "moe_permute_nvfp4": (C.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                    _P, C.c_size_t, _P]),
+    "moe_grouped_ffn_nvfp4": (C.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                        C.c_size_t, _P]),
     "moe_permute_noalloc": (C.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 

@@ -263,6 +263,12 @@ static Layout layout(const moe_config_t& c, int op) {
       L.h_sc = take(Rp * c.I / 16);
       L.hs_sc = take(Tp * c.I_shared / 16);
     }
+    if (op == MOE_OP_GROUPED_FFN) {
+      // the expert outputs as fp16 + power-of-two scales per 32 columns, widened
+      // into the caller's fp32 rows by the last kernel of the call
+      L.y_perm = take(size_t(R) * c.H * 2 + size_t(R) * (c.H / 32) * 4);
+      L.shared_out = take(size_t(T) * c.H * 2 + size_t(T) * (c.H / 32) * 4);
+    }
     if (op == MOE_OP_FORWARD) {
       L.ids = take(size_t(R) * 4);
       L.w = take(size_t(R) * 4);
@@ -953,44 +959,56 @@ static moe_status_t run_ffn_fp8(const moe_config_t& c, const WeightView& W, cons
   return MOE_OK;
 }
 
-// NVFP4: histogram, scan (with the 128-row padded offsets) and the quantising
-// scatter; then the tile plan, GEMM1 (NVFP4 h + scales) and GEMM2 (fp16 y with
-// power-of-two scales per 32 columns, unpadded rows).
-static moe_status_t run_nvfp4(const moe_config_t& c, const WeightView& W, const Layout& L, void* ws,
-                              const void* x, const int32_t* ids, const float* topk_w,
-                              int32_t* counts, int32_t* offsets, int32_t* perm_token,
-                              int32_t* inv_row, float* row_weight, void* y, float* y_sc,
-                              void* shared_out, float* sh_sc, cudaStream_t st) {
-  uint32_t* err = err_word(ws);
-  const bool shared = c.I_shared > 0;
-  const int64_t R = c.T * c.k;
-  const int64_t Rp = nvfp4_rows(c), Tp = nvfp4_tokens(c);
+// NVFP4 permuted activations: the 128-row-padded expert segments and the
+// token-order copy for the shared expert (codes + MMA-layout scales each).
+struct Nvfp4Acts {
+  int32_t* pad_offsets;  // [E+1]
+  uint8_t* x;            // [Rp, H/2]
+  uint8_t* x_sf;         // Rp * H/16 bytes
+  uint8_t* xs;           // [Tp, H/2] or null
+  uint8_t* xs_sf;
+};
+
+// NVFP4 permutation: histogram, scan (with the 128-row padded offsets) and the
+// quantising scatter.
+static moe_status_t run_permute_nvfp4(const moe_config_t& c, const WeightView& W,
+                                      int32_t* blk_counts, int32_t* blk_base, uint32_t* err,
+                                      const void* x, const int32_t* ids, const float* topk_w,
+                                      int32_t* counts, int32_t* offsets, int32_t* perm_token,
+                                      int32_t* inv_row, float* row_weight, const Nvfp4Acts& A,
+                                      cudaStream_t st) {
   const int nblk = static_cast<int>((c.T + kPermTok - 1) / kPermTok);
-  int32_t* blk_counts = at<int32_t*>(ws, L.blk_counts);
-  int32_t* blk_base = at<int32_t*>(ws, L.blk_base);
-  int32_t* pad_offsets = at<int32_t*>(ws, L.pad_offsets);
-  uint8_t* xq = at<uint8_t*>(ws, L.x_perm);
-  uint8_t* xq_sf = at<uint8_t*>(ws, L.x_perm_sc);
-  uint8_t* xs = shared ? at<uint8_t*>(ws, L.xq) : nullptr;
-  uint8_t* xs_sf = shared ? at<uint8_t*>(ws, L.xq_sc) : nullptr;
   trace_mark(st, MOE_K_HIST);
   MOE_CUDA(launch_hist(ids, c.T, c.k, c.E, blk_counts, err, st));
   trace_mark(st, MOE_K_SCAN);
-  MOE_CUDA(launch_scan(blk_counts, nblk, c.E, blk_base, counts, offsets, st, pad_offsets));
+  MOE_CUDA(launch_scan(blk_counts, nblk, c.E, blk_base, counts, offsets, st, A.pad_offsets));
   Nvfp4Scatter q{};
-  q.pad_offsets = pad_offsets;
+  q.pad_offsets = A.pad_offsets;
   q.act_scales = W.act;
   q.layer = W.layer;
   q.num_layers = W.num_layers;
-  q.rows_pad = Rp;
-  q.x_codes = xq;
-  q.x_sf = xq_sf;
-  q.xs_codes = xs;
-  q.xs_sf = xs_sf;
+  q.rows_pad = nvfp4_rows(c);
+  q.x_codes = A.x;
+  q.x_sf = A.x_sf;
+  q.xs_codes = A.xs;
+  q.xs_sf = A.xs_sf;
   trace_mark(st, MOE_K_SCATTER);
   MOE_CUDA(launch_scatter_nvfp4(ids, topk_w, x, c.T, c.k, c.E, c.H, blk_base, offsets, perm_token,
                                 inv_row, row_weight, q, err, st));
+  return MOE_OK;
+}
 
+// NVFP4 expert FFN: the tile plan, GEMM1 (NVFP4 h + scales in the workspace)
+// and GEMM2 (fp16 y with power-of-two scales per 32 columns, unpadded rows).
+// A.xs null: no shared-expert group.
+static moe_status_t run_ffn_nvfp4(const moe_config_t& c, const WeightView& W, const Layout& L,
+                                  void* ws, const int32_t* offsets, const Nvfp4Acts& A,
+                                  const float* row_weight, void* y, float* y_sc, void* shared_out,
+                                  float* sh_sc, cudaStream_t st) {
+  uint32_t* err = err_word(ws);
+  const bool shared = c.I_shared > 0 && A.xs != nullptr;
+  const int64_t R = c.T * c.k;
+  const int64_t Rp = nvfp4_rows(c), Tp = nvfp4_tokens(c);
   int32_t* s1 = at<int32_t*>(ws, L.sched1);
   int32_t* s2 = at<int32_t*>(ws, L.sched2);
   uint8_t* h = at<uint8_t*>(ws, L.h);
@@ -1004,8 +1022,8 @@ static moe_status_t run_nvfp4(const moe_config_t& c, const WeightView& W, const 
                        kNvfp4Rows, st));
   const int grid = sm_count();
   CUtensorMap a0, a1;
-  MOE_TRY(encode_2d(&a0, false, xq, c.H / 2, Rp, 128, kNvfp4Rows));
-  if (shared) MOE_TRY(encode_2d(&a1, false, xs, c.H / 2, Tp, 128, kNvfp4Rows));
+  MOE_TRY(encode_2d(&a0, false, A.x, c.H / 2, Rp, 128, kNvfp4Rows));
+  if (shared) MOE_TRY(encode_2d(&a1, false, A.xs, c.H / 2, Tp, 128, kNvfp4Rows));
   else a1 = a0;
   Nvfp4GemmArgs g1{};
   g1.w_maps = W.maps1;
@@ -1016,10 +1034,10 @@ static moe_status_t run_nvfp4(const moe_config_t& c, const WeightView& W, const 
   g1.layer_stride = W.stride;
   g1.num_layers = W.num_layers;
   g1.offsets = offsets;
-  g1.pad_offsets = pad_offsets;
+  g1.pad_offsets = A.pad_offsets;
   g1.sched = s1;
-  g1.a_sf0 = xq_sf;
-  g1.a_sf1 = shared ? xs_sf : xq_sf;
+  g1.a_sf0 = A.x_sf;
+  g1.a_sf1 = shared ? A.xs_sf : A.x_sf;
   g1.out0 = h;
   g1.out1 = hs;
   g1.out_sf0 = h_sf;
@@ -1066,6 +1084,25 @@ static moe_status_t run_nvfp4(const moe_config_t& c, const WeightView& W, const 
   trace_mark(st, MOE_K_GEMM2);
   MOE_CUDA(launch_grouped_gemm_nvfp4(false, b0, b1, y0, y1, g2, grid, st));
   return MOE_OK;
+}
+
+// The whole NVFP4 permutation + expert FFN of the layer forward, in the workspace.
+static moe_status_t run_nvfp4(const moe_config_t& c, const WeightView& W, const Layout& L, void* ws,
+                              const void* x, const int32_t* ids, const float* topk_w,
+                              int32_t* counts, int32_t* offsets, int32_t* perm_token,
+                              int32_t* inv_row, float* row_weight, void* y, float* y_sc,
+                              void* shared_out, float* sh_sc, cudaStream_t st) {
+  const bool shared = c.I_shared > 0;
+  Nvfp4Acts A;
+  A.pad_offsets = at<int32_t*>(ws, L.pad_offsets);
+  A.x = at<uint8_t*>(ws, L.x_perm);
+  A.x_sf = at<uint8_t*>(ws, L.x_perm_sc);
+  A.xs = shared ? at<uint8_t*>(ws, L.xq) : nullptr;
+  A.xs_sf = shared ? at<uint8_t*>(ws, L.xq_sc) : nullptr;
+  MOE_TRY(run_permute_nvfp4(c, W, at<int32_t*>(ws, L.blk_counts), at<int32_t*>(ws, L.blk_base),
+                            err_word(ws), x, ids, topk_w, counts, offsets, perm_token, inv_row,
+                            row_weight, A, st));
+  return run_ffn_nvfp4(c, W, L, ws, offsets, A, row_weight, y, y_sc, shared_out, sh_sc, st);
 }
 
 static bool same_shape(const moe_config_t& a, const moe_config_t& b) {
@@ -1182,7 +1219,7 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, const
                          float* x_perm_scales, void* ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(check_config(cfg));
   if (cfg->wtype == MOE_DTYPE_NVFP4)
-    return fail(MOE_ERR_UNSUPPORTED, "NVFP4 layers run through moe_forward / moe_forward_stack");
+    return fail(MOE_ERR_UNSUPPORTED, "NVFP4 layers permute through moe_permute_nvfp4");
   MOE_TRY(check_ws(*cfg, MOE_OP_PERMUTE, ws, ws_bytes));
   MOE_TRY(check_ptr4(expert_counts, "expert_counts"));
   MOE_TRY(check_ptr4(expert_offsets, "expert_offsets"));
@@ -1220,7 +1257,7 @@ moe_status_t moe_grouped_ffn(const moe_config_t* cfg, moe_weights_t weights, con
                              void* ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(check_config(cfg));
   if (cfg->wtype == MOE_DTYPE_NVFP4)
-    return fail(MOE_ERR_UNSUPPORTED, "NVFP4 layers run through moe_forward / moe_forward_stack");
+    return fail(MOE_ERR_UNSUPPORTED, "NVFP4 layers run their experts through moe_grouped_ffn_nvfp4");
   MOE_TRY(check_ws(*cfg, MOE_OP_GROUPED_FFN, ws, ws_bytes));
   if (!weights) return fail(MOE_ERR_INVALID_ARG, "weights is NULL");
   if (!same_shape(weights->cfg, *cfg))
@@ -1249,6 +1286,109 @@ moe_status_t moe_grouped_ffn(const moe_config_t* cfg, moe_weights_t weights, con
                     shared_out, st);
   trace_mark(st, -1);
   return s;
+}
+
+moe_status_t moe_nvfp4_rows(const moe_config_t* cfg, int64_t* padded_rows, int64_t* padded_tokens) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->wtype != MOE_DTYPE_NVFP4) return fail(MOE_ERR_INVALID_ARG, "not an NVFP4 layer");
+  if (padded_rows) *padded_rows = nvfp4_rows(*cfg);
+  if (padded_tokens) *padded_tokens = nvfp4_tokens(*cfg);
+  return MOE_OK;
+}
+
+moe_status_t moe_permute_nvfp4(const moe_config_t* cfg, moe_weights_t weights,
+                               const int32_t* topk_ids, const float* topk_w, const void* x,
+                               int32_t* expert_counts, int32_t* expert_offsets,
+                               int32_t* pad_offsets, int32_t* perm_token, int32_t* inv_row,
+                               float* row_weight, uint8_t* x_perm, uint8_t* x_perm_sf,
+                               uint8_t* x_tok, uint8_t* x_tok_sf, void* ws, size_t ws_bytes,
+                               moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->wtype != MOE_DTYPE_NVFP4)
+    return fail(MOE_ERR_INVALID_ARG, "moe_permute_nvfp4 takes NVFP4 layers only");
+  MOE_TRY(check_ws(*cfg, MOE_OP_PERMUTE, ws, ws_bytes));
+  if (!weights) return fail(MOE_ERR_INVALID_ARG, "weights is NULL");
+  if (!same_shape(weights->cfg, *cfg))
+    return fail(MOE_ERR_INVALID_ARG, "weights were created for a different layer shape");
+  MOE_TRY(check_ptr4(expert_counts, "expert_counts"));
+  MOE_TRY(check_ptr4(expert_offsets, "expert_offsets"));
+  MOE_TRY(check_ptr4(pad_offsets, "pad_offsets"));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cfg->T == 0) {
+    MOE_CUDA(cudaMemsetAsync(expert_counts, 0, size_t(cfg->E) * 4, st));
+    MOE_CUDA(cudaMemsetAsync(expert_offsets, 0, size_t(cfg->E + 1) * 4, st));
+    MOE_CUDA(cudaMemsetAsync(pad_offsets, 0, size_t(cfg->E + 1) * 4, st));
+    return MOE_OK;
+  }
+  MOE_TRY(check_ptr4(topk_ids, "topk_ids"));
+  MOE_TRY(check_ptr(x, "x"));
+  MOE_TRY(check_ptr4(perm_token, "perm_token"));
+  MOE_TRY(check_ptr4(inv_row, "inv_row"));
+  if (row_weight) {
+    MOE_TRY(check_ptr4(row_weight, "row_weight"));
+    if (!topk_w) return fail(MOE_ERR_INVALID_ARG, "row_weight needs topk_w");
+    MOE_TRY(check_ptr4(topk_w, "topk_w"));
+  }
+  MOE_TRY(check_ptr(x_perm, "x_perm"));
+  MOE_TRY(check_ptr(x_perm_sf, "x_perm_sf"));
+  if (x_tok) MOE_TRY(check_ptr(x_tok_sf, "x_tok_sf"));
+  if (x_tok) MOE_TRY(check_ptr(x_tok, "x_tok"));
+  const Layout L = layout(*cfg, MOE_OP_PERMUTE);
+  Nvfp4Acts A{pad_offsets, x_perm, x_perm_sf, x_tok, x_tok ? x_tok_sf : nullptr};
+  const moe_status_t s = run_permute_nvfp4(
+      *cfg, view_of(weights), at<int32_t*>(ws, L.blk_counts), at<int32_t*>(ws, L.blk_base),
+      err_word(ws), x, topk_ids, topk_w, expert_counts, expert_offsets, perm_token, inv_row,
+      row_weight, A, st);
+  trace_mark(st, -1);
+  return s;
+}
+
+moe_status_t moe_grouped_ffn_nvfp4(const moe_config_t* cfg, moe_weights_t weights,
+                                   const uint8_t* x_perm, const uint8_t* x_perm_sf,
+                                   const int32_t* expert_offsets, const int32_t* pad_offsets,
+                                   const float* row_weight, const uint8_t* x_tok,
+                                   const uint8_t* x_tok_sf, float* y_perm, float* shared_out,
+                                   void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->wtype != MOE_DTYPE_NVFP4)
+    return fail(MOE_ERR_INVALID_ARG, "moe_grouped_ffn_nvfp4 takes NVFP4 layers only");
+  MOE_TRY(check_ws(*cfg, MOE_OP_GROUPED_FFN, ws, ws_bytes));
+  if (!weights) return fail(MOE_ERR_INVALID_ARG, "weights is NULL");
+  if (!same_shape(weights->cfg, *cfg))
+    return fail(MOE_ERR_INVALID_ARG, "weights were created for a different layer shape");
+  if (cfg->T == 0) return MOE_OK;
+  MOE_TRY(check_ptr(x_perm, "x_perm"));
+  MOE_TRY(check_ptr(x_perm_sf, "x_perm_sf"));
+  MOE_TRY(check_ptr4(expert_offsets, "expert_offsets"));
+  MOE_TRY(check_ptr4(pad_offsets, "pad_offsets"));
+  MOE_TRY(check_ptr(y_perm, "y_perm"));
+  if (row_weight) MOE_TRY(check_ptr4(row_weight, "row_weight"));
+  const bool shared = cfg->I_shared > 0 && shared_out != nullptr;
+  if (shared) {
+    MOE_TRY(check_ptr(shared_out, "shared_out"));
+    MOE_TRY(check_ptr(x_tok, "x_tok"));
+    MOE_TRY(check_ptr(x_tok_sf, "x_tok_sf"));
+  }
+  const Layout L = layout(*cfg, MOE_OP_GROUPED_FFN);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t R = cfg->T * cfg->k;
+  // GEMM2 writes fp16 rows + power-of-two scales into the workspace; they are
+  // widened exactly into the caller's fp32 rows
+  void* y16 = at<void*>(ws, L.y_perm);
+  float* y_sc = reinterpret_cast<float*>(static_cast<uint8_t*>(y16) + size_t(R) * cfg->H * 2);
+  void* s16 = shared ? at<void*>(ws, L.shared_out) : nullptr;
+  float* s_sc = shared ? reinterpret_cast<float*>(static_cast<uint8_t*>(s16) +
+                                                  size_t(cfg->T) * cfg->H * 2)
+                       : nullptr;
+  Nvfp4Acts A{const_cast<int32_t*>(pad_offsets), const_cast<uint8_t*>(x_perm),
+              const_cast<uint8_t*>(x_perm_sf), shared ? const_cast<uint8_t*>(x_tok) : nullptr,
+              shared ? const_cast<uint8_t*>(x_tok_sf) : nullptr};
+  MOE_TRY(run_ffn_nvfp4(*cfg, view_of(weights), L, ws, expert_offsets, A, row_weight, y16, y_sc,
+                        s16, s_sc, st));
+  MOE_CUDA(launch_widen_half(y16, y_sc, y_perm, R, cfg->H, st));
+  if (shared) MOE_CUDA(launch_widen_half(s16, s_sc, shared_out, cfg->T, cfg->H, st));
+  trace_mark(st, -1);
+  return MOE_OK;
 }
 
 moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm, const int32_t* inv_row,

@@ -139,6 +139,34 @@ __global__ void __launch_bounds__(kThreads, 8)
   }
 }
 
+// fp16 rows with a power-of-two scale per 32 columns widened to fp32 rows:
+// each value is h * s exactly (the step interface of NVFP4 layers hands fp32
+// expert rows to the combine).  One thread per 8 columns, grid-stride.
+__global__ void __launch_bounds__(256)
+    widen_half_kernel(const uint4* __restrict__ y, const float* __restrict__ ysc,
+                      float4* __restrict__ out, int64_t rows, int H) {
+  const int nch = H / 8;
+  const int nsc = H / 32;
+  const int64_t n = rows * nch;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = i / nch;
+    const int c = static_cast<int>(i - r * nch);
+    const uint4 v = __ldcs(y + i);
+    const float s = __ldg(ysc + r * nsc + (c >> 2));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float f[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+      f[2 * j] = h.x * s;
+      f[2 * j + 1] = h.y * s;
+    }
+    out[2 * i] = make_float4(f[0], f[1], f[2], f[3]);
+    out[2 * i + 1] = make_float4(f[4], f[5], f[6], f[7]);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_combine_half(const void* y, const float* y_scales, const int32_t* inv_row,
@@ -157,6 +185,21 @@ cudaError_t launch_combine(const void* y_perm, const int32_t* inv_row, const voi
   combine_kernel<<<static_cast<unsigned>(T), kThreads, 0, stream>>>(
       static_cast<const float4*>(y_perm), inv_row, static_cast<const float4*>(shared_out),
       static_cast<uint4*>(out), k, H, R, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_widen_half(const void* y, const float* scales, float* out, int64_t rows, int H,
+                              cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t n = rows * (H / 8);
+  int64_t grid = (n + 255) / 256;
+  const int64_t cap = int64_t(sms > 0 ? sms : 1) * 8;
+  if (grid > cap) grid = cap;
+  widen_half_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+      static_cast<const uint4*>(y), scales, reinterpret_cast<float4*>(out), rows, H);
   return cudaGetLastError();
 }
 

@@ -49,7 +49,10 @@
 namespace moe {
 namespace {
 
-constexpr int kStages = 5;
+// Ring depth of each GEMM (stages of 32 KB per CTA).
+constexpr int kStagesG1 = 5;
+constexpr int kStagesG2 = 5;
+constexpr int kStages = kStagesG1 > kStagesG2 ? kStagesG1 : kStagesG2;  // barrier arrays
 constexpr int kThreads = 192;
 constexpr int kPairRows = kGemmTileRows;      // 256 rows per pair tile (128 per CTA)
 static_assert(kPairRows == 2 * kTileM, "a pair tile is two CTA tiles");
@@ -80,8 +83,12 @@ struct __align__(8) SmemCtl {
 // Epilogue staging: each epilogue warp transposes its 32 rows x 32 columns
 // through shared memory so global stores cover whole lines of a few rows.
 constexpr int kStageOutBytes = 4096;  // per epilogue warp (32 rows x 128 B)
-constexpr size_t kSmemBytes =
-    1024 + size_t(kStages) * kStageBytes + 4 * kStageOutBytes + sizeof(SmemCtl);
+template <bool kSwiGLU>
+constexpr int stages_of() { return kSwiGLU ? kStagesG1 : kStagesG2; }
+template <bool kSwiGLU>
+constexpr size_t smem_bytes() {
+  return 1024 + size_t(stages_of<kSwiGLU>()) * kStageBytes + 4 * kStageOutBytes + sizeof(SmemCtl);
+}
 
 struct Tile {
   int g, m_blk, n_blk, rows, row0, K, N;
@@ -158,6 +165,7 @@ template <bool kSwiGLU>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a0,
                              const __grid_constant__ CUtensorMap map_a1, const GemmArgs args) {
+  constexpr int kStages = stages_of<kSwiGLU>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -509,10 +517,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 template <bool kSwiGLU>
 cudaError_t launch_impl(const CUtensorMap& a0, const CUtensorMap& a1, const GemmArgs& args, int grid,
                         cudaStream_t stream) {
+  constexpr size_t kSmem = smem_bytes<kSwiGLU>();
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(grouped_gemm_bf16_kernel<kSwiGLU>),
-                                   static_cast<int>(kSmemBytes));
+                                   static_cast<int>(kSmem));
   if (e != cudaSuccess) return e;
-  grouped_gemm_bf16_kernel<kSwiGLU><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, args);
+  grouped_gemm_bf16_kernel<kSwiGLU><<<grid, kThreads, kSmem, stream>>>(a0, a1, args);
   return cudaGetLastError();
 }
 
@@ -521,7 +530,7 @@ int max_pairs() {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes<kSwiGLU>();
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
   attr.val.clusterDim.x = 2;
@@ -540,9 +549,9 @@ int max_pairs() {
 int grouped_gemm_grid(int sm_count) {
   // One CTA pair for every pair of SMs that can hold one at the same time.
   ensure_smem_attr(reinterpret_cast<const void*>(grouped_gemm_bf16_kernel<true>),
-                   static_cast<int>(kSmemBytes));
+                   static_cast<int>(smem_bytes<true>()));
   ensure_smem_attr(reinterpret_cast<const void*>(grouped_gemm_bf16_kernel<false>),
-                   static_cast<int>(kSmemBytes));
+                   static_cast<int>(smem_bytes<false>()));
   int pairs = max_pairs<true>();
   const int p2 = max_pairs<false>();
   if (p2 > 0 && (pairs <= 0 || p2 < pairs)) pairs = p2;

@@ -217,6 +217,11 @@ cudaError_t launch_combine_half(const void* y, const float* y_scales, const int3
                                 int64_t T, int k, int H, int64_t R, uint32_t* err,
                                 cudaStream_t stream);
 
+// fp16 rows with one power-of-two scale per 32 columns ([rows][H/32] fp32)
+// widened to fp32 rows: out[r][c] = float(y[r][c]) * scales[r][c / 32] (exact).
+cudaError_t launch_widen_half(const void* y, const float* scales, float* out, int64_t rows, int H,
+                              cudaStream_t stream);
+
 cudaError_t launch_quant_weight_fp8(const float* w, int64_t N, int64_t K, uint8_t* q,
                                     float* scales, cudaStream_t stream);
 

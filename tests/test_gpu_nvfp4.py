@@ -289,3 +289,71 @@ def test_nvfp4_stack_layers_match_single_layer_calls():
                            mean_rel=NVFP4_MEAN_REL, what=f"graph, NVFP4 stack layer {l}")
         assert torch.equal(out, refs[l]), f"graph, layer {l}"
     assert m.moe_get_device_error(ws) == 0
+
+
+# ---------------------------------------------------------------- the step calls
+@pytest.mark.parametrize("lc", [SMALL[0], SMALL[1], SMALL[3], SMALL[4]], ids=lambda c: c.name)
+def test_nvfp4_four_calls_match_forward_and_oracle(lc):
+    """moe_route -> moe_permute_nvfp4 -> moe_grouped_ffn_nvfp4 -> moe_combine: the
+    maps and the padded segments against the oracle's permutation, every
+    quantised row against the oracle's codec, and the output bit-exact against
+    moe_forward (the same fp16 expert rows, widened exactly) and within the
+    NVFP4 bound of the oracle's layer."""
+    dev = torch.device("cuda")
+    L = Nvfp4Layer(lc, dev)
+    cfg = L.cfg
+    out_f, ids_f, w_f = m.moe_forward(cfg, L.weights, L.x, L.wr, L.bias, return_routing=True)
+    ids, w, _ = m.moe_route(cfg, L.x, L.wr, L.bias)
+    p = m.moe_permute_nvfp4(cfg, L.weights, ids, w, L.x)
+    y, s = m.moe_grouped_ffn_nvfp4(cfg, L.weights, p, p["row_weight"])
+    out4 = m.moe_combine(cfg, y, p["inv_row"], s)
+    torch.cuda.synchronize()
+    assert torch.equal(ids, ids_f) and torch.equal(w, w_f)
+    assert torch.equal(out4, out_f), "the four calls differ from moe_forward"
+
+    ids_np = ids.cpu().numpy()
+    counts, offsets = om.expert_histogram(ids_np, lc.E)
+    perm, slot, inv = om.permutation(ids_np, lc.E)
+    pad = np.zeros(lc.E + 1, np.int64)
+    pad[1:] = np.cumsum((counts + 127) // 128 * 128)
+    assert (p["expert_counts"].cpu().numpy() == counts).all()
+    assert (p["expert_offsets"].cpu().numpy() == offsets).all()
+    assert (p["pad_offsets"].cpu().numpy() == pad).all()
+    assert (p["perm_token"].cpu().numpy() == perm).all()
+    assert (p["inv_row"].cpu().numpy() == inv).all()
+    assert (p["row_weight"].cpu().numpy() == w.cpu().numpy()[perm, slot]).all()
+    # quantised rows: routed row r of expert e sits at pad[e] + (r - offsets[e])
+    xq, xs = onv.quantize_blocks(f64(L.x).astype(np.float32), np.float32(L.gx))
+    Rp, Tp = m.moe_nvfp4_rows(cfg)
+    codes, sf = unpack(p["x_perm"]), sf_rowmajor(p["x_perm_sf"], Rp, lc.H)
+    e_of = np.repeat(np.arange(lc.E), counts)
+    dst = pad[e_of] + (np.arange(lc.R) - offsets[e_of])
+    assert (codes[dst] == xq[perm]).all() and (sf[dst] == xs[perm]).all()
+    padding = np.setdiff1d(np.arange(pad[-1]), dst)
+    assert (sf[padding] == 0).all()
+    if lc.I_shared:
+        assert (unpack(p["x_tok"])[:lc.T] == xq).all()
+        assert (sf_rowmajor(p["x_tok_sf"], Tp, lc.H)[:lc.T] == xs).all()
+
+    r = Routing(lc.name, lc, cfg, L.x, L.wr, L.bias, ids_np, m)
+    b = None if L.bias is None else f64(L.bias)
+    ref = onv.moe_layer_nvfp4(f64(L.x), f64(L.wr), b, L.oracle_expert, L.oracle_shared(), lc.k,
+                              lc.score, lc.renormalize, lc.route_scale, L.gx, L.gh)
+    ref_out = with_flips(r, ref["out"], lambda t, i, w_: onv.moe_tokens_nvfp4(
+        f64(L.x)[t], i, w_, L.oracle_expert, L.oracle_shared(), L.gx, L.gh))
+    assert_close_layer(out4, ref_out, max_over_rms=NVFP4_MAX_OVER_RMS, mean_rel=NVFP4_MEAN_REL,
+                       what=f"{lc.name} four calls")
+
+
+def test_nvfp4_step_calls_validate_their_layer():
+    """The bf16 step calls refuse NVFP4 layers (pointing at the NVFP4 calls), and
+    the NVFP4 calls refuse other layers."""
+    dev = torch.device("cuda")
+    lc = SMALL[0]
+    L = Nvfp4Layer(lc, dev)
+    ids, w, _ = m.moe_route(L.cfg, L.x, L.wr)
+    with pytest.raises(m.MoeError, match="moe_permute_nvfp4"):
+        m.moe_permute(L.cfg, ids, w, L.x)
+    bcfg = m.config_from(lc.with_(wtype="bf16"))
+    with pytest.raises(m.MoeError, match="NVFP4"):
+        m.moe_permute_nvfp4(bcfg, L.weights, ids, w, L.x)
