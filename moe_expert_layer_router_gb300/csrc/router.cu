@@ -34,6 +34,11 @@ namespace {
 
 constexpr int kStages = 4;
 constexpr int kThreads = 192;
+// Each token tile walks its K slice starting at a tile-dependent k-step (and
+// wraps around), so that the CTAs running at once do not all read the same
+// router-weight k-block (and the same column offset of their token rows) at
+// the same moment.
+constexpr bool kRotateK = true;
 constexpr int kABytes = kTileM * kTileK * 2;
 constexpr int kMaxBBytes = 256 * kTileK * 2;
 
@@ -226,11 +231,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb_all = a.H / kTileK;
   const int kb0 = static_cast<int>(crank) * kb_all / S;  // this CTA's K slice (S <= kb_all)
   const int kb1 = (static_cast<int>(crank) + 1) * kb_all / S;
+  const int kb_n = kb1 - kb0;
+  const int rot = kRotateK ? static_cast<int>((blockIdx.x / S) % static_cast<unsigned>(kb_n)) : 0;
 
   if (warp == 0) {
     if (lane == 0) {
       uint32_t it = 0;
-      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+      for (int i = 0; i < kb_n; ++i, ++it) {
+        const int kb = kb0 + (i + rot) % kb_n;
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1;
         if (!ptx::mbar_wait(&c.empty[s], ph ^ 1, abort, a.err)) break;
@@ -248,16 +256,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = ptx::idesc_bf16(kTileM, a.E_pad);
       bool ok = true;
-      for (int kb = kb0; kb < kb1; ++kb) {
-        const int s = (kb - kb0) % kStages;
-        const uint32_t ph = ((kb - kb0) / kStages) & 1;
+      for (int i = 0; i < kb_n; ++i) {
+        const int s = i % kStages;
+        const uint32_t ph = (i / kStages) & 1;
         if (!ptx::mbar_wait(&c.full[s], ph, abort, a.err)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint64_t da = ptx::sw128_desc(ptx::smem_u32(a_tiles + s * kABytes));
         const uint64_t db = ptx::sw128_desc(ptx::smem_u32(b_tiles + s * kMaxBBytes));
 #pragma unroll
         for (int k = 0; k < kTileK / 16; ++k)
-          ptx::mma_f16(tmem_base, da + 2 * k, db + 2 * k, idesc, (kb != kb0) || (k != 0));
+          ptx::mma_f16(tmem_base, da + 2 * k, db + 2 * k, idesc, (i != 0) || (k != 0));
         ptx::mma_commit(&c.empty[s]);
       }
       if (ok) ptx::mma_commit(&c.tfull);
