@@ -63,6 +63,26 @@ def test_grouped_ffn_ragged_segments():
     assert_close_layer(y, ref, what="ragged")
 
 
+def test_grouped_ffn_tile_boundaries():
+    """Segments on every side of the GEMM1 tile boundaries: a group's last 1..128
+    rows join the 256-row tile before them (a big tile of 257..384 rows), 129..256
+    rows make a tile of their own; with and without the shared expert."""
+    dev = torch.device("cuda")
+    sizes = [256, 257, 300, 383, 384, 385, 511, 512, 513, 640, 641, 767, 768, 769, 1, 200]
+    R = sum(sizes)
+    for I_shared in (0, 256):
+        lc = wl.TINY.with_(name=f"bounds_s{I_shared}", T=R, E=len(sizes), k=1, H=256, I=256,
+                           I_shared=I_shared)
+        L = Layer(lc, dev)
+        offsets = np.concatenate([[0], np.cumsum(sizes)])
+        rw = np.linspace(0.5, 1.5, R).astype(np.float32)
+        y, s = run_ffn(lc, L, L.x, offsets, rw)
+        ref = om.grouped_ffn(f64(L.x), offsets, L.experts_cpu, rw.astype(np.float64))
+        assert_close_layer(y, ref, what=lc.name)
+        if I_shared:
+            assert_close_layer(s, om.swiglu_ffn(f64(L.x), *L.shared_cpu()), what="shared_out")
+
+
 def test_grouped_ffn_single_expert_is_dense_swiglu():
     """E = 1: one group holding every row; output = the dense SwiGLU FFN."""
     dev = torch.device("cuda")

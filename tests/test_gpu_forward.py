@@ -36,6 +36,8 @@ SMALL = [
     wl.TINY.with_(name="skewish", T=700, E=16, k=3, H=384, I=128, zipf_bias=False),
     wl.TINY.with_(name="one_token_k1", T=1, k=1),
     wl.TINY.with_(name="e40_k5", T=300, E=40, k=5, H=512, I=256, I_shared=128),
+    # about 350 rows per expert: every expert ends in a big tile (256 + tail)
+    wl.DSV3.with_(name="big_tiles", T=700, E=4, k=2, H=512, I=256, I_shared=256),
 ]
 
 
