@@ -221,3 +221,39 @@ def test_nvfp4_quantize_validation(L):
     assert L.moe_quantize_act_nvfp4(16, 4, 100, 1.0, 16, 16, None) == N.MOE_ERR_INVALID_ARG
     assert L.moe_quantize_act_nvfp4(16, 4, 128, 0.0, 16, 16, None) == N.MOE_ERR_INVALID_ARG
     assert L.moe_quantize_act_nvfp4(None, 0, 128, 1.0, None, None, None) == N.MOE_OK
+
+
+def test_nvfp4_step_calls_validate(L):
+    """The NVFP4 step calls: buffer sizes, and host checks before any launch."""
+    c = cfg(wtype="nvfp4", I_shared=256)
+    rows, toks = C.c_int64(0), C.c_int64(0)
+    assert L.moe_nvfp4_rows(C.byref(c), C.byref(rows), C.byref(toks)) == N.MOE_OK
+    assert rows.value == (256 * 2 + 127 * 8 + 127) // 128 * 128 and toks.value == 256
+    b = cfg()
+    assert L.moe_nvfp4_rows(C.byref(b), C.byref(rows), None) == N.MOE_ERR_INVALID_ARG
+    n = C.c_size_t(0)
+    assert L.moe_workspace_size(C.byref(c), N.MOE_OP_PERMUTE, C.byref(n)) == N.MOE_OK
+    ws = 0x100000
+    args = (16, 16, 16, 16, 16, 16, 16, 16, 16, 16, 16, 16, 16)
+    assert L.moe_permute_nvfp4(C.byref(b), 16, *args, ws, 1 << 30, None) == N.MOE_ERR_INVALID_ARG
+    assert b"NVFP4 layers only" in L.moe_last_error_message()
+    assert L.moe_permute_nvfp4(C.byref(c), None, *args, ws, n.value, None) == N.MOE_ERR_INVALID_ARG
+    assert b"weights" in L.moe_last_error_message()
+    assert L.moe_permute_nvfp4(C.byref(c), 16, *args, ws, 64, None) == N.MOE_ERR_WORKSPACE
+    assert L.moe_workspace_size(C.byref(c), N.MOE_OP_GROUPED_FFN, C.byref(n)) == N.MOE_OK
+    fargs = (16, 16, 16, 16, 16, 16, 16, 16, 16)
+    assert L.moe_grouped_ffn_nvfp4(C.byref(b), 16, *fargs, ws, 1 << 30, None) == N.MOE_ERR_INVALID_ARG
+    assert L.moe_grouped_ffn_nvfp4(C.byref(c), None, *fargs, ws, n.value, None) == N.MOE_ERR_INVALID_ARG
+
+
+def test_failure_test_hook_and_noalloc_checks(L):
+    """moe_test_stall_gemm1 rejects a negative count; moe_permute_noalloc validates
+    exactly as moe_permute (E > 256 is unsupported, not an invalid argument)."""
+    assert L.moe_test_stall_gemm1(-1) == N.MOE_ERR_INVALID_ARG
+    assert L.moe_test_stall_gemm1(0) == N.MOE_OK
+    c = cfg(E=300)
+    assert L.moe_permute_noalloc(C.byref(c), 16, None, None, 16, 16, 16, 16, None, None, None,
+                                 None, None) == N.MOE_ERR_UNSUPPORTED
+    c = cfg(wtype="nvfp4", I_shared=256)
+    assert L.moe_permute_noalloc(C.byref(c), 16, None, None, 16, 16, 16, 16, None, None, None,
+                                 None, None) == N.MOE_ERR_UNSUPPORTED
