@@ -699,7 +699,8 @@ moe_status_t moe_stack_create(const moe_config_t* cfg, int32_t num_layers,
                          (fp8 || fp4) ? scales.data() + size_t(l) * 3 * G : nullptr, true,
                          fp4 ? gs.data() + size_t(l) * 3 * G : nullptr,
                          fp4 ? act.data() + size_t(l) * 2 : nullptr));
-    MOE_TRY(encode_2d(&router[l], true, w_router[l], cfg->H, cfg->E, kTileK, E_pad));
+    // boxes of E_pad / 2 router rows (the router kernel loads one or two per stage)
+    MOE_TRY(encode_2d(&router[l], true, w_router[l], cfg->H, cfg->E, kTileK, E_pad / 2));
   }
   // device table: maps [L][3G] | router maps [L] | bias [L] | fp8 scales [L][3G]
   const size_t maps_b = maps.size() * sizeof(CUtensorMap);
@@ -780,7 +781,8 @@ static moe_status_t run_route(const moe_config_t& c, const void* x, const void* 
   CUtensorMap mx, mw;
   MOE_TRY(encode_2d(&mx, true, x, c.H, c.T, kTileK, kTileM));
   if (table) mw = mx;  // unused: the kernel reads the layer's descriptor from the table
-  else MOE_TRY(encode_2d(&mw, true, w_router, c.H, c.E, kTileK, E_pad));
+  // boxes of E_pad / 2 router rows (the router kernel loads one or two per stage)
+  else MOE_TRY(encode_2d(&mw, true, w_router, c.H, c.E, kTileK, E_pad / 2));
   trace_mark(st, MOE_K_ROUTER);
   MOE_CUDA(launch_router(mx, mw, c.T, c.H, c.E, E_pad, c.k, c.score, c.renormalize, c.route_scale,
                          bias, ids, w, logits, err, sm_count(), st, table));

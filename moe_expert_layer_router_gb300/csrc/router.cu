@@ -12,18 +12,19 @@
 // batch spreads its K loop over many SMs instead of running one CTA per 128
 // tokens through all of H.
 //
-//   S = 1: each epilogue thread holds one token's complete logit row.
-//   S > 1: each CTA parks its partial tile in shared memory; after a cluster
-//          barrier CTA c finishes tokens [c 128 / S, (c + 1) 128 / S), S
-//          threads per token, each summing the S partials of E_pad / S
-//          logits over distributed shared memory (in CTA order).  Thread p
-//          of a token owns experts 4 S m + 4 p + {0..3}, so the S threads read
-//          one contiguous 16 S-byte segment of a peer's row per load.
-// A thread scans its logits once, keeping the k largest (strictly greater
-// replaces, so among equal logits the lower expert index stays ahead) and a
-// running softmax normaliser; the S threads of a token then merge their lists
-// and normalisers by shuffles, ordering equal logits by expert index, which
-// selects exactly what one scan of the whole row would.
+// After the K loop the logit tile (S > 1: each CTA's partial) goes from TMEM
+// to shared memory, and after a cluster barrier CTA c finishes tokens
+// [c 128 / S, (c + 1) 128 / S) with Q = 4 S threads per token, 16 warps in
+// all.  Thread p of a token owns experts 4 Q m + 4 p + {0..3} and reads each
+// as the sum of the S partials (distributed shared memory, in CTA order) plus
+// the bias.  The selection takes three passes over a thread's logits: the
+// thread's few largest values give a threshold that the token's k-th largest
+// logit cannot be below; the logits at or above it are marked in a bitmask;
+// only the marked ones are inserted into the thread's top-k list (strictly
+// greater replaces, so among equal logits the lower expert index stays
+// ahead).  The Q lists and softmax normalisers of a token are then merged by
+// shuffles, ordering equal logits by expert index, which selects exactly what
+// one scan of the whole row would.
 #include <math.h>
 
 #include "moe_internal.h"
@@ -33,7 +34,10 @@ namespace moe {
 namespace {
 
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+// warp 0: TMA producer, warp 1: MMA issuer, warps 2..17: TMEM copy-out and
+// the top-k selection
+constexpr int kEpiWarps = 16;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 // Each token tile walks its K slice starting at a tile-dependent k-step (and
 // wraps around), so that the CTAs running at once do not all read the same
 // router-weight k-block (and the same column offset of their token rows) at
@@ -41,15 +45,24 @@ constexpr int kThreads = 192;
 constexpr bool kRotateK = true;
 constexpr int kABytes = kTileM * kTileK * 2;
 constexpr int kMaxBBytes = 256 * kTileK * 2;
+// CTA pairs (one cluster of 2 per 256 tokens, K unsplit): each CTA loads its
+// 128 token rows and half of the router rows per stage, so a stage is at most
+// 32 KB and six fit where a single CTA fits four 48 KB stages.
+constexpr int kPairStages = 6;
+constexpr int kMaxStages = kPairStages;
+template <bool PAIR>
+constexpr int stages_of() { return PAIR ? kPairStages : kStages; }
+template <bool PAIR>
+constexpr int b_slot_bytes() { return PAIR ? kMaxBBytes / 2 : kMaxBBytes; }
 
-struct __align__(8) RouterCtl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+struct __align__(16) RouterCtl {
+  float bias[kMaxExperts];  // first, so that four experts' biases are one 16-byte load
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t tfull;
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  float bias[kMaxExperts];
 };
 
 constexpr size_t kSmemBytes = 1024 + size_t(kStages) * (kABytes + kMaxBBytes) + sizeof(RouterCtl);
@@ -57,6 +70,8 @@ constexpr int kMaxSplit = 8;  // CTAs per cluster (portable cluster size)
 // Partial logit tile of one CTA, [128 tokens][E_pad + 4] fp32, in the stage
 // area once the main loop is over (the +4 skews rows across banks).
 static_assert(kTileM * (256 + 4) * 4 <= kStages * (kABytes + kMaxBBytes), "partial tile fits");
+static_assert(kPairStages * (kABytes + kMaxBBytes / 2) == kStages * (kABytes + kMaxBBytes),
+              "both layouts put the control block at the same offset");
 
 struct RouterArgs {
   int64_t T;
@@ -145,58 +160,79 @@ __device__ __forceinline__ void softmax_add(float& run_max, float& run_sum, floa
   }
 }
 
-// Gate weights of one token from its top-k list and softmax normaliser;
-// writes ids and weights (k entries).
+// Gate weights of one token from its top-k list and softmax normaliser, which
+// the Q threads of the token hold alike (Q a power of two; thread p is lane
+// p of the token's group).  Thread p computes slots j = p, p + Q, ...; every
+// thread then sums all k weights in slot order (the same fp32 sum as one
+// thread would form) and writes its own slots.
 template <int KMAX>
-__device__ __forceinline__ void finish_token(const RouterArgs& a, int64_t t, const float (&tv)[KMAX],
-                                             const int (&ti)[KMAX], float run_max, float run_sum) {
+__device__ __forceinline__ void finish_token(const RouterArgs& a, int64_t t, bool valid, int p,
+                                             int Q, const float (&tv)[KMAX], const int (&ti)[KMAX],
+                                             float run_max, float run_sum) {
   const int k = a.k;
+  const int base = (threadIdx.x & 31) & ~(Q - 1);  // lane of thread 0 of the group
   float w[KMAX];
-  float denom = 0.0f;
   bool bad = false;
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) {
-    if (j < k) {
+    float v = 0.0f;
+    if (j < k && (j & (Q - 1)) == p) {
       bad |= ti[j] < 0;
       if (a.score == 0) {
-        w[j] = a.renormalize ? expf(tv[j] - tv[0]) : expf(tv[j] - run_max) / run_sum;
+        v = a.renormalize ? expf(tv[j] - tv[0]) : expf(tv[j] - run_max) / run_sum;
       } else {
-        w[j] = 1.0f / (1.0f + expf(-tv[j]));
+        v = 1.0f / (1.0f + expf(-tv[j]));
       }
-      denom += w[j];
-    } else {
-      w[j] = 0.0f;
     }
+    w[j] = __shfl_sync(0xffffffffu, v, base + (j & (Q - 1)));
   }
-  if (bad) atomicOr(a.err, kErrNoSelect);
+  float denom = 0.0f;
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j)
+    if (j < k) denom += w[j];
+  if (bad && valid) atomicOr(a.err, kErrNoSelect);
   const float norm = a.renormalize ? a.route_scale / denom : a.route_scale;
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) {
-    if (j < k) {
+    if (valid && j < k && (j & (Q - 1)) == p) {
       a.topk_ids[t * k + j] = ti[j];
       a.topk_w[t * k + j] = w[j] * norm;
     }
   }
 }
 
-template <int KMAX>
+// PAIR: the cluster is a CTA pair that owns 256 tokens (CTA r: rows 128 r ..
+// 128 r + 127) over all of H; one thread of the even CTA issues M = 256 pair
+// MMAs whose B (the E_pad router rows) is split between the two CTAs, and each
+// CTA's TMEM receives its own 128 x E_pad logit tile.  Otherwise the cluster
+// is the K split of one 128-token tile.
+template <int KMAX, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     router_kernel(const __grid_constant__ CUtensorMap map_x,
                   const __grid_constant__ CUtensorMap map_w, const RouterArgs a) {
+  constexpr int kSt = stages_of<PAIR>();
+  constexpr int kBSlot = b_slot_bytes<PAIR>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int b_bytes = a.E_pad * kTileK * 2;
+  // router rows per TMA box: E_pad / 2 (a pair CTA loads one box, a single CTA two)
+  const int b_half_rows = a.E_pad / 2;
+  const int b_bytes = (PAIR ? 1 : 2) * b_half_rows * kTileK * 2;  // this CTA's B per stage
   const int stage_bytes = kABytes + b_bytes;
   uint8_t* a_tiles = smem;
-  uint8_t* b_tiles = smem + kStages * kABytes;
-  RouterCtl& c = *reinterpret_cast<RouterCtl*>(smem + kStages * (kABytes + kMaxBBytes));
+  uint8_t* b_tiles = smem + kSt * kABytes;
+  RouterCtl& c = *reinterpret_cast<RouterCtl*>(smem + kSt * (kABytes + kBSlot));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int S = static_cast<int>(ptx::cluster_nctarank());   // K split of this token tile
   const uint32_t crank = ptx::cluster_ctarank();
-  const int64_t m0 = int64_t(blockIdx.x / S) * kTileM;
+  const bool leader = crank == 0;
+  // K split of this token tile, and this CTA's slice index in it
+  const int S = PAIR ? 1 : static_cast<int>(ptx::cluster_nctarank());
+  const int kr = PAIR ? 0 : static_cast<int>(crank);
+  const int tile = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x) / S;
+  const int64_t m0 = PAIR ? int64_t(tile) * (2 * kTileM) + int64_t(crank) * kTileM
+                          : int64_t(tile) * kTileM;
   // this call's router matrix and bias (a layer stack indexes its tables)
   const float* bias = a.bias;
   const void* map_w_ptr = &map_w;
@@ -206,9 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bias = a.table.bias_table[l];
   }
 
-  for (int i = threadIdx.x; i < a.E; i += kThreads) c.bias[i] = bias ? bias[i] : 0.0f;
+  for (int i = threadIdx.x; i < a.E_pad; i += kThreads) c.bias[i] = bias && i < a.E ? bias[i] : 0.0f;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSt; ++s) {
       ptx::mbar_init(&c.full[s], 1);
       ptx::mbar_init(&c.empty[s], 1);
     }
@@ -218,51 +254,90 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(&c.tmem_base, a.tmem_cols);
-    ptx::tmem_relinquish();
+    if (PAIR) {
+      ptx::tmem_alloc_pair(&c.tmem_base, a.tmem_cols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(&c.tmem_base, a.tmem_cols);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if (PAIR) ptx::cluster_sync();  // both CTAs' barriers exist before either signals them
   ptx::tc_fence_after();
   const uint32_t tmem_base = c.tmem_base;
   volatile int* abort = &c.abort;
   // the softmax normaliser over all E is needed only for unrenormalised softmax
   const bool need_norm = a.score == 0 && !a.renormalize;
   const int kb_all = a.H / kTileK;
-  const int kb0 = static_cast<int>(crank) * kb_all / S;  // this CTA's K slice (S <= kb_all)
-  const int kb1 = (static_cast<int>(crank) + 1) * kb_all / S;
+  const int kb0 = kr * kb_all / S;  // this CTA's K slice (S <= kb_all)
+  const int kb1 = (kr + 1) * kb_all / S;
   const int kb_n = kb1 - kb0;
-  const int rot = kRotateK ? static_cast<int>((blockIdx.x / S) % static_cast<unsigned>(kb_n)) : 0;
+  const int rot = kRotateK ? tile % kb_n : 0;  // the same in both CTAs of a pair
 
   if (warp == 0) {
     if (lane == 0) {
+      // PAIR: both CTAs' copies of a stage complete on the even CTA's barrier
+      const uint32_t full0 = ptx::mapa(ptx::smem_u32(&c.full[0]), 0);
       uint32_t it = 0;
       for (int i = 0; i < kb_n; ++i, ++it) {
         const int kb = kb0 + (i + rot) % kb_n;
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
+        const int s = it % kSt;
+        const uint32_t ph = (it / kSt) & 1;
         if (!ptx::mbar_wait(&c.empty[s], ph ^ 1, abort, a.err)) break;
-        ptx::mbar_arrive_expect_tx(&c.full[s], stage_bytes);
-        ptx::tma_load_2d(a_tiles + s * kABytes, &map_x, &c.full[s], kb * kTileK, int32_t(m0));
-        ptx::tma_load_2d(b_tiles + s * kMaxBBytes, map_w_ptr, &c.full[s], kb * kTileK, 0);
+        if (PAIR) {
+          const uint32_t fb = full0 + s * 8;
+          if (leader) ptx::mbar_arrive_expect_tx(&c.full[s], 2 * stage_bytes);
+          ptx::tma_load_2d_pair(a_tiles + s * kABytes, &map_x, fb, kb * kTileK, int32_t(m0));
+          ptx::tma_load_2d_pair(b_tiles + s * kBSlot, map_w_ptr, fb, kb * kTileK,
+                                int32_t(crank) * b_half_rows);
+        } else {
+          ptx::mbar_arrive_expect_tx(&c.full[s], stage_bytes);
+          ptx::tma_load_2d(a_tiles + s * kABytes, &map_x, &c.full[s], kb * kTileK, int32_t(m0));
+          ptx::tma_load_2d(b_tiles + s * kBSlot, map_w_ptr, &c.full[s], kb * kTileK, 0);
+          ptx::tma_load_2d(b_tiles + s * kBSlot + b_half_rows * kTileK * 2, map_w_ptr,
+                           &c.full[s], kb * kTileK, b_half_rows);
+        }
       }
-      if (*abort) {
-        const uint32_t first = it > kStages ? it - kStages : 0;
+      // no copy may be in flight at exit (PAIR: the even CTA's barriers see
+      // both CTAs' copies; the odd CTA waits at the final cluster barrier)
+      if (*abort && (!PAIR || leader)) {
+        const uint32_t first = it > kSt ? it - kSt : 0;
         for (uint32_t j = first; j < it; ++j)
-          drain_wait(&c.full[j % kStages], (j / kStages) & 1, a.err);
+          drain_wait(&c.full[j % kSt], (j / kSt) & 1, a.err);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = ptx::idesc_bf16(kTileM, a.E_pad);
+    if (PAIR && lane == 0 && leader) {
+      const uint32_t idesc = ptx::idesc_bf16(2 * kTileM, a.E_pad);
       bool ok = true;
       for (int i = 0; i < kb_n; ++i) {
-        const int s = i % kStages;
-        const uint32_t ph = (i / kStages) & 1;
+        const int s = i % kSt;
+        const uint32_t ph = (i / kSt) & 1;
         if (!ptx::mbar_wait(&c.full[s], ph, abort, a.err)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint64_t da = ptx::sw128_desc(ptx::smem_u32(a_tiles + s * kABytes));
-        const uint64_t db = ptx::sw128_desc(ptx::smem_u32(b_tiles + s * kMaxBBytes));
+        const uint64_t db = ptx::sw128_desc(ptx::smem_u32(b_tiles + s * kBSlot));
+#pragma unroll
+        for (int k = 0; k < kTileK / 16; ++k)
+          ptx::mma_f16_pair(tmem_base, da + 2 * k, db + 2 * k, idesc, (i != 0) || (k != 0));
+        ptx::mma_commit_pair_mc(&c.empty[s], 0x3);
+      }
+      if (ok) ptx::mma_commit_pair_mc(&c.tfull, 0x3);
+      // every pair MMA issued by this thread has finished once `drain` flips
+      ptx::mma_commit_pair_mc(&c.drain, 0x1);
+      drain_wait(&c.drain, 0, a.err);
+    } else if (!PAIR && lane == 0) {
+      const uint32_t idesc = ptx::idesc_bf16(kTileM, a.E_pad);
+      bool ok = true;
+      for (int i = 0; i < kb_n; ++i) {
+        const int s = i % kSt;
+        const uint32_t ph = (i / kSt) & 1;
+        if (!ptx::mbar_wait(&c.full[s], ph, abort, a.err)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint64_t da = ptx::sw128_desc(ptx::smem_u32(a_tiles + s * kABytes));
+        const uint64_t db = ptx::sw128_desc(ptx::smem_u32(b_tiles + s * kBSlot));
 #pragma unroll
         for (int k = 0; k < kTileK / 16; ++k)
           ptx::mma_f16(tmem_base, da + 2 * k, db + 2 * k, idesc, (i != 0) || (k != 0));
@@ -272,17 +347,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mma_commit(&c.drain);
       drain_wait(&c.drain, 0, a.err);
     }
-  } else if (S > 1) {
-    // partial tile -> this CTA's shared memory, row = token
+  } else {
+    // Logit tile -> this CTA's shared memory, row = token (S > 1: the partial
+    // over this CTA's K slice).  Warp w may read TMEM lane quarter w % 4; the
+    // kEpiWarps / 4 warps of a quarter take every (kEpiWarps / 4)-th 32-column
+    // chunk.
     const int q = warp & 3;
     const int r = q * 32 + lane;
-    const int stride = a.E_pad + 4;
-    float* part = reinterpret_cast<float*>(smem) + r * stride;
+    float* part = reinterpret_cast<float*>(smem) + r * (a.E_pad + 4);
     if (ptx::mbar_wait(&c.tfull, 0, abort, a.err)) {
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
-      for (int c0 = 0; c0 < a.E_pad; c0 += 32) {
+      for (int c0 = 32 * ((warp - 2) >> 2); c0 < a.E_pad; c0 += 32 * (kEpiWarps / 4)) {
         uint32_t v[32];
         ptx::tmem_ld32(taddr + c0, v);
         ptx::tmem_ld_wait();
@@ -296,154 +373,164 @@ __global__ void __launch_bounds__(kThreads, 1)
                             __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
       }
     }
-  } else {
-    const int q = warp & 3;
-    const int r = q * 32 + lane;
-    const int64_t t = m0 + r;
-    const bool valid = t < a.T;
-    if (ptx::mbar_wait(&c.tfull, 0, abort, a.err)) {
-      ptx::tc_fence_after();
-      float tv[KMAX];
-      int ti[KMAX];
-#pragma unroll
-      for (int i = 0; i < KMAX; ++i) {
-        tv[i] = -INFINITY;
-        ti[i] = -1;
-      }
-      float run_max = -INFINITY, run_sum = 0.0f;  // softmax over all E (online)
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-      float* lrow = (valid && a.logits_out) ? a.logits_out + t * a.E : nullptr;
-#pragma unroll 1
-      for (int c0 = 0; c0 < a.E_pad; c0 += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld32(taddr + c0, v);
-        ptx::tmem_ld_wait();
-        float lv[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int e = c0 + j;
-          lv[j] = e < a.E ? __uint_as_float(v[j]) + c.bias[e] : -INFINITY;
-        }
-        if (lrow) {
-          if (c0 + 32 <= a.E) {
-            float4* d = reinterpret_cast<float4*>(lrow + c0);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              d[j] = make_float4(lv[4 * j], lv[4 * j + 1], lv[4 * j + 2], lv[4 * j + 3]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (c0 + j < a.E) lrow[c0 + j] = lv[j];
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (c0 + j < a.E) {
-            topk_insert<KMAX>(tv, ti, lv[j], c0 + j);
-            if (need_norm) softmax_add(run_max, run_sum, lv[j]);
-          }
-        }
-      }
-      if (valid) finish_token<KMAX>(a, t, tv, ti, run_max, run_sum);
-    }
   }
 
-  if (S > 1) {
-    ptx::cluster_sync();  // every CTA's partial tile is in its shared memory
-    if (warp >= 2) {
-      // tokens [crank 128 / S, +128 / S) of the tile, S threads per token
-      const int et = threadIdx.x - 64;
-      const int p = et % S;
-      const int tl = static_cast<int>(crank) * (kTileM / S) + et / S;
-      const int64_t t = m0 + tl;
-      const bool valid = t < a.T;
-      const int nchunk = a.E_pad / (4 * S);  // E_pad is a multiple of 4 S
-      const uint32_t src = ptx::smem_u32(reinterpret_cast<float*>(smem) + tl * (a.E_pad + 4) + 4 * p);
-      uint32_t peer[kMaxSplit];
+  ptx::cluster_sync();  // every CTA's logit tile is in its shared memory
+  if (warp >= 2) {
+    // CTA c finishes tokens [c 128 / S, (c + 1) 128 / S) with Q = 4 S adjacent
+    // threads per token (Q <= 32 divides the warp).  Thread p of a token owns
+    // experts 4 Q m + 4 p + {0..3}, m = 0..nchunk-1 (at most 64 of them), and
+    // reads each as the sum of the S partial tiles in CTA order plus the bias.
+    const int Q = 4 * S;
+    const int et = threadIdx.x - 64;
+    const int p = et & (Q - 1);
+    const int tl = kr * (kTileM / S) + et / Q;
+    const int64_t t = m0 + tl;
+    const bool valid = t < a.T;
+    const int nchunk = (a.E_pad + 4 * Q - 1) / (4 * Q);
+    const int row = tl * (a.E_pad + 4) + 4 * p;  // float index of this thread's first expert
+    float* own = reinterpret_cast<float*>(smem) + row;
+    uint32_t peer[kMaxSplit];
 #pragma unroll
-      for (int j = 0; j < kMaxSplit; ++j) peer[j] = j < S ? ptx::mapa(src, j) : 0u;
-      float tv[KMAX];
-      int ti[KMAX];
+    for (int j = 0; j < kMaxSplit; ++j)
+      peer[j] = j < S ? ptx::mapa(ptx::smem_u32(own), j) : 0u;
+    // Logits of experts 4 Q m + 4 p + {0..3}: the S partials summed in CTA
+    // order (this CTA's own from local shared memory), plus the bias.  Pass 1
+    // stores them over this CTA's own partial of those experts, which no other
+    // CTA reads (CTA j reads only the rows of the tokens it finishes).
+    auto logits4 = [&](int m, float (&v)[4]) {
+      float4 acc = *reinterpret_cast<const float4*>(own + 4 * Q * m);
+      if (S > 1) {
+        acc = kr == 0 ? acc : ptx::ld_cluster_f32x4(peer[0] + 16u * Q * m);
 #pragma unroll
-      for (int i = 0; i < KMAX; ++i) {
-        tv[i] = -INFINITY;
-        ti[i] = -1;
-      }
-      float run_max = -INFINITY, run_sum = 0.0f;
-      float* lrow = (valid && a.logits_out) ? a.logits_out + t * a.E : nullptr;
-      // the S partials of four logits per chunk; chunk m + 1 is loaded before
-      // chunk m is scanned, so the remote-load latency overlaps the scan
-      float4 nxt[kMaxSplit];
-#pragma unroll
-      for (int j = 0; j < kMaxSplit; ++j)
-        nxt[j] = j < S ? ptx::ld_cluster_f32x4(peer[j]) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll 1
-      for (int m = 0; m < nchunk; ++m) {
-        float4 pv[kMaxSplit];
-#pragma unroll
-        for (int j = 0; j < kMaxSplit; ++j) pv[j] = nxt[j];
-        if (m + 1 < nchunk) {
-          const uint32_t off = 16u * S * (m + 1);
-#pragma unroll
-          for (int j = 0; j < kMaxSplit; ++j)
-            if (j < S) nxt[j] = ptx::ld_cluster_f32x4(peer[j] + off);
-        }
-        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-        for (int j = 0; j < kMaxSplit; ++j)
+        for (int j = 1; j < kMaxSplit; ++j)
           if (j < S) {
-            v[0] += pv[j].x;
-            v[1] += pv[j].y;
-            v[2] += pv[j].z;
-            v[3] += pv[j].w;
+            const float4 pv = j == kr ? *reinterpret_cast<const float4*>(own + 4 * Q * m)
+                                      : ptx::ld_cluster_f32x4(peer[j] + 16u * Q * m);
+            acc.x += pv.x;
+            acc.y += pv.y;
+            acc.z += pv.z;
+            acc.w += pv.w;
           }
+      }
+      const float4 b = *reinterpret_cast<const float4*>(&c.bias[4 * Q * m + 4 * p]);
+      v[0] = acc.x + b.x;
+      v[1] = acc.y + b.y;
+      v[2] = acc.z + b.z;
+      v[3] = acc.w + b.w;
+    };
+
+    // Pass 1: logits out, the softmax normaliser, and this thread's kTop
+    // largest logits.  With m = ceil(k / Q) <= kTop, the Q threads' m-th
+    // largest values are Q m >= k logits of the token, so their minimum theta
+    // is at most the token's k-th largest logit: every selected expert has a
+    // logit >= theta.
+    constexpr int kTop = (KMAX + 3) / 4;
+    float top[kTop];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const int e = 4 * S * m + 4 * p + h;  // increasing in (m, h)
-          if (e < a.E) {
-            const float lv = v[h] + c.bias[e];
-            if (lrow) lrow[e] = lv;
-            topk_insert<KMAX>(tv, ti, lv, e);
-            if (need_norm) softmax_add(run_max, run_sum, lv);
+    for (int i = 0; i < kTop; ++i) top[i] = -INFINITY;
+    float run_max = -INFINITY, run_sum = 0.0f;  // softmax over all E (online)
+    float* lrow = (valid && a.logits_out) ? a.logits_out + t * a.E : nullptr;
+    // chunks of this thread that hold at least one expert < E
+    const int n_m = a.E > 4 * p ? min(nchunk, (a.E - 4 * p + 4 * Q - 1) / (4 * Q)) : 0;
+#pragma unroll 2
+    for (int m = 0; m < n_m; ++m) {
+      const int e0 = 4 * Q * m + 4 * p;
+      float v[4];
+      logits4(m, v);
+      *reinterpret_cast<float4*>(own + 4 * Q * m) = make_float4(v[0], v[1], v[2], v[3]);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        if (e0 + h < a.E) {
+          if (lrow) lrow[e0 + h] = v[h];
+          float x = v[h];
+#pragma unroll
+          for (int i = 0; i < kTop; ++i) {
+            const float hi = fmaxf(top[i], x);
+            x = fminf(top[i], x);
+            top[i] = hi;
           }
+          if (need_norm) softmax_add(run_max, run_sum, v[h]);
         }
       }
-      // merge the S lists of the token (adjacent lanes)
-#pragma unroll
-      for (int d = 1; d < kMaxSplit; d <<= 1) {
-        if (d < S) {
-          float ov[KMAX];
-          int oi[KMAX];
-#pragma unroll
-          for (int i = 0; i < KMAX; ++i) {
-            ov[i] = __shfl_xor_sync(0xffffffffu, tv[i], d);
-            oi[i] = __shfl_xor_sync(0xffffffffu, ti[i], d);
-          }
-          topk_merge<KMAX>(tv, ti, ov, oi);
-          const float om = __shfl_xor_sync(0xffffffffu, run_max, d);
-          const float os = __shfl_xor_sync(0xffffffffu, run_sum, d);
-          if (om > run_max) {
-            run_sum = run_sum * expf(run_max - om) + os;
-            run_max = om;
-          } else if (om != -INFINITY) {
-            run_sum += os * expf(om - run_max);
-          }
-        }
-      }
-      if (valid && p == 0) finish_token<KMAX>(a, t, tv, ti, run_max, run_sum);
     }
-    ptx::cluster_sync();  // no CTA leaves while a peer still reads its partial tile
+    const int mth = ((a.k + Q - 1) / Q < kTop ? (a.k + Q - 1) / Q : kTop) - 1;
+    float theta = top[0];
+#pragma unroll
+    for (int i = 1; i < kTop; ++i)
+      if (i == mth) theta = top[i];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1)
+      if (d < Q) theta = fminf(theta, __shfl_xor_sync(0xffffffffu, theta, d));
+
+    // Pass 2: the candidates (logit >= theta) as a bitmask of positions 4 m + h.
+    uint64_t cand = 0;
+#pragma unroll 4
+    for (int m = 0; m < n_m; ++m) {
+      const int e0 = 4 * Q * m + 4 * p;
+      const float4 v = *reinterpret_cast<const float4*>(own + 4 * Q * m);
+      const float vh[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h)
+        if (e0 + h < a.E && vh[h] >= theta) cand |= 1ull << (4 * m + h);
+    }
+
+    // Pass 3: the candidates in increasing expert order into the top-k list
+    // (strictly greater replaces, so the lower index stays ahead among equal
+    // logits).  The warp iterates as long as any lane has a candidate left.
+    float tv[KMAX];
+    int ti[KMAX];
+#pragma unroll
+    for (int i = 0; i < KMAX; ++i) {
+      tv[i] = -INFINITY;
+      ti[i] = -1;
+    }
+    while (__any_sync(0xffffffffu, cand != 0)) {
+      if (cand != 0) {
+        const int i = __ffsll(static_cast<long long>(cand)) - 1;
+        cand &= cand - 1;
+        const int m = i >> 2, h = i & 3;
+        topk_insert<KMAX>(tv, ti, own[4 * Q * m + h], 4 * Q * m + 4 * p + h);
+      }
+    }
+
+    // merge the Q lists of the token (adjacent lanes)
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      if (d < Q) {
+        float ov[KMAX];
+        int oi[KMAX];
+#pragma unroll
+        for (int i = 0; i < KMAX; ++i) {
+          ov[i] = __shfl_xor_sync(0xffffffffu, tv[i], d);
+          oi[i] = __shfl_xor_sync(0xffffffffu, ti[i], d);
+        }
+        topk_merge<KMAX>(tv, ti, ov, oi);
+        const float om = __shfl_xor_sync(0xffffffffu, run_max, d);
+        const float os = __shfl_xor_sync(0xffffffffu, run_sum, d);
+        if (om > run_max) {
+          run_sum = run_sum * expf(run_max - om) + os;
+          run_max = om;
+        } else if (om != -INFINITY) {
+          run_sum += os * expf(om - run_max);
+        }
+      }
+    }
+    finish_token<KMAX>(a, t, valid, p, Q, tv, ti, run_max, run_sum);
   }
+  ptx::cluster_sync();  // no CTA leaves while a peer still reads its logit tile
 
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, a.tmem_cols);
+    if (PAIR)
+      ptx::tmem_dealloc_pair(tmem_base, a.tmem_cols);
+    else
+      ptx::tmem_dealloc(tmem_base, a.tmem_cols);
   }
 }
 
-template <int KMAX>
 cudaLaunchConfig_t cluster_config(int grid, int split, cudaStream_t stream,
                                   cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
@@ -468,9 +555,11 @@ int max_split() {
   int split = kMaxSplit;
   for (; split > 1; split >>= 1) {
     cudaLaunchAttribute attr;
-    cudaLaunchConfig_t cfg = cluster_config<KMAX>(split, split, nullptr, &attr);
+    cudaLaunchConfig_t cfg = cluster_config(split, split, nullptr, &attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, router_kernel<KMAX>, &cfg) == cudaSuccess && n > 0) break;
+    if (cudaOccupancyMaxActiveClusters(&n, router_kernel<KMAX, false>, &cfg) == cudaSuccess &&
+        n > 0)
+      break;
     cudaGetLastError();
   }
   cached = split;
@@ -480,8 +569,13 @@ int max_split() {
 template <int KMAX>
 cudaError_t launch_k(const CUtensorMap& mx, const CUtensorMap& mw, const RouterArgs& a, int tiles,
                      int sm_count, cudaStream_t stream) {
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(router_kernel<KMAX>),
+  // both kernels may use the full shared memory (the cluster occupancy query
+  // below depends on it)
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(router_kernel<KMAX, false>),
                                    static_cast<int>(kSmemBytes));
+  if (e == cudaSuccess)
+    e = ensure_smem_attr(reinterpret_cast<const void*>(router_kernel<KMAX, true>),
+                         static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   // split K while the grid still fits the GPU, every CTA keeps a K step and
   // E_pad divides into 16-byte chunks per finishing thread
@@ -491,9 +585,17 @@ cudaError_t launch_k(const CUtensorMap& mx, const CUtensorMap& mw, const RouterA
   while (split < cap && tiles * split * 2 <= sm_count && split * 2 <= kb_all &&
          a.E_pad % (8 * split) == 0)
     split *= 2;
+  // unsplit tiles: CTA pairs over 256 tokens each (router-row halves of a
+  // multiple of 16 rows)
+  const bool pair = split == 1 && tiles > 1 && a.E_pad % 32 == 0;
   cudaLaunchAttribute attr;
-  cudaLaunchConfig_t cfg = cluster_config<KMAX>(tiles * split, split, stream, &attr);
-  e = cudaLaunchKernelEx(&cfg, router_kernel<KMAX>, mx, mw, a);
+  if (pair) {
+    cudaLaunchConfig_t cfg = cluster_config(2 * ((tiles + 1) / 2), 2, stream, &attr);
+    e = cudaLaunchKernelEx(&cfg, router_kernel<KMAX, true>, mx, mw, a);
+  } else {
+    cudaLaunchConfig_t cfg = cluster_config(tiles * split, split, stream, &attr);
+    e = cudaLaunchKernelEx(&cfg, router_kernel<KMAX, false>, mx, mw, a);
+  }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -87,6 +87,40 @@ def test_route_bias_decides_ties():
     np.testing.assert_allclose(w.cpu().numpy(), (e / e.sum())[None, :].repeat(64, 0), rtol=1e-6)
 
 
+# T = 64, 2000, 5000, 10000 give K splits S = 8, 4, 2, 1 on a 152-SM GPU, so the
+# selection runs with Q = 4 S = 32, 16, 8, 4 finishing threads per token.
+@pytest.mark.parametrize("T", [64, 2000, 5000, 10000])
+@pytest.mark.parametrize("pattern", ["one_owner", "tied_boundary"])
+def test_route_exact_logits_selection(T, pattern):
+    """Logits set exactly (x[:, 0] = 1, router column 0 = the logit, every other
+    router column 0), so the selection has one right answer, taken from the
+    oracle's stable top-k.  one_owner: the k best are experts 0..k-1, which the
+    same finishing thread owns; tied_boundary: six experts share the k-th largest
+    value, and the lowest-indexed of them must be taken."""
+    dev = torch.device("cuda")
+    E, k, H = 64, 4, 256
+    lc = wl.TINY.with_(T=T, E=E, k=k, H=H, score="softmax", renormalize=True, I_shared=0)
+    cfg = m.config_from(lc)
+    x = wl.gen_x(lc, dev)
+    x[:, 0] = 1.0
+    # distinct values in [-4, 0) on a 1/16 grid: exact in bf16 and in fp32 sums
+    v = np.random.default_rng(5).permutation(np.arange(E)) / 16.0 - 4.0
+    if pattern == "one_owner":
+        v[:k] = 4.0 + np.arange(k)[::-1]
+    else:
+        v[[50, 20, 7]] = [3.0, 2.5, 2.25]
+        v[[5, 9, 17, 33, 40, 63]] = 2.0
+    wr = torch.zeros(E, H, dtype=torch.bfloat16, device=dev)
+    wr[:, 0] = torch.tensor(v, dtype=torch.bfloat16, device=dev)
+    ids, w, lg = m.moe_route(cfg, x, wr, return_logits=True)
+    exact = np.broadcast_to(v, (T, E))
+    np.testing.assert_array_equal(lg.cpu().numpy().astype(np.float64), exact)
+    ref = om.select_topk(exact, k)
+    np.testing.assert_array_equal(ids.cpu().numpy(), ref)
+    if pattern == "tied_boundary":
+        assert (ref[:, 3] == 5).all()
+
+
 def test_route_full_size_dsv3():
     """Full DeepSeek-V3 router shape (T=16384, H=7168, E=256, k=8)."""
     dev = torch.device("cuda")
