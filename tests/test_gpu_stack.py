@@ -62,6 +62,9 @@ SHAPES = [
     wl.TINY.with_(name="tiny_shared_sigmoid", T=200, I_shared=256, score="sigmoid",
                   route_scale=2.5),
     wl.DSV3.with_(name="dsv3_shape_T64", T=64, E=32, k=4, I=256, I_shared=256),
+    # 79 token tiles: the router runs on CTA pairs (K unsplit) with the stack's table
+    wl.TINY.with_(name="pair_router_T10000", T=10000, H=256, E=32, k=4, I=128, I_shared=128,
+                  score="sigmoid", route_scale=2.5),
 ]
 
 
