@@ -662,13 +662,22 @@ def run_reference(args, lc, rank, world, dev):
     class HostLayer:  # inputs only; the oracle needs no descriptor table
         pass
 
+    class Experts:  # an expert's matrices are generated the first time a sample needs them
+        def __init__(self):
+            self.cache = {}
+
+        def __getitem__(self, e):
+            if e not in self.cache:
+                self.cache[e] = tuple(wl.gen_expert(lc, e, w, layer_dev)
+                                      for w in ("gate", "up", "down"))
+            return self.cache[e]
+
     L = HostLayer()
     L.x = wl.gen_x(lc, layer_dev)
     L.wr = wl.gen_router(lc, layer_dev)
     b = wl.gen_bias(lc)
     L.bias = b.to(layer_dev) if b is not None else None
-    L.W = [tuple(wl.gen_expert(lc, e, w, layer_dev) for w in ("gate", "up", "down"))
-           for e in range(lc.E)]
+    L.W = Experts()
     L.S = (tuple(wl.gen_shared(lc, w, layer_dev) for w in ("gate", "up", "down"))
            if lc.I_shared else None)
     g = np.random.default_rng(2)
