@@ -466,9 +466,12 @@ MOE_API moe_status_t moe_test_stall_gemm1(int32_t count);
  * records one of the caller's CUDA events on its stream before each kernel it
  * launches (kernel_ids[i] = the moe_kernel_t that follows events[i]) and one
  * after the last (kernel_ids[i] = -1), so consecutive events bracket each
- * kernel.  Recording stops silently when `capacity` is reached; `count` is
- * advanced by the library.  The events must be created by the caller
- * (cudaEventCreate) on the current device.  NULL clears the trace. */
+ * kernel.  A nonzero kernel_mask restricts the events to the kernels whose bit
+ * (1 << moe_kernel_t) is set and drops the trailing one; e.g. the GEMM1 and
+ * GEMM2 bits bracket GEMM1 alone.  Recording stops silently when `capacity`
+ * is reached; `count` is advanced by the library.  The events must be created
+ * by the caller (cudaEventCreate) on the current device.  NULL clears the
+ * trace. */
 typedef enum moe_kernel {
   MOE_K_ROUTER = 0,
   MOE_K_HIST = 1,
@@ -483,10 +486,11 @@ typedef enum moe_kernel {
 } moe_kernel_t;
 
 typedef struct moe_trace {
-  void** events;       /* cudaEvent_t[capacity] */
-  int32_t* kernel_ids; /* int32[capacity], written by the library */
+  void** events;        /* cudaEvent_t[capacity] */
+  int32_t* kernel_ids;  /* int32[capacity], written by the library */
   int32_t capacity;
   int32_t count;
+  uint32_t kernel_mask; /* 0: every kernel; else only the kernels whose bit is set */
 } moe_trace_t;
 
 MOE_API moe_status_t moe_set_trace(moe_trace_t* trace);

@@ -43,7 +43,7 @@ class MoeWeightList(C.Structure):
 
 class MoeTrace(C.Structure):
     _fields_ = [("events", C.POINTER(C.c_void_p)), ("kernel_ids", C.POINTER(C.c_int32)),
-                ("capacity", C.c_int32), ("count", C.c_int32)]
+                ("capacity", C.c_int32), ("count", C.c_int32), ("kernel_mask", C.c_uint32)]
 
 
 KERNEL_NAMES = ["router", "hist", "scan", "scatter", "plan", "gemm1_gate_up_swiglu",

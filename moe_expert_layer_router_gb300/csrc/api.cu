@@ -110,6 +110,7 @@ static thread_local moe_trace_t* g_trace = nullptr;
 void trace_mark(cudaStream_t stream, int id) {
   moe_trace_t* t = g_trace;
   if (!t || t->count >= t->capacity) return;
+  if (t->kernel_mask != 0u && (id < 0 || ((t->kernel_mask >> id) & 1u) == 0u)) return;
   if (cudaEventRecord(static_cast<cudaEvent_t>(t->events[t->count]), stream) != cudaSuccess) return;
   t->kernel_ids[t->count] = id;
   t->count += 1;

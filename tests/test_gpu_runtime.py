@@ -102,3 +102,42 @@ def test_a_wait_that_runs_out_is_reported_and_the_next_call_recovers():
     ref_out = with_flips(r, ref["out"], lambda t, i, w_: om.moe_tokens(
         f64(L.x)[t], i, w_, L.experts_cpu, L.shared_cpu()))
     assert_close_layer(out, ref_out, what="after the stalled call")
+
+
+def _trace(n, mask):
+    from moe_expert_layer_router_gb300 import _native as N
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in evs:
+        e.record()
+    torch.cuda.synchronize()
+    arr = (N.C.c_void_p * n)(*[e.cuda_event for e in evs])
+    kid = (N.C.c_int32 * n)()
+    t = N.MoeTrace(N.C.cast(arr, N.C.POINTER(N.C.c_void_p)),
+                   N.C.cast(kid, N.C.POINTER(N.C.c_int32)), n, 0, mask)
+    return t, kid, evs
+
+
+def test_trace_marks_every_kernel_or_the_masked_ones():
+    """The trace hook: without a mask an event before each of the layer's 8
+    kernels and one after the last; with the GEMM1 and GEMM2 bits, exactly the
+    two events that bracket GEMM1, and the output is unchanged."""
+    from moe_expert_layer_router_gb300 import _native as N
+    dev = torch.device("cuda")
+    L = Layer(LC, dev)
+    cfg = m.config_from(LC)
+    W = weights_of(L, cfg)
+    ws = m.Workspace(cfg, "forward")
+    ref = m.moe_forward(cfg, W, L.x, L.wr, L.bias, ws=ws)
+    torch.cuda.synchronize()
+    g1, g2 = N.KERNEL_NAMES.index("gemm1_gate_up_swiglu"), N.KERNEL_NAMES.index("gemm2_down")
+    for mask, want in ((0, [0, 1, 2, 3, 4, g1, g2, 7, -1]), ((1 << g1) | (1 << g2), [g1, g2])):
+        t, kid, evs = _trace(16, mask)
+        N.check(N.lib().moe_set_trace(N.C.byref(t)), "moe_set_trace")
+        try:
+            out = m.moe_forward(cfg, W, L.x, L.wr, L.bias, ws=ws)
+        finally:
+            N.lib().moe_set_trace(None)
+        torch.cuda.synchronize()
+        assert [kid[i] for i in range(t.count)] == want
+        assert torch.equal(out, ref)
+        assert evs[0].elapsed_time(evs[1]) >= 0.0
