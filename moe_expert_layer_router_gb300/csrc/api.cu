@@ -214,6 +214,7 @@ static size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
 
 struct Layout {
   size_t blk_counts = 0, blk_base = 0;        // permute
+  size_t amap = 0;                            // bf16 grouped ffn: cut A tensor maps
   size_t sched1 = 0, sched2 = 0, h = 0, hs = 0;  // grouped ffn
   size_t h_sc = 0, hs_sc = 0;                 // fp8: scales of h and of the shared h
   size_t ids = 0, w = 0, counts = 0, offsets = 0, perm_token = 0, inv_row = 0, row_weight = 0,
@@ -294,6 +295,7 @@ static Layout layout(const moe_config_t& c, int op) {
     L.sched2 = take(size_t(sched_ints(G)) * 4);
     L.h = take(size_t(R) * c.I * esz);
     L.hs = take(size_t(T) * c.I_shared * esz);
+    if (!fp8) L.amap = take(size_t(2) * c.E * 128);
     if (fp8) {
       L.h_sc = take(size_t(R) * (c.I / 128) * 4);
       L.hs_sc = take(size_t(T) * (c.I_shared / 128) * 4);
@@ -827,15 +829,21 @@ static moe_status_t run_ffn(const moe_config_t& c, const WeightView& W, const La
   __nv_bfloat16* hs = at<__nv_bfloat16*>(ws, L.hs);
   const int n1r = c.I / kGemm1TileN, n1s = c.I_shared / kGemm1TileN;
   const int n2 = (c.H + kGemm2TileN - 1) / kGemm2TileN;
-  trace_mark(st, MOE_K_PLAN);
-  MOE_CUDA(launch_plan(offsets, c.E, shared ? 1 : 0, c.T, n1r, n1s, n2, n2, s1, s2, kGemmTileRows,
-                       kGemmTileRows, st));
-
-  CUtensorMap a0, a1;
+  CUtensorMap a0, a1, b0, b1;
   if (gather_rows) MOE_TRY(encode_2d(&a0, true, x_perm, c.H, c.T, kTileK, 1));
   else MOE_TRY(encode_2d(&a0, true, x_perm, c.H, R, kTileK, kTileM));
   if (shared) MOE_TRY(encode_2d(&a1, true, x_shared, c.H, c.T, kTileK, kTileM));
   else a1 = a0;
+  MOE_TRY(encode_2d(&b0, true, h, c.I, R, kTileK, kTileM));
+  if (shared) MOE_TRY(encode_2d(&b1, true, hs, c.I_shared, c.T, kTileK, kTileM));
+  else b1 = b0;
+  // the plan kernel also writes each expert's A maps of both GEMMs with the row
+  // extent cut at the end of its rows (zeros past it; GemmArgs::amap)
+  uint8_t* cut = L.amap ? at<uint8_t*>(ws, L.amap) : nullptr;
+  trace_mark(st, MOE_K_PLAN);
+  MOE_CUDA(launch_plan(offsets, c.E, shared ? 1 : 0, c.T, n1r, n1s, n2, n2, s1, s2, kGemmTileRows,
+                       kGemmTileRows, st, &a0, &b0, cut));
+
   GemmArgs g1{};
   g1.b_maps = W.maps1;
   g1.layer = W.layer;
@@ -857,15 +865,13 @@ static moe_status_t run_ffn(const moe_config_t& c, const WeightView& W, const La
   g1.N_routed = c.I;
   g1.N_shared = c.I_shared;
   g1.stall_test = take_gemm1_stall() ? 1 : 0;
+  g1.amap = (cut && !gather_rows) ? cut : nullptr;
   const int grid = gemm_grid();
   trace_mark(st, MOE_K_GEMM1);
   MOE_CUDA(launch_grouped_gemm(true, a0, a1, g1, grid, st));
 
-  CUtensorMap b0, b1;
-  MOE_TRY(encode_2d(&b0, true, h, c.I, R, kTileK, kTileM));
-  if (shared) MOE_TRY(encode_2d(&b1, true, hs, c.I_shared, c.T, kTileK, kTileM));
-  else b1 = b0;
   GemmArgs g2 = g1;
+  g2.amap = cut ? cut + size_t(c.E) * 128 : nullptr;
   g2.stall_test = 0;
   g2.gather_rows = nullptr;
   g2.b_maps = W.maps2;

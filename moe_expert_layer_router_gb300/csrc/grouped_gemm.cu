@@ -235,6 +235,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // brings 128 rows, the MMA reads the first 64)
           const int a_row = x.row0 + x.m_blk * kPairRows +
                             int(rank) * (x.half ? kTileM / 2 : kTileM);
+          // A box rows past the end of the expert's rows (the MMA computes them,
+          // the epilogue discards them) come through the expert's copy of the A
+          // map whose row extent ends there (written by the plan kernel), so the
+          // TMA fills them with zeros: a product with zeros draws less power
+          // than one with the next expert's rows.
+          if (args.amap != nullptr && x.g < args.E && a_row + kTileM > x.row0 + x.rows) {
+            const uint8_t* cut = args.amap + size_t(x.g) * 128;
+            ptx::fence_tensormap_acquire(cut);
+            map_a = cut;
+          }
           const int kb_n = x.K / kTileK;
           bool ok = true;
           for (int kb = 0; kb < kb_n; ++kb, ++it) {

@@ -75,6 +75,8 @@ struct GemmArgs {
   int32_t K_routed, K_shared;  // reduction sizes
   int32_t N_routed, N_shared;  // output columns
   int32_t stall_test;          // failure-path test: pair 0 waits on a barrier nothing ends
+  const uint8_t* amap;         // [E] 128-byte A tensor maps, expert e's with its row extent
+                               // cut at offsets[e + 1] (written by the plan kernel), or null
 };
 
 // Failure-path test hook (moe_test_stall_gemm1): whether the next bf16 GEMM1
@@ -188,9 +190,14 @@ cudaError_t launch_scatter_nvfp4(const int32_t* ids, const float* topk_w, const 
 // device can hold at once.
 int grouped_gemm_grid(int sm_count);
 
+// With cut (bf16 layers: 2 E x 128 bytes, 128-byte aligned) the plan kernel also
+// writes each expert's copies of cut_a1 (GEMM1's A map) and cut_a2 (GEMM2's) with
+// the row extent cut at the end of the expert's rows (GemmArgs::amap).
 cudaError_t launch_plan(const int32_t* offsets, int E, int has_shared, int64_t T, int n1_routed,
                         int n1_shared, int n2_routed, int n2_shared, int32_t* sched1,
-                        int32_t* sched2, int tile_rows1, int tile_rows2, cudaStream_t stream);
+                        int32_t* sched2, int tile_rows1, int tile_rows2, cudaStream_t stream,
+                        const CUtensorMap* cut_a1 = nullptr, const CUtensorMap* cut_a2 = nullptr,
+                        uint8_t* cut = nullptr);
 
 cudaError_t launch_grouped_gemm_fp8(bool gate_up, const CUtensorMap& tok_map0,
                                     const CUtensorMap& tok_map1, const Fp8GemmArgs& args, int grid,

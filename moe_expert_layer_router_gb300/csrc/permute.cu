@@ -19,6 +19,8 @@
 //            blocks; each recomputes the ranks, the first writes the maps.
 #include <cuda_fp8.h>
 
+#include <cstring>
+
 #include "moe_internal.h"
 #include "nvfp4.cuh"
 #include "ptx.cuh"
@@ -414,12 +416,30 @@ __global__ void __launch_bounds__(kScatterThreads)
 // Tile schedules of GEMM1 and GEMM2 from the row offsets: per group
 // ceil(rows/tile_rows) x n_tiles tiles; groups ordered by descending tile count
 // (ties: lower group first) so the heaviest experts start first.
+// With `cut` (bf16 layers), also each expert's copies of the two GEMMs' A
+// tensor maps with the row extent cut at the end of its rows, offsets[e + 1]:
+// cut[e] from a1 (GEMM1), cut[E + e] from a2 (GEMM2).
 __global__ void __launch_bounds__(256)
     plan_kernel(const int32_t* __restrict__ offsets, int E, int has_shared, int64_t T,
                 int n1r, int n1s, int n2r, int n2s, int32_t* __restrict__ sched1,
-                int32_t* __restrict__ sched2, int tile_rows1, int tile_rows2) {
+                int32_t* __restrict__ sched2, int tile_rows1, int tile_rows2,
+                const __grid_constant__ CUtensorMap a1, const __grid_constant__ CUtensorMap a2,
+                uint8_t* __restrict__ cut) {
   __shared__ int tiles[2][kMaxGroups];
   __shared__ int order[2][kMaxGroups];
+  if (cut != nullptr) {
+    for (int i = threadIdx.x; i < 2 * E; i += blockDim.x) {
+      const int e = i < E ? i : i - E;
+      const uint4* src = reinterpret_cast<const uint4*>(i < E ? &a1 : &a2);
+      uint4* dst = reinterpret_cast<uint4*>(cut + size_t(i) * 128);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) dst[j] = src[j];
+      // (an expert with no rows has no tiles; its map still gets a nonzero extent)
+      const int32_t end = offsets[e + 1];
+      ptx::tensormap_set_extent<1>(dst, static_cast<uint32_t>(end > 0 ? end : 1));
+    }
+    ptx::fence_tensormap_release();
+  }
   const int G = E + has_shared;
   for (int g = threadIdx.x; g < G; g += blockDim.x) {
     const int64_t rows = g < E ? int64_t(offsets[g + 1]) - offsets[g] : T;
@@ -534,9 +554,15 @@ cudaError_t launch_scatter_nvfp4(const int32_t* ids, const float* topk_w, const 
 
 cudaError_t launch_plan(const int32_t* offsets, int E, int has_shared, int64_t T, int n1_routed,
                         int n1_shared, int n2_routed, int n2_shared, int32_t* sched1,
-                        int32_t* sched2, int tile_rows1, int tile_rows2, cudaStream_t stream) {
+                        int32_t* sched2, int tile_rows1, int tile_rows2, cudaStream_t stream,
+                        const CUtensorMap* cut_a1, const CUtensorMap* cut_a2, uint8_t* cut) {
+  CUtensorMap none;
+  memset(&none, 0, sizeof none);
+  const bool with_cut = cut != nullptr && cut_a1 != nullptr && cut_a2 != nullptr;
   plan_kernel<<<1, 256, 0, stream>>>(offsets, E, has_shared, T, n1_routed, n1_shared, n2_routed,
-                                     n2_shared, sched1, sched2, tile_rows1, tile_rows2);
+                                     n2_shared, sched1, sched2, tile_rows1, tile_rows2,
+                                     with_cut ? *cut_a1 : none, with_cut ? *cut_a2 : none,
+                                     with_cut ? cut : nullptr);
   return cudaGetLastError();
 }
 

@@ -77,6 +77,29 @@ __device__ __forceinline__ void prefetch_tmap(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Tensor maps edited on the device.  tensormap_set_extent replaces the extent
+// of dimension kDim of the 128-byte tensor map at `map` (global memory); the
+// release fence orders that and earlier writes of the map before the
+// tensor-map proxy's reads, and the acquire fence makes this thread's later
+// TMA copies through `map` see it.
+template <int kDim>
+__device__ __forceinline__ void tensormap_set_extent(void* map, uint32_t extent) {
+  asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], %1, %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "n"(kDim), "r"(extent)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_tensormap_release() {
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_tensormap_acquire(const void* map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(
+                   reinterpret_cast<uint64_t>(map))
+               : "memory");
+}
+
 // 2-D tiled load of the box at (c0 = innermost element index, c1 = row) into
 // shared memory, completing `bytes` of transaction count on `bar`.
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, uint64_t* bar, int32_t c0,
