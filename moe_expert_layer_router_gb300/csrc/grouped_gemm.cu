@@ -380,7 +380,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool valid = m < x.rows;
       const bool routed = x.g < args.E;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN;
-      if (kSwiGLU) {
+      if (m_base >= x.rows) {
+        // all 32 rows of this warp lie past the tile's rows: nothing to read or
+        // write (skipping the TMEM loads and the math saves power)
+      } else if (kSwiGLU) {
         // full tile: TMEM columns [g | u] of output columns 128 n + [0,64), then
         // [g | u] of 128 n + [64,128); half tile: one [g | u] block, the one of
         // CTA-half hs.  Each 32-column chunk: 32 rows x 64 B staged, then written
