@@ -838,11 +838,12 @@ static moe_status_t run_ffn(const moe_config_t& c, const WeightView& W, const La
   if (shared) MOE_TRY(encode_2d(&b1, true, hs, c.I_shared, c.T, kTileK, kTileM));
   else b1 = b0;
   // the plan kernel also writes each expert's A maps of both GEMMs with the row
-  // extent cut at the end of its rows (zeros past it; GemmArgs::amap)
-  uint8_t* cut = L.amap ? at<uint8_t*>(ws, L.amap) : nullptr;
+  // extent cut at the end of its rows (zeros past it; GemmArgs::amap); not on
+  // the fused-dispatch path, whose GEMM1 gathers rows from x
+  uint8_t* cut = (L.amap && !gather_rows) ? at<uint8_t*>(ws, L.amap) : nullptr;
   trace_mark(st, MOE_K_PLAN);
   MOE_CUDA(launch_plan(offsets, c.E, shared ? 1 : 0, c.T, n1r, n1s, n2, n2, s1, s2, kGemmTileRows,
-                       kGemmTileRows, st, &a0, &b0, cut));
+                       kGemmTileRows, st, &a0, &b0, cut, R));
 
   GemmArgs g1{};
   g1.b_maps = W.maps1;
@@ -865,7 +866,7 @@ static moe_status_t run_ffn(const moe_config_t& c, const WeightView& W, const La
   g1.N_routed = c.I;
   g1.N_shared = c.I_shared;
   g1.stall_test = take_gemm1_stall() ? 1 : 0;
-  g1.amap = (cut && !gather_rows) ? cut : nullptr;
+  g1.amap = cut;
   const int grid = gemm_grid();
   trace_mark(st, MOE_K_GEMM1);
   MOE_CUDA(launch_grouped_gemm(true, a0, a1, g1, grid, st));

@@ -192,12 +192,13 @@ int grouped_gemm_grid(int sm_count);
 
 // With cut (bf16 layers: 2 E x 128 bytes, 128-byte aligned) the plan kernel also
 // writes each expert's copies of cut_a1 (GEMM1's A map) and cut_a2 (GEMM2's) with
-// the row extent cut at the end of the expert's rows (GemmArgs::amap).
+// the row extent cut at the end of the expert's rows (GemmArgs::amap), never past
+// cut_rows (both templates' row extent).
 cudaError_t launch_plan(const int32_t* offsets, int E, int has_shared, int64_t T, int n1_routed,
                         int n1_shared, int n2_routed, int n2_shared, int32_t* sched1,
                         int32_t* sched2, int tile_rows1, int tile_rows2, cudaStream_t stream,
                         const CUtensorMap* cut_a1 = nullptr, const CUtensorMap* cut_a2 = nullptr,
-                        uint8_t* cut = nullptr);
+                        uint8_t* cut = nullptr, int64_t cut_rows = 0);
 
 cudaError_t launch_grouped_gemm_fp8(bool gate_up, const CUtensorMap& tok_map0,
                                     const CUtensorMap& tok_map1, const Fp8GemmArgs& args, int grid,

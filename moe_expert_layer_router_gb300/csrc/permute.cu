@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(256)
                 int n1r, int n1s, int n2r, int n2s, int32_t* __restrict__ sched1,
                 int32_t* __restrict__ sched2, int tile_rows1, int tile_rows2,
                 const __grid_constant__ CUtensorMap a1, const __grid_constant__ CUtensorMap a2,
-                uint8_t* __restrict__ cut) {
+                uint8_t* __restrict__ cut, int64_t cut_rows) {
   __shared__ int tiles[2][kMaxGroups];
   __shared__ int order[2][kMaxGroups];
   if (cut != nullptr) {
@@ -434,9 +434,12 @@ __global__ void __launch_bounds__(256)
       uint4* dst = reinterpret_cast<uint4*>(cut + size_t(i) * 128);
 #pragma unroll
       for (int j = 0; j < 8; ++j) dst[j] = src[j];
-      // (an expert with no rows has no tiles; its map still gets a nonzero extent)
-      const int32_t end = offsets[e + 1];
-      ptx::tensormap_set_extent<1>(dst, static_cast<uint32_t>(end > 0 ? end : 1));
+      // within [1, cut_rows], the templates' own extent: the cut never reaches
+      // past the buffer, whatever the offsets hold (an expert with no rows has
+      // no tiles; its map still gets a nonzero extent)
+      const int64_t end = offsets[e + 1];
+      const int64_t ext = end < 1 ? 1 : (end > cut_rows ? cut_rows : end);
+      ptx::tensormap_set_extent<1>(dst, static_cast<uint32_t>(ext));
     }
     ptx::fence_tensormap_release();
   }
@@ -555,14 +558,15 @@ cudaError_t launch_scatter_nvfp4(const int32_t* ids, const float* topk_w, const 
 cudaError_t launch_plan(const int32_t* offsets, int E, int has_shared, int64_t T, int n1_routed,
                         int n1_shared, int n2_routed, int n2_shared, int32_t* sched1,
                         int32_t* sched2, int tile_rows1, int tile_rows2, cudaStream_t stream,
-                        const CUtensorMap* cut_a1, const CUtensorMap* cut_a2, uint8_t* cut) {
+                        const CUtensorMap* cut_a1, const CUtensorMap* cut_a2, uint8_t* cut,
+                        int64_t cut_rows) {
   CUtensorMap none;
   memset(&none, 0, sizeof none);
-  const bool with_cut = cut != nullptr && cut_a1 != nullptr && cut_a2 != nullptr;
+  const bool with_cut = cut != nullptr && cut_a1 != nullptr && cut_a2 != nullptr && cut_rows > 0;
   plan_kernel<<<1, 256, 0, stream>>>(offsets, E, has_shared, T, n1_routed, n1_shared, n2_routed,
                                      n2_shared, sched1, sched2, tile_rows1, tile_rows2,
                                      with_cut ? *cut_a1 : none, with_cut ? *cut_a2 : none,
-                                     with_cut ? cut : nullptr);
+                                     with_cut ? cut : nullptr, cut_rows);
   return cudaGetLastError();
 }
 
