@@ -1,5 +1,6 @@
 """Host-side logic of bench.py (no GPU): the kernel source hash that ties a
-committed ncu summary to the sources it was captured on."""
+committed ncu summary to the sources it was captured on, and the reference
+arm's line."""
 import bench
 
 
@@ -22,3 +23,23 @@ def test_comment_edits_keep_the_hash_and_code_edits_change_it(tmp_path, monkeypa
     (csrc / "k.cu").write_text("// kernel\n__global__ void k(int* p) { p[0] = 2; }\n")
     assert bench.kernel_source_hash("test") != h0
 
+
+
+def test_reference_arm_line_on_the_host():
+    """--impl reference on a small workload, on the host: the oracle timed per
+    step on sampled tokens, with only the sampled tokens' experts generated."""
+    import argparse
+
+    import torch
+
+    import workload as wl
+
+    lc = wl.TINY.with_(T=64, H=256, E=8, k=2, I=128)
+    args = argparse.Namespace(ref_tokens=2, warmup=1, steps=2)
+    res = bench.run_reference(args, lc, 0, 1, torch.device("cpu"))
+    assert res["impl"] == "reference" and res["unit"] == "tokens/s" and res["value"] > 0
+    assert res["steps"] == 2 and res["warmup"] == 1 and res["higher_is_better"] is True
+    assert res["e2e"] == {"value": res["value"], "unit": "tokens/s",
+                          "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert res["cpu_baseline"]["kind"] == "oracle" and res["cpu_baseline"]["value"] == res["value"]
+    assert bench.run_reference(args, lc, 1, 2, torch.device("cpu")) is None  # rank > 0: no line
