@@ -40,14 +40,21 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// A thread whose phase has not completed is suspended until it does, or for
+// at most kWaitSuspendNs, instead of returning at once: waiting roles (the
+// epilogue warps through a tile, the producer on a full ring) then draw less
+// power, and the power-capped bf16 GEMMs run 3-4% faster (same process, both
+// orders; the waits end as soon as their phase completes).
+constexpr uint32_t kWaitSuspendNs = 200000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(kWaitSuspendNs)
       : "memory");
   return ok != 0;
 }
