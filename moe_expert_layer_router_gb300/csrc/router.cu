@@ -242,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bias = a.table.bias_table[l];
   }
 
-  for (int i = threadIdx.x; i < a.E_pad; i += kThreads) c.bias[i] = bias && i < a.E ? bias[i] : 0.0f;
+  for (int i = threadIdx.x; i < a.E_pad; i += kThreads)
+    c.bias[i] = bias && i < a.E ? bias[i] : 0.0f;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSt; ++s) {
       ptx::mbar_init(&c.full[s], 1);
