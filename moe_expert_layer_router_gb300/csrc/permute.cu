@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kScatterThreads)
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int cc = c0 + u * 32 + lane;
-            if (cc < c_hi) d4[cc] = v[u];
+            if (cc < c_hi) __stcs(d4 + cc, v[u]);  // streamed: x_perm (1.9 GB) outlives L2
           }
         }
       }
