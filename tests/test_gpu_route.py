@@ -24,6 +24,11 @@ CASES = [
     wl.TINY.with_(name="softmax_full", E=64, k=6, T=200, renormalize=False),
     wl.TINY.with_(name="k16", E=48, k=16, T=140, H=256),
     wl.TINY.with_(name="e40", E=40, k=5, T=300, H=512),                   # E_pad = 48: 8 padded columns
+    # more than one 128-token tile per SM pair: unsplit K; E_pad = 48 keeps single
+    # CTAs, E_pad = 64 runs CTA pairs (79 tiles, the last pair half past T)
+    wl.TINY.with_(name="unsplit_e40", E=40, k=5, T=10000, H=512),
+    wl.TINY.with_(name="pairs_softmax_full", E=64, k=6, T=10000, H=256, renormalize=False),
+    wl.TINY.with_(name="pairs_k16", E=64, k=16, T=10000, H=256, score="sigmoid"),
 ]
 
 
