@@ -32,6 +32,10 @@
 // output columns of the pair and lanes 64-127 the same rows' other 128, both in
 // TMEM columns 0-127.  Either way every epilogue thread owns one output row and
 // holds both the gate and the up value of each of its columns.
+// Rows of an A box past the tile's expert segment are loaded as zeros, through
+// the expert's copy of the A tensor map whose row extent the plan kernel cut
+// at the segment's end: the kernels run into the GPU's power cap, and products
+// with zeros draw less power than products with the next expert's rows.
 //
 // Warp roles per CTA (192 threads, one CTA per SM):
 //   warp 0      TMA producer (one lane), completing on the even CTA's barriers
