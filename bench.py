@@ -657,8 +657,6 @@ def stack_dispatch(args, lc, layer, dev):
                                 stream=torch.cuda.current_stream())
 
     def timed(fn, reps):
-        for _ in range(args.warmup):
-            fn()
         torch.cuda.synchronize(dev)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -666,15 +664,28 @@ def stack_dispatch(args, lc, layer, dev):
             fn()
         b.record(stream)
         torch.cuda.synchronize(dev)
-        return a.elapsed_time(b) / (reps * L)
+        return a.elapsed_time(b)
 
+    for _ in range(args.warmup):
+        direct()
+        graph.replay()
+    # Segments in the order direct, graph, graph, direct, ...: a power-capped
+    # GPU runs the first of two back-to-back measurements a few percent faster,
+    # so each way is measured first as often as second.
     reps = max(1, args.steps // L)
-    d_ms = timed(direct, reps)
-    g_ms = timed(graph.replay, reps)
+    segs = 4
+    tot = {"direct": 0.0, "graph": 0.0}
+    for i in range(segs):
+        pair = (("direct", direct), ("graph", graph.replay))
+        for name, fn in (pair if i % 2 == 0 else pair[::-1]):
+            tot[name] += timed(fn, reps)
     m.moe_get_device_error(ws)
-    return {"layers": L, "direct_ms_per_layer": d_ms, "graph_ms_per_layer": g_ms,
-            "how": f"{reps} rounds over {L} seeded layers on one input: moe_forward per layer "
-                   f"vs one CUDA graph of moe_forward_stack (layer index written on the device)"}
+    per = segs * reps * L
+    return {"layers": L, "direct_ms_per_layer": tot["direct"] / per,
+            "graph_ms_per_layer": tot["graph"] / per,
+            "how": f"{segs} segments of {reps} rounds each way, alternating which way runs "
+                   f"first, over {L} seeded layers on one input: moe_forward per layer vs "
+                   f"one CUDA graph of moe_forward_stack (layer index written on the device)"}
 
 
 # ------------------------------------------------------------------ reference arm
