@@ -94,12 +94,21 @@ constexpr size_t smem_bytes() {
   return 1024 + size_t(stages_of<kSwiGLU>()) * kStageBytes + 4 * kStageOutBytes + sizeof(SmemCtl);
 }
 
+// A group's tiles run in chunks of kChunkM m-tiles: all n-blocks of one chunk
+// (m-tiles of one n-block consecutive) before the next chunk.  A group with
+// many rows (the shared expert, whose rows are all T tokens, or a hot expert)
+// then keeps a few m-tiles of A in L2 while every n-block reads them, instead
+// of streaming all its rows once per n-block; groups of at most kChunkM m-tiles
+// run n-block by n-block as before.
+constexpr int kChunkM = 8;
+
 struct Tile {
   int g, m_blk, n_blk, rows, row0, K, N;
   bool half;  // at most 128 rows left: M=128 pair MMA, 64 rows per CTA
 };
 
-__device__ __forceinline__ Tile decode_tile(int t, const SmemCtl& c, const GemmArgs& a, int G) {
+__device__ __forceinline__ Tile decode_tile(int t, const SmemCtl& c, const GemmArgs& a, int G,
+                                            int tile_n) {
   const int32_t* ts = c.sched + 1;
   int lo = 0, hi = G - 1;
   while (lo < hi) {  // last slot whose first tile is <= t
@@ -115,8 +124,16 @@ __device__ __forceinline__ Tile decode_tile(int t, const SmemCtl& c, const GemmA
   x.K = routed ? a.K_routed : a.K_shared;
   x.N = routed ? a.N_routed : a.N_shared;
   const int mt = (x.rows + kPairRows - 1) / kPairRows;
-  x.n_blk = local / mt;
-  x.m_blk = local - x.n_blk * mt;
+  const int nt = (x.N + tile_n - 1) / tile_n;
+  const int full_chunks = mt / kChunkM;
+  int chunk = local / (kChunkM * nt), cm = kChunkM;
+  if (chunk >= full_chunks) {  // the last, partial chunk (the only one when mt < kChunkM)
+    chunk = full_chunks;
+    cm = mt - full_chunks * kChunkM;
+  }
+  const int r = local - chunk * kChunkM * nt;
+  x.n_blk = r / cm;
+  x.m_blk = chunk * kChunkM + (r - x.n_blk * cm);
   x.half = x.rows - x.m_blk * kPairRows <= kTileM;
   return x;
 }
@@ -185,6 +202,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int pair = blockIdx.x >> 1;
   const int num_pairs = gridDim.x >> 1;
   const int G = args.E + args.has_shared;
+  constexpr int kTileNOut = kSwiGLU ? kGemm1TileN : kGemm2TileN;  // output columns per tile
   // weight descriptors of this call's layer (layer stacks index their table)
   const CUtensorMap* bmaps =
       args.b_maps + resolve_layer(args.layer, args.num_layers, args.err) * args.layer_stride;
@@ -229,7 +247,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // tile loads: one lane issues everything
       if (lane == 0) {
         for (int t = pair; t < num_tiles && !*abort; t += num_pairs) {
-          const Tile x = decode_tile(t, c, args, G);
+          const Tile x = decode_tile(t, c, args, G, kTileNOut);
           const void* map_a = x.g < args.E ? static_cast<const void*>(&map_a0)
                                            : static_cast<const void*>(&map_a1);
           const CUtensorMap* mb;
@@ -269,7 +287,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // barrier decision and broadcasts it, so the warp never diverges.
       bool stop = false;
       for (int t = pair; t < num_tiles && !stop; t += num_pairs) {
-        const Tile x = decode_tile(t, c, args, G);
+        const Tile x = decode_tile(t, c, args, G, kTileNOut);
         const bool routed = x.g < args.E;
         const int cta_rows = x.half ? kTileM / 2 : kTileM;
         const void* map_a = routed ? static_cast<const void*>(&map_a0)
@@ -327,7 +345,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       int local = 0;
       for (int t = pair; t < num_tiles; t += num_pairs, ++local) {
-        const Tile x = decode_tile(t, c, args, G);
+        const Tile x = decode_tile(t, c, args, G, kTileNOut);
         const int acc = local & 1;
         const uint32_t acc_ph = (local >> 1) & 1;
         if (!ptx::mbar_wait(&c.tempty[acc], acc_ph ^ 1, abort, args.err)) break;
@@ -369,7 +387,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t tempty0 = ptx::mapa(ptx::smem_u32(&c.tempty[0]), 0);
     int local = 0;
     for (int t = pair; t < num_tiles; t += num_pairs, ++local) {
-      const Tile x = decode_tile(t, c, args, G);
+      const Tile x = decode_tile(t, c, args, G, kTileNOut);
       const int acc = local & 1;
       const uint32_t acc_ph = (local >> 1) & 1;
       if (!ptx::mbar_wait(&c.tfull[acc], acc_ph, abort, args.err)) break;
